@@ -1,0 +1,420 @@
+// Grouped NVFP4 block-scaled GEMM on the 5th-generation tensor cores.
+//
+//   D[m, n] = sum_k e2m1(A[m,k]) e4m3(SFA[m,k/16]) e2m1(B[n,k]) e4m3(SFB[n,k/16])
+//
+// with one fp32 accumulator tile of 128 x 128 in TMEM per output tile
+// (tcgen05.mma kind::mxf4nvf4, scale_vec::4X, K = 64 per instruction), operands
+// staged in shared memory by TMA (128-byte swizzle, 256 FP4 elements of K per
+// stage) and the block scales copied from shared memory to TMEM with
+// tcgen05.cp.  One persistent CTA per SM walks the tiles of all groups:
+//   warp 0      TMA producer (one lane): A box rows only as far as the group's
+//               live rows reach, B tile, A/B scale blocks (bulk copies);
+//   warp 1      MMA issuer (one lane), owns the TMEM allocation;
+//   warps 2..5  epilogue, one accumulator row per thread (TMEM lane quarters).
+// Two accumulator buffers let the epilogue of tile i overlap the main loop of
+// tile i+1.  Every wait is bounded (kPipelineTimeoutNs); a role that gives up
+// sets a shared abort flag, the others drain and the CTA frees TMEM and exits
+// with NVFP4_DEVERR_PIPELINE_TIMEOUT raised.
+//
+// Epilogues (the fused steps of the MoE expert path):
+//   kLinear  y = bf16(gs * ws2 * D)                       (Nvfp4Linear)
+//   kW13     h = SiLU(a * D_gate) * (a * D_up), a = gs * ws2_e, then h is
+//            re-quantised to NVFP4 with the static scale gs2_e into the
+//            permuted rows of the w2 input                 (gate/up projection)
+//   kW2      y_acc[t] += topk_w * gs2_e * ws2_e * D        (down projection,
+//            top-k weighted scatter-add in fp32)
+#include "common.cuh"
+
+namespace nvfp4 {
+
+namespace {
+
+struct Tile {
+  int g;       // group
+  int mt;      // m tile inside the group
+  int nt;      // n tile
+  int rows;    // live rows of this m tile (1..128)
+  int a_row0;  // first A row (permuted/padded row index)
+};
+
+__device__ __forceinline__ void decode_tile(const GemmArgs &a, int idx, int n_tiles, Tile &t) {
+  const int mtg = idx / n_tiles;
+  t.nt = idx - mtg * n_tiles;
+  if (a.counts == nullptr) {
+    t.g = 0;
+    t.mt = mtg;
+    t.rows = min(kBlockM, a.dense_M - mtg * kBlockM);
+    t.a_row0 = mtg * kBlockM;
+    return;
+  }
+  // largest g with tile_offsets[g] <= mtg (empty groups have equal neighbours)
+  int lo = 0, hi = a.G - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (__ldg(a.tile_offsets + mid) <= mtg)
+      lo = mid;
+    else
+      hi = mid - 1;
+  }
+  t.g = lo;
+  t.mt = mtg - __ldg(a.tile_offsets + lo);
+  t.rows = min(kBlockM, __ldg(a.counts + lo) - t.mt * kBlockM);
+  t.a_row0 = __ldg(a.pad_offsets + lo) + t.mt * kBlockM;
+}
+
+// instruction descriptor: E2M1 x E2M1, UE4M3 scales, K-major A and B, M=128, N=128
+constexpr uint32_t kIdesc = (1u << 7) | (1u << 10) | ((uint32_t(kBlockN) >> 3) << 17) |
+                            ((uint32_t(kBlockM) >> 4) << 24);
+
+__device__ __forceinline__ float silu_mul(float g, float u) { return g / (1.0f + expf(-g)) * u; }
+
+template <int kEpi>
+__global__ void __launch_bounds__(kGemmThreads, 1)
+    nvfp4_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
+                      const __grid_constant__ CUtensorMap tmB,
+                      const __grid_constant__ CUtensorMap tmBs, const GemmArgs args) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint8_t *sA = smem;
+  uint8_t *sB = sA + kStages * kTileBytesA;
+  uint8_t *sSFA = sB + kStages * kTileBytesB;
+  uint8_t *sSFB = sSFA + kStages * kSfBytesStage;
+  uint64_t *full = reinterpret_cast<uint64_t *>(sSFB + kStages * kSfBytesStage);
+  uint64_t *empty = full + kStages;
+  uint64_t *tfull = empty + kStages;
+  uint64_t *tempty = tfull + 2;
+  uint64_t *drain = tempty + 2;
+  uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(drain + 1);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_holder + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&tfull[i], 1);
+      mbar_init(&tempty[i], 4);
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+    fence_proxy_async_shared();
+  }
+  if (warp == 0 && lane == 0) {
+    prefetch_tensormap(&tmA);
+    prefetch_tensormap(&tmB);
+    if (args.shared_group >= 0) prefetch_tensormap(&tmBs);
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_holder, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_holder;
+
+  const int n_tiles = args.N / kBlockN;
+  const int k_steps = args.K / kUmmaK;
+  const int k_stages = (k_steps + 3) / 4;
+  const int total_mtiles = args.counts ? __ldg(args.tile_offsets + args.G)
+                                       : (args.dense_M + kBlockM - 1) / kBlockM;
+  const int total_tiles = total_mtiles * n_tiles;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ------------------------------------------------------------ TMA producer
+      const uint64_t pol_w = policy_evict_first();  // weights stream through once
+      const uint64_t pol_a = policy_evict_last();   // activations are re-read per n tile
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t issued = 0;  // bit s: stage s has a load in flight with parity bit (s+8)
+      bool ok = true;
+      for (int idx = blockIdx.x; ok && idx < total_tiles; idx += gridDim.x) {
+        Tile t;
+        decode_tile(args, idx, n_tiles, t);
+        const bool sh = t.g == args.shared_group;
+        const CUtensorMap *mb = sh ? &tmBs : &tmB;
+        const int b_row0 = (sh ? 0 : t.g * args.N) + t.nt * kBlockN;
+        const uint8_t *sfb =
+            (sh ? args.b_sf_shared
+                : args.b_sf + static_cast<size_t>(t.g) * args.N * (args.K / 16)) +
+            static_cast<size_t>(t.nt) * k_steps * kSfBytesPerKStep;
+        const uint8_t *sfa =
+            args.a_sf + static_cast<size_t>(t.a_row0 / kBlockM) * k_steps * kSfBytesPerKStep;
+        const int nbox = (t.rows + kABoxRows - 1) / kABoxRows;
+        for (int ks = 0; ks < k_stages; ++ks) {
+          const int kv = min(4, k_steps - 4 * ks);
+          if (!mbar_wait_bounded(&empty[stage], phase ^ 1, abort_flag, args.err,
+                                 kPipelineTimeoutNs)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&full[stage], nbox * (kABoxRows * kStageK / 2) + kTileBytesB +
+                                                  2 * kv * kSfBytesPerKStep);
+          uint8_t *a_dst = sA + stage * kTileBytesA;
+          for (int b = 0; b < nbox; ++b)
+            tma_load_2d(a_dst + b * (kABoxRows * kStageK / 2), &tmA, ks * (kStageK / 2),
+                        t.a_row0 + b * kABoxRows, &full[stage], pol_a);
+          tma_load_2d(sB + stage * kTileBytesB, mb, ks * (kStageK / 2), b_row0, &full[stage],
+                      pol_w);
+          bulk_load(sSFA + stage * kSfBytesStage, sfa + static_cast<size_t>(ks) * kSfBytesStage,
+                    kv * kSfBytesPerKStep, &full[stage], pol_a);
+          bulk_load(sSFB + stage * kSfBytesStage, sfb + static_cast<size_t>(ks) * kSfBytesStage,
+                    kv * kSfBytesPerKStep, &full[stage], pol_w);
+          issued = (issued & ~(0x101u << stage)) | (1u << stage) | (phase << (stage + 8));
+          if (++stage == kStages) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+      }
+      if (!ok) {
+        // let the copies already in flight land before the CTA leaves (this wait
+        // ignores the abort flag; it is bounded by its own 100 ms limit)
+        volatile int never = 0;
+        for (int s = 0; s < kStages; ++s)
+          if (issued & (1u << s))
+            mbar_wait_bounded(&full[s], (issued >> (s + 8)) & 1u, &never, nullptr, 100000000ull);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ------------------------------------------------------------ MMA issuer
+      int stage = 0;
+      uint32_t phase = 0;
+      int it = 0;
+      bool ok = true;
+      const uint32_t sA0 = smem_u32(sA), sB0 = smem_u32(sB);
+      const uint32_t sSFA0 = smem_u32(sSFA), sSFB0 = smem_u32(sSFB);
+      for (int idx = blockIdx.x; ok && idx < total_tiles; idx += gridDim.x, ++it) {
+        const int acc = it & 1;
+        const uint32_t acc_phase = (it >> 1) & 1;
+        if (!mbar_wait_bounded(&tempty[acc], acc_phase ^ 1, abort_flag, args.err,
+                               kPipelineTimeoutNs)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + acc * kBlockN;
+        for (int ks = 0; ks < k_stages; ++ks) {
+          const int kv = min(4, k_steps - 4 * ks);
+          if (!mbar_wait_bounded(&full[stage], phase, abort_flag, args.err,
+                                 kPipelineTimeoutNs)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sf_col = tmem_base + kTmemAccCols + stage * kTmemSfCols;
+          for (int j = 0; j < kv; ++j) {
+            tc_cp_sf(sf_col + j * 4,
+                     smem_desc(sSFA0 + stage * kSfBytesStage + j * kSfBytesPerKStep, 0, 128, 0));
+            tc_cp_sf(sf_col + 16 + j * 4,
+                     smem_desc(sSFB0 + stage * kSfBytesStage + j * kSfBytesPerKStep, 0, 128, 0));
+          }
+          const uint64_t adesc = smem_desc(sA0 + stage * kTileBytesA, 16, 1024, 2);
+          const uint64_t bdesc = smem_desc(sB0 + stage * kTileBytesB, 16, 1024, 2);
+          for (int j = 0; j < kv; ++j) {
+            // +32 bytes of K per step inside the 128-byte swizzle row (descriptor units of 16 B)
+            tc_mma_nvf4(d_tmem, adesc + 2 * j, bdesc + 2 * j, kIdesc, sf_col + j * 4,
+                        sf_col + 16 + j * 4, (ks | j) != 0);
+          }
+          tc_commit(&empty[stage]);
+          if (++stage == kStages) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+        if (!ok) break;
+        tc_commit(&tfull[acc]);
+      }
+      // every MMA this thread issued has completed before TMEM is released
+      volatile int never = 0;
+      tc_commit(drain);
+      mbar_wait_bounded(drain, 0, &never, nullptr, 100000000ull);
+    }
+  } else {
+    // -------------------------------------------------------------- epilogue
+    const int quarter = warp & 3;  // TMEM lanes [32*quarter, 32*quarter + 32)
+    const int m = quarter * 32 + lane;
+    const float gs_scalar = (kEpi == static_cast<int>(Epi::kW2)) ? 0.f : __ldg(args.gs_a);
+    int it = 0;
+    for (int idx = blockIdx.x; idx < total_tiles; idx += gridDim.x, ++it) {
+      Tile t;
+      decode_tile(args, idx, n_tiles, t);
+      const int acc = it & 1;
+      const uint32_t acc_phase = (it >> 1) & 1;
+      bool ok = mbar_wait_bounded(&tfull[acc], acc_phase, abort_flag, args.err,
+                                  kPipelineTimeoutNs);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+      tc_fence_after();
+      const uint32_t tbase = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
+                             static_cast<uint32_t>(acc * kBlockN);
+      const bool row_ok = m < t.rows;
+      const bool sh = t.g == args.shared_group;
+      const float ws2 = sh ? __ldg(args.ws2_shared) : __ldg(args.ws2 + t.g);
+
+      if constexpr (kEpi == static_cast<int>(Epi::kLinear)) {
+        const float alpha = gs_scalar * ws2;
+        const int64_t row = t.a_row0 + m;
+        __nv_bfloat16 *y = static_cast<__nv_bfloat16 *>(args.out) +
+                           row * static_cast<int64_t>(args.out_ld) + t.nt * kBlockN;
+#pragma unroll 1
+        for (int c = 0; c < kBlockN / 16; ++c) {
+          uint32_t r[16];
+          tmem_ld16(tbase + c * 16, r);
+          tmem_ld_wait();
+          if (row_ok) {
+            uint32_t packed[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              const __nv_bfloat162 v = __floats2bfloat162_rn(
+                  __uint_as_float(r[2 * i]) * alpha, __uint_as_float(r[2 * i + 1]) * alpha);
+              packed[i] = *reinterpret_cast<const uint32_t *>(&v);
+            }
+            uint4 *dst = reinterpret_cast<uint4 *>(y + c * 16);
+            dst[0] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+            dst[1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
+          }
+        }
+      } else if constexpr (kEpi == static_cast<int>(Epi::kW13)) {
+        const float alpha = gs_scalar * ws2;
+        const float gs2 = __ldg(args.gs_out + t.g);
+        const float six_gs2 = __fmul_rn(6.0f, gs2);
+        const int64_t p = t.a_row0 + m;
+        const int I = args.out_ld * 2;
+        uint32_t codes[8];
+        uint32_t sfw = 0;
+#pragma unroll 1
+        for (int c = 0; c < 4; ++c) {
+          uint32_t rg[16], ru[16];
+          tmem_ld16(tbase + c * 16, rg);
+          tmem_ld16(tbase + kBlockN / 2 + c * 16, ru);
+          tmem_ld_wait();
+          float h[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i)
+            h[i] = silu_mul(__uint_as_float(rg[i]) * alpha, __uint_as_float(ru[i]) * alpha);
+          if (args.h_debug != nullptr && row_ok) {
+            float4 *hd = reinterpret_cast<float4 *>(args.h_debug + p * I + t.nt * 64 + c * 16);
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+              hd[i] = make_float4(h[4 * i], h[4 * i + 1], h[4 * i + 2], h[4 * i + 3]);
+          }
+          uint32_t cw[2];
+          const uint32_t sfb = encode_block16(h, gs2, six_gs2, cw);
+          codes[2 * c] = cw[0];
+          codes[2 * c + 1] = cw[1];
+          sfw |= sfb << (8 * c);
+        }
+        if (row_ok) {
+          uint4 *dst = reinterpret_cast<uint4 *>(static_cast<uint8_t *>(args.out) +
+                                                 p * args.out_ld + t.nt * 32);
+          dst[0] = make_uint4(codes[0], codes[1], codes[2], codes[3]);
+          dst[1] = make_uint4(codes[4], codes[5], codes[6], codes[7]);
+          *reinterpret_cast<uint32_t *>(args.out_sf + sf_word_offset(p, t.nt, I / 64)) = sfw;
+        }
+      } else {  // kW2
+        float scale = 0.f;
+        int64_t tok = 0;
+        if (row_ok) {
+          const int seg_row = t.mt * kBlockM + m;
+          float w = 1.f;
+          if (sh) {
+            tok = seg_row;
+          } else {
+            const int f = __ldg(args.sorted_idx + __ldg(args.offsets + t.g) + seg_row);
+            tok = f / args.topk;
+            w = __ldg(args.topk_w + f);
+          }
+          scale = __ldg(args.gs_a + t.g) * ws2 * w;
+        }
+        float4 *dst = reinterpret_cast<float4 *>(static_cast<float *>(args.out) +
+                                                 tok * args.out_ld + t.nt * kBlockN);
+#pragma unroll 1
+        for (int c = 0; c < kBlockN / 16; ++c) {
+          uint32_t r[16];
+          tmem_ld16(tbase + c * 16, r);
+          tmem_ld_wait();
+          if (row_ok) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+              atomicAdd(dst + c * 4 + i,
+                        make_float4(__uint_as_float(r[4 * i]) * scale,
+                                    __uint_as_float(r[4 * i + 1]) * scale,
+                                    __uint_as_float(r[4 * i + 2]) * scale,
+                                    __uint_as_float(r[4 * i + 3]) * scale));
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&tempty[acc]);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem_base, kTmemCols);
+}
+
+// Bounded-wait probe: one thread waits on a barrier that never completes.
+__global__ void wait_timeout_probe_kernel(uint64_t timeout_ns, uint32_t *err) {
+  __shared__ uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    abort_flag = 0;
+    fence_barrier_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    const bool done = mbar_wait_bounded(&bar, 0, &abort_flag, err, timeout_ns);
+    if (done) raise_device_error(err, 0x80000000u);  // impossible: nothing arrives
+  }
+}
+
+template <int kEpi>
+cudaError_t launch_gemm_t(const CUtensorMap &ta, const CUtensorMap &tb, const CUtensorMap &tbs,
+                          const GemmArgs &args, int grid, cudaStream_t s) {
+  static bool attr_done[64] = {false};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 64 && !attr_done[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(nvfp4_gemm_kernel<kEpi>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(kGemmSmemBytes));
+    if (e != cudaSuccess) return e;
+    attr_done[dev] = true;
+  }
+  nvfp4_gemm_kernel<kEpi><<<grid, kGemmThreads, kGemmSmemBytes, s>>>(ta, tb, tbs, args);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_gemm(Epi epi, const CUtensorMap &ta, const CUtensorMap &tb,
+                        const CUtensorMap &tbs, const GemmArgs &args, int grid, cudaStream_t s) {
+  switch (epi) {
+    case Epi::kLinear:
+      return launch_gemm_t<static_cast<int>(Epi::kLinear)>(ta, tb, tbs, args, grid, s);
+    case Epi::kW13:
+      return launch_gemm_t<static_cast<int>(Epi::kW13)>(ta, tb, tbs, args, grid, s);
+    case Epi::kW2:
+      return launch_gemm_t<static_cast<int>(Epi::kW2)>(ta, tb, tbs, args, grid, s);
+  }
+  return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_wait_timeout_probe(uint32_t timeout_us, uint32_t *err, cudaStream_t s) {
+  wait_timeout_probe_kernel<<<1, 32, 0, s>>>(static_cast<uint64_t>(timeout_us) * 1000ull, err);
+  return cudaGetLastError();
+}
+
+}  // namespace nvfp4

@@ -1,0 +1,98 @@
+// Internal declarations shared by the translation units of the library (not part of the ABI).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "../../include/nvfp4.h"
+
+namespace nvfp4 {
+
+constexpr int kMaxPartials = 1024;      // block-max partials of the amax reduction
+constexpr int kMaxExperts = 1024;       // routing limit (E)
+constexpr int kMaxTopk = 32;
+constexpr uint64_t kPipelineTimeoutNs = 2000000000ull;  // 2 s: no healthy wait comes close
+
+// GEMM tile geometry (one CTA per SM, persistent).
+constexpr int kBlockM = 128;            // UMMA M
+constexpr int kBlockN = 128;            // UMMA N and output tile width
+constexpr int kStageK = 256;            // FP4 elements per pipeline stage (128 bytes per row)
+constexpr int kUmmaK = 64;              // K per tcgen05.mma (kind::mxf4nvf4, scale_vec::4X)
+constexpr int kStages = 6;
+constexpr int kABoxRows = 32;           // A rows per TMA box (only boxes with live rows load)
+constexpr int kTileBytesA = kBlockM * kStageK / 2;   // 16 KiB
+constexpr int kTileBytesB = kBlockN * kStageK / 2;   // 16 KiB
+constexpr int kSfBytesPerKStep = 512;   // 128 rows x 4 scales
+constexpr int kSfBytesStage = kSfBytesPerKStep * (kStageK / kUmmaK);  // 2 KiB
+constexpr int kGemmThreads = 192;       // warp 0 TMA, warp 1 MMA, warps 2..5 epilogue
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kTmemAccCols = 2 * kBlockN;       // two accumulator buffers
+constexpr uint32_t kTmemSfCols = 32;                 // per stage: 16 SFA + 16 SFB columns
+
+constexpr size_t kGemmSmemBytes =
+    1024 /* alignment slack */ +
+    static_cast<size_t>(kStages) * (kTileBytesA + kTileBytesB + 2 * kSfBytesStage) +
+    256 /* barriers and flags */;
+
+enum class Epi : int { kLinear = 0, kW13 = 1, kW2 = 2 };
+
+struct GemmArgs {
+  // problem
+  int G;              // groups (1 for a dense GEMM)
+  int N;              // output width per group, multiple of 128
+  int K;              // reduction length, multiple of 64
+  int dense_M;        // rows of a dense GEMM (counts == nullptr)
+  // grouped segments (device arrays written by the routing kernel)
+  const int *counts;        // [G]
+  const int *offsets;       // [G+1] unpadded (sorted order)
+  const int *pad_offsets;   // [G+1]
+  const int *tile_offsets;  // [G+1]
+  int shared_group;         // group using the *_shared weights, or -1
+  // scale factors
+  const uint8_t *a_sf;      // swizzled, 128-row blocks aligned with the A rows
+  const uint8_t *b_sf;      // G blocks of N*K/16 bytes
+  const uint8_t *b_sf_shared;
+  // epilogue
+  const float *gs_a;        // activation global scale (device scalar)
+  const float *ws2;         // per-group weight scale (G entries, or 1 for dense)
+  const float *ws2_shared;  // shared-expert weight scale
+  const float *gs_out;      // W13: static global scale of h per group (G entries)
+  void *out;                // Linear: bf16 y (dense_M, N); W13: hq codes; W2: fp32 y_acc
+  uint8_t *out_sf;          // W13: hsf (swizzled)
+  float *h_debug;           // W13 optional fp32 h
+  int out_ld;               // Linear: N; W13: I/2 bytes; W2: H floats
+  const int *sorted_idx;    // W2
+  const float *topk_w;      // W2
+  int topk;                 // W2
+  uint32_t *err;            // device fault flags
+};
+
+// launchers (return cudaError_t of the launch)
+cudaError_t launch_amax_partials(const void *x, int64_t M, int64_t K, int64_t ldx,
+                                 uint32_t *partials, int nparts, cudaStream_t s);
+int amax_partial_count(int64_t M, int64_t K);
+cudaError_t launch_quantize(const void *x, int64_t M, int64_t K, int64_t ldx,
+                            const uint32_t *partials, int nparts, const float *gs_static,
+                            float *gs_out, uint8_t *q, uint8_t *sf, int sf_layout,
+                            cudaStream_t s);
+cudaError_t launch_prepare(const uint8_t *w, const uint8_t *sf, int64_t G, int64_t N, int64_t K,
+                           int flags, uint8_t *w_out, uint8_t *sf_out, cudaStream_t s);
+
+struct RouteBufs {
+  int *counts, *offsets, *pad_offsets, *tile_offsets, *sorted_idx, *inv_idx;
+};
+cudaError_t launch_route_amax(const int32_t *ids, int T, int topk, int E, int has_shared,
+                              RouteBufs rb, const void *x, int64_t H, uint32_t *partials,
+                              int nparts, float *y_acc, uint32_t *err, cudaStream_t s);
+cudaError_t launch_dispatch_quant(const void *x, int T, int64_t H, int topk, int E,
+                                  int has_shared, const int32_t *ids, RouteBufs rb,
+                                  const uint32_t *partials, int nparts, const float *gs_static,
+                                  float *gs_out, uint8_t *xq, uint8_t *xsf, cudaStream_t s);
+cudaError_t launch_finalize(const float *y_acc, int64_t n, void *y, cudaStream_t s);
+cudaError_t launch_gemm(Epi epi, const CUtensorMap &ta, const CUtensorMap &tb,
+                        const CUtensorMap &tbs, const GemmArgs &args, int grid, cudaStream_t s);
+cudaError_t launch_wait_timeout_probe(uint32_t timeout_us, uint32_t *err, cudaStream_t s);
+
+}  // namespace nvfp4

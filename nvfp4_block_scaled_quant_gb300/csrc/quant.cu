@@ -1,0 +1,183 @@
+// Activation quantisation (amax reduction + NVFP4 block encoding) and the one-time
+// weight prepare step (scale swizzle, gate/up row interleave).
+//
+// Both are HBM-bound streams: 16-byte vector loads along K, one thread per
+// 16-element scale block, the four scale bytes of one 64-element group gathered
+// with warp shuffles into one 32-bit store of the tensor-core layout.
+#include "common.cuh"
+
+namespace nvfp4 {
+
+namespace {
+
+constexpr int kAmaxThreads = 256;
+constexpr int kQuantThreads = 256;
+
+__device__ __forceinline__ uint32_t max_abs_bf16x2(uint32_t w) {
+  // |bf16| compares like an unsigned integer once the sign bit is cleared
+  return max(w & 0x7FFFu, (w >> 16) & 0x7FFFu);
+}
+
+__device__ __forceinline__ uint32_t block_reduce_max(uint32_t v, uint32_t *scratch) {
+#pragma unroll
+  for (int o = 16; o; o >>= 1) v = max(v, __shfl_xor_sync(0xffffffffu, v, o));
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (lane == 0) scratch[warp] = v;
+  __syncthreads();
+  if (warp == 0) {
+    v = lane < static_cast<int>(blockDim.x >> 5) ? scratch[lane] : 0u;
+#pragma unroll
+    for (int o = 16; o; o >>= 1) v = max(v, __shfl_xor_sync(0xffffffffu, v, o));
+    if (lane == 0) scratch[0] = v;
+  }
+  __syncthreads();
+  return scratch[0];
+}
+
+// Block partial maxima of |x| (as bf16 bit patterns).  Block b reduces rows
+// b, b + gridDim.x, ...
+__global__ void __launch_bounds__(kAmaxThreads) amax_partials_kernel(const uint16_t *__restrict__ x,
+                                                                     int64_t M, int64_t K,
+                                                                     int64_t ldx,
+                                                                     uint32_t *__restrict__ partials) {
+  __shared__ uint32_t scratch[32];
+  const int64_t chunks = K / 8;
+  uint32_t m = 0;
+  for (int64_t r = blockIdx.x; r < M; r += gridDim.x) {
+    const uint4 *row = reinterpret_cast<const uint4 *>(x + r * ldx);
+    for (int64_t c = threadIdx.x; c < chunks; c += blockDim.x) {
+      const uint4 v = __ldg(row + c);
+      m = max(m, max(max(max_abs_bf16x2(v.x), max_abs_bf16x2(v.y)),
+                     max(max_abs_bf16x2(v.z), max_abs_bf16x2(v.w))));
+    }
+  }
+  m = block_reduce_max(m, scratch);
+  if (threadIdx.x == 0) partials[blockIdx.x] = m;
+}
+
+// One thread per 16-element block of a (M, K) bf16 tensor.  Swizzled output
+// also covers the padding rows up to a multiple of 128 (scale 0, no codes).
+__global__ void __launch_bounds__(kQuantThreads) quantize_kernel(
+    const uint16_t *__restrict__ x, int64_t M, int64_t K, int64_t ldx,
+    const uint32_t *__restrict__ partials, int nparts, const float *__restrict__ gs_static,
+    float *__restrict__ gs_out, uint8_t *__restrict__ q, uint8_t *__restrict__ sf,
+    int sf_layout, int64_t rows_total) {
+  __shared__ uint32_t scratch[32];
+  float gs;
+  if (partials) {
+    gs = gs_from_partials(partials, nparts, scratch);
+    if (blockIdx.x == 0 && threadIdx.x == 0) *gs_out = gs;
+  } else {
+    gs = *gs_static;
+  }
+  const float six_gs = __fmul_rn(6.0f, gs);
+  const int64_t kb = K / 16;
+  const int64_t gb = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const bool valid = gb < rows_total * kb;
+  const int64_t r = valid ? gb / kb : 0;
+  const int64_t c = valid ? gb - r * kb : 0;
+  const bool live = valid && r < M;
+  uint32_t sfb = 0;
+  if (live) {
+    const uint4 *src = reinterpret_cast<const uint4 *>(x + r * ldx + c * 16);
+    const uint4 a = __ldg(src), b = __ldg(src + 1);
+    const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+    float v[16];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      v[2 * i] = __uint_as_float(w[i] << 16);
+      v[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+    }
+    uint32_t codes[2];
+    sfb = encode_block16(v, gs, six_gs, codes);
+    *reinterpret_cast<uint2 *>(q + r * (K / 2) + c * 8) = make_uint2(codes[0], codes[1]);
+  }
+  if (sf_layout == NVFP4_SF_LINEAR) {
+    if (live) sf[r * kb + c] = static_cast<uint8_t>(sfb);
+  } else {
+    // lanes 4i..4i+3 hold the scale columns 4c'..4c'+3 of one row (kb % 4 == 0)
+    const int lane = threadIdx.x & 31;
+    uint32_t word = sfb << ((lane & 3) * 8);
+    word |= __shfl_xor_sync(0xffffffffu, word, 1);
+    word |= __shfl_xor_sync(0xffffffffu, word, 2);
+    if (valid && (lane & 3) == 0)
+      *reinterpret_cast<uint32_t *>(sf + sf_word_offset(r, c >> 2, kb >> 2)) = word;
+  }
+}
+
+// Prepared weight layout.  Codes: 16-byte chunks, row permuted for the w13
+// interleave.  Scales: one 32-bit word (4 scales) per thread, written in the
+// swizzled layout.
+__device__ __forceinline__ int64_t interleave_src_row(int64_t n, int64_t N, int flags) {
+  if (!(flags & NVFP4_PREP_W13_INTERLEAVE)) return n;
+  const int64_t tile = n >> 7, j = n & 127;
+  return j < 64 ? tile * 64 + j : N / 2 + tile * 64 + (j - 64);
+}
+
+__global__ void prepare_kernel(const uint8_t *__restrict__ w, const uint8_t *__restrict__ sf,
+                               int64_t G, int64_t N, int64_t K, int flags,
+                               uint8_t *__restrict__ w_out, uint8_t *__restrict__ sf_out) {
+  const int64_t row_chunks = K / 32;              // 16-byte chunks per packed row
+  const int64_t code_items = G * N * row_chunks;
+  const int64_t words_per_group = N * K / 64;     // 4 scales per word
+  const int64_t total = code_items + G * words_per_group;
+  const int64_t kb = K / 16, kc4 = K / 64;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    if (i < code_items) {
+      const int64_t row = i / row_chunks, ch = i - row * row_chunks;
+      const int64_t g = row / N, n = row - g * N;
+      const int64_t src = g * N + interleave_src_row(n, N, flags);
+      reinterpret_cast<uint4 *>(w_out + row * (K / 2))[ch] =
+          __ldg(reinterpret_cast<const uint4 *>(w + src * (K / 2)) + ch);
+    } else {
+      const int64_t j = i - code_items;
+      const int64_t g = j / words_per_group, wi = j - g * words_per_group;
+      const int64_t blk = wi >> 7, within = wi & 127;
+      const int64_t rb = blk / kc4, cb = blk - rb * kc4;
+      const int64_t r = rb * 128 + (within & 3) * 32 + (within >> 2);
+      const int64_t src = g * N + interleave_src_row(r, N, flags);
+      const uint32_t word = __ldg(reinterpret_cast<const uint32_t *>(sf + src * kb + cb * 4));
+      reinterpret_cast<uint32_t *>(sf_out + g * (N * kb))[wi] = word;
+    }
+  }
+}
+
+}  // namespace
+
+int amax_partial_count(int64_t M, int64_t K) {
+  (void)K;
+  if (M <= 0) return 1;
+  return static_cast<int>(M < kMaxPartials ? M : kMaxPartials);
+}
+
+cudaError_t launch_amax_partials(const void *x, int64_t M, int64_t K, int64_t ldx,
+                                 uint32_t *partials, int nparts, cudaStream_t s) {
+  amax_partials_kernel<<<nparts, kAmaxThreads, 0, s>>>(static_cast<const uint16_t *>(x), M, K,
+                                                       ldx, partials);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_quantize(const void *x, int64_t M, int64_t K, int64_t ldx,
+                            const uint32_t *partials, int nparts, const float *gs_static,
+                            float *gs_out, uint8_t *q, uint8_t *sf, int sf_layout,
+                            cudaStream_t s) {
+  const int64_t rows_total = sf_layout == NVFP4_SF_LINEAR ? M : ((M + 127) / 128) * 128;
+  const int64_t items = rows_total * (K / 16);
+  const int64_t blocks = items > 0 ? (items + kQuantThreads - 1) / kQuantThreads : 1;
+  quantize_kernel<<<static_cast<unsigned>(blocks), kQuantThreads, 0, s>>>(
+      static_cast<const uint16_t *>(x), M, K, ldx, partials, nparts, gs_static, gs_out, q, sf,
+      sf_layout, rows_total);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_prepare(const uint8_t *w, const uint8_t *sf, int64_t G, int64_t N, int64_t K,
+                           int flags, uint8_t *w_out, uint8_t *sf_out, cudaStream_t s) {
+  int dev = 0, sms = 148;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  prepare_kernel<<<sms * 8, 256, 0, s>>>(w, sf, G, N, K, flags, w_out, sf_out);
+  return cudaGetLastError();
+}
+
+}  // namespace nvfp4

@@ -1,0 +1,288 @@
+// MoE routing (histogram, scans, stable permutation), the dispatch step that
+// quantises each token once and writes its codes into the row of every expert
+// segment it is routed to, and the final fp32 -> bf16 conversion.
+#include "common.cuh"
+
+namespace nvfp4 {
+
+namespace {
+
+constexpr int kRouteThreads = 512;
+constexpr int kDispatchThreads = 256;
+
+// Block-wide exclusive scan of three int sequences of length n (n <= 4 * blockDim).
+// Writes out_x[0..n] (n+1 entries, the last one the total; n >= 1); out_pad and
+// out_tiles may be null.
+__device__ void block_scan3(const int *in_count, int n, int *out_off, int *out_pad,
+                            int *out_tiles, int *tmp /* 3 * 32 ints */) {
+  const int per = (n + blockDim.x - 1) / blockDim.x;  // <= 4
+  const int lo = threadIdx.x * per;
+  int s0 = 0, s1 = 0, s2 = 0;
+  for (int i = 0; i < per; ++i) {
+    const int idx = lo + i;
+    if (idx < n) {
+      const int c = in_count[idx];
+      s0 += c;
+      s1 += (c + 127) & ~127;
+      s2 += (c + 127) >> 7;
+    }
+  }
+  // inclusive warp scan of the thread sums
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int i0 = s0, i1 = s1, i2 = s2;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int a = __shfl_up_sync(0xffffffffu, i0, o), b = __shfl_up_sync(0xffffffffu, i1, o),
+              c = __shfl_up_sync(0xffffffffu, i2, o);
+    if (lane >= o) {
+      i0 += a;
+      i1 += b;
+      i2 += c;
+    }
+  }
+  if (lane == 31) {
+    tmp[warp] = i0;
+    tmp[32 + warp] = i1;
+    tmp[64 + warp] = i2;
+  }
+  __syncthreads();
+  if (warp == 0) {
+    const int nw = blockDim.x >> 5;
+    int a = lane < nw ? tmp[lane] : 0, b = lane < nw ? tmp[32 + lane] : 0,
+        c = lane < nw ? tmp[64 + lane] : 0;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int x = __shfl_up_sync(0xffffffffu, a, o), y = __shfl_up_sync(0xffffffffu, b, o),
+                z = __shfl_up_sync(0xffffffffu, c, o);
+      if (lane >= o) {
+        a += x;
+        b += y;
+        c += z;
+      }
+    }
+    if (lane < nw) {  // exclusive prefix of the warp totals
+      tmp[lane] = a - tmp[lane];
+      tmp[32 + lane] = b - tmp[32 + lane];
+      tmp[64 + lane] = c - tmp[64 + lane];
+    }
+  }
+  __syncthreads();
+  int e0 = tmp[warp] + i0 - s0, e1 = tmp[32 + warp] + i1 - s1, e2 = tmp[64 + warp] + i2 - s2;
+  for (int i = 0; i < per; ++i) {
+    const int idx = lo + i;
+    if (idx < n) {
+      out_off[idx] = e0;
+      if (out_pad) out_pad[idx] = e1;
+      if (out_tiles) out_tiles[idx] = e2;
+      const int c = in_count[idx];
+      e0 += c;
+      e1 += (c + 127) & ~127;
+      e2 += (c + 127) >> 7;
+    }
+    if (idx == n - 1) {
+      out_off[n] = e0;
+      if (out_pad) out_pad[n] = e1;
+      if (out_tiles) out_tiles[n] = e2;
+    }
+  }
+}
+
+// Block 0 routes; blocks 1.. compute amax partials of x (when partials != nullptr)
+// and zero the fp32 accumulator y_acc (T*H floats).
+__global__ void __launch_bounds__(kRouteThreads) route_amax_kernel(
+    const int32_t *__restrict__ ids, int T, int topk, int E, int has_shared, RouteBufs rb,
+    const uint16_t *__restrict__ x, int64_t H, uint32_t *__restrict__ partials, int nparts,
+    float *__restrict__ y_acc, uint32_t *err) {
+  if (blockIdx.x == 0) {
+    __shared__ int s_cnt[kMaxExperts + 1];
+    __shared__ int s_cursor[kMaxExperts];
+    __shared__ int s_tmp[96];
+    const int G = E + (has_shared ? 1 : 0);
+    const int Tk = T * topk;
+    for (int g = threadIdx.x; g < G; g += blockDim.x) s_cnt[g] = 0;
+    __syncthreads();
+    for (int f = threadIdx.x; f < Tk; f += blockDim.x) {
+      const int e = ids[f];
+      if (e >= 0 && e < E)
+        atomicAdd(&s_cnt[e], 1);
+      else
+        raise_device_error(err, NVFP4_DEVERR_BAD_EXPERT_ID);
+    }
+    if (has_shared && threadIdx.x == 0) s_cnt[E] = T;
+    __syncthreads();
+    for (int g = threadIdx.x; g < G; g += blockDim.x) rb.counts[g] = s_cnt[g];
+    block_scan3(s_cnt, G, rb.offsets, rb.pad_offsets, rb.tile_offsets, s_tmp);
+    __syncthreads();
+    for (int e = threadIdx.x; e < E; e += blockDim.x) s_cursor[e] = rb.offsets[e];
+    __syncthreads();
+    // Stable ranking: one warp walks the entries in order, 32 at a time; lanes
+    // holding the same expert get consecutive positions in flat order.
+    if (threadIdx.x < 32) {
+      const int lane = threadIdx.x;
+      for (int base = 0; base < Tk; base += 32) {
+        const int f = base + lane;
+        int e = f < Tk ? ids[f] : -1;
+        if (e < 0 || e >= E) e = -1;
+        const unsigned peers = __match_any_sync(0xffffffffu, e);
+        const int leader = __ffs(peers) - 1;
+        const int rank = __popc(peers & ((1u << lane) - 1u));
+        int start = 0;
+        if (lane == leader && e >= 0) {
+          start = s_cursor[e];
+          s_cursor[e] = start + __popc(peers);
+        }
+        start = __shfl_sync(0xffffffffu, start, leader);
+        if (f < Tk) {
+          if (e >= 0) {
+            rb.sorted_idx[start + rank] = f;
+            rb.inv_idx[f] = start + rank;
+          } else {
+            rb.inv_idx[f] = -1;
+          }
+        }
+      }
+    }
+    return;
+  }
+  // amax partials + zeroing
+  const int b = blockIdx.x - 1, nb = gridDim.x - 1;
+  if (partials && b < nparts) {
+    // partial b covers rows b, b + nparts, ... so every row lands in exactly one partial
+    __shared__ uint32_t scratch[32];
+    uint32_t m = 0;
+    const int64_t chunks = H / 8;
+    for (int64_t r = b; r < T; r += nparts) {
+      const uint4 *row = reinterpret_cast<const uint4 *>(x + r * H);
+      for (int64_t c = threadIdx.x; c < chunks; c += blockDim.x) {
+        const uint4 v = __ldg(row + c);
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) m = max(m, max(w[i] & 0x7FFFu, (w[i] >> 16) & 0x7FFFu));
+      }
+    }
+#pragma unroll
+    for (int o = 16; o; o >>= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, o));
+    if ((threadIdx.x & 31) == 0) scratch[threadIdx.x >> 5] = m;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      for (int i = 1; i < static_cast<int>(blockDim.x >> 5); ++i) m = max(m, scratch[i]);
+      partials[b] = m;
+    }
+  }
+  const int64_t n4 = static_cast<int64_t>(T) * H / 4;
+  float4 *y4 = reinterpret_cast<float4 *>(y_acc);
+  for (int64_t i = static_cast<int64_t>(b) * blockDim.x + threadIdx.x; i < n4;
+       i += static_cast<int64_t>(nb) * blockDim.x)
+    y4[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+}
+
+// One thread per 16-element block of x (T, H).  Every token is quantised once
+// and its codes and scales are written to its row in each routed expert's
+// segment (and the shared expert's segment).
+__global__ void __launch_bounds__(kDispatchThreads) dispatch_quant_kernel(
+    const uint16_t *__restrict__ x, int T, int64_t H, int topk, int E, int has_shared,
+    const int32_t *__restrict__ ids, RouteBufs rb, const uint32_t *__restrict__ partials,
+    int nparts, const float *__restrict__ gs_static, float *__restrict__ gs_out,
+    uint8_t *__restrict__ xq, uint8_t *__restrict__ xsf) {
+  __shared__ uint32_t scratch[32];
+  float gs;
+  if (partials) {
+    gs = gs_from_partials(partials, nparts, scratch);
+    if (blockIdx.x == 0 && threadIdx.x == 0) *gs_out = gs;
+  } else {
+    gs = *gs_static;
+  }
+  const float six_gs = __fmul_rn(6.0f, gs);
+  const int64_t kb = H / 16;
+  const int64_t gb = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const bool valid = gb < static_cast<int64_t>(T) * kb;
+  const int64_t t = valid ? gb / kb : 0;
+  const int64_t c = valid ? gb - t * kb : 0;
+  uint32_t codes[2] = {0u, 0u}, sfb = 0;
+  if (valid) {
+    const uint4 *src = reinterpret_cast<const uint4 *>(x + t * H + c * 16);
+    const uint4 a = __ldg(src), b = __ldg(src + 1);
+    const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+    float v[16];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      v[2 * i] = __uint_as_float(w[i] << 16);
+      v[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+    }
+    sfb = encode_block16(v, gs, six_gs, codes);
+  }
+  const int lane = threadIdx.x & 31;
+  uint32_t word = sfb << ((lane & 3) * 8);
+  word |= __shfl_xor_sync(0xffffffffu, word, 1);
+  word |= __shfl_xor_sync(0xffffffffu, word, 2);
+  if (!valid) return;
+  const uint2 cv = make_uint2(codes[0], codes[1]);
+  const bool sf_writer = (lane & 3) == 0;
+  for (int j = 0; j <= topk; ++j) {
+    int64_t p;
+    if (j < topk) {
+      const int64_t f = t * topk + j;
+      const int pos = rb.inv_idx[f];
+      if (pos < 0) continue;
+      const int e = ids[f];
+      p = static_cast<int64_t>(rb.pad_offsets[e]) + (pos - rb.offsets[e]);
+    } else {
+      if (!has_shared) break;
+      p = static_cast<int64_t>(rb.pad_offsets[E]) + t;
+    }
+    *reinterpret_cast<uint2 *>(xq + p * (H / 2) + c * 8) = cv;
+    if (sf_writer) *reinterpret_cast<uint32_t *>(xsf + sf_word_offset(p, c >> 2, kb >> 2)) = word;
+  }
+}
+
+__global__ void finalize_kernel(const float4 *__restrict__ acc, int64_t n4, uint2 *__restrict__ y) {
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n4;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const float4 v = acc[i];
+    const __nv_bfloat162 lo = __floats2bfloat162_rn(v.x, v.y);
+    const __nv_bfloat162 hi = __floats2bfloat162_rn(v.z, v.w);
+    y[i] = make_uint2(*reinterpret_cast<const uint32_t *>(&lo),
+                      *reinterpret_cast<const uint32_t *>(&hi));
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_route_amax(const int32_t *ids, int T, int topk, int E, int has_shared,
+                              RouteBufs rb, const void *x, int64_t H, uint32_t *partials,
+                              int nparts, float *y_acc, uint32_t *err, cudaStream_t s) {
+  // enough helper blocks to zero y_acc quickly and to give every partial a block
+  const int64_t n4 = static_cast<int64_t>(T) * H / 4;
+  int helpers = static_cast<int>((n4 + kRouteThreads * 8 - 1) / (kRouteThreads * 8));
+  if (partials && helpers < nparts) helpers = nparts;
+  if (helpers < 1) helpers = 1;
+  if (helpers > 1024) helpers = 1024;
+  route_amax_kernel<<<1 + helpers, kRouteThreads, 0, s>>>(
+      ids, T, topk, E, has_shared, rb, static_cast<const uint16_t *>(x), H, partials, nparts,
+      y_acc, err);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_dispatch_quant(const void *x, int T, int64_t H, int topk, int E,
+                                  int has_shared, const int32_t *ids, RouteBufs rb,
+                                  const uint32_t *partials, int nparts, const float *gs_static,
+                                  float *gs_out, uint8_t *xq, uint8_t *xsf, cudaStream_t s) {
+  const int64_t items = static_cast<int64_t>(T) * (H / 16);
+  const int64_t blocks = items > 0 ? (items + kDispatchThreads - 1) / kDispatchThreads : 1;
+  dispatch_quant_kernel<<<static_cast<unsigned>(blocks), kDispatchThreads, 0, s>>>(
+      static_cast<const uint16_t *>(x), T, H, topk, E, has_shared, ids, rb, partials, nparts,
+      gs_static, gs_out, xq, xsf);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_finalize(const float *y_acc, int64_t n, void *y, cudaStream_t s) {
+  const int64_t n4 = n / 4;
+  int64_t blocks = (n4 + 255) / 256;
+  if (blocks < 1) blocks = 1;
+  if (blocks > 4096) blocks = 4096;
+  finalize_kernel<<<static_cast<unsigned>(blocks), 256, 0, s>>>(
+      reinterpret_cast<const float4 *>(y_acc), n4, static_cast<uint2 *>(y));
+  return cudaGetLastError();
+}
+
+}  // namespace nvfp4

@@ -1,0 +1,78 @@
+"""(e) dense Nvfp4Linear and the GEMM core on the GPU against the oracle (identical operands)."""
+
+import numpy as np
+import pytest
+import torch
+
+from nvfp4_block_scaled_quant_gb300 import model, ops, workloads
+from oracle import nvfp4_oracle as O
+from tests.helpers import assert_parity, bf16_to_np, unpack
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+def _weights(N, K, seed):
+    wb = workloads.weight(N, K, seed, "cpu")
+    q, sf, ws2 = model.quantize_weight(wb.to(DEV))
+    wq = O.quantize(wb.float().numpy())
+    # the weight quantisation (the checkpoint format) is bit-exact with the oracle
+    assert ws2.item() == float(wq.gs)
+    np.testing.assert_array_equal(unpack(q), wq.codes)
+    np.testing.assert_array_equal(sf.cpu().numpy().reshape(N, K // 16), wq.sf)
+    wp, sfp = ops.prepare_weights(q, sf, N, K)
+    return wp, sfp, ws2, wq
+
+
+@pytest.mark.parametrize("M,K,N", [(1, 64, 128), (5, 128, 256), (130, 256, 384), (257, 1536, 512), (64, 7168, 256),
+                                   (128, 128, 128), (300, 192, 640)])
+def test_linear_ragged_shapes(M, K, N):
+    x = workloads.activations(M, K, seed=M + K + N, device="cpu", outliers=True)
+    wp, sfp, ws2, wq = _weights(N, K, seed=M * 7 + N)
+    y, gs = ops.linear(x.to(DEV), wp, sfp, ws2, N)
+    torch.cuda.synchronize()
+    xq = O.quantize(x.float().numpy())
+    assert gs.item() == float(xq.gs)
+    assert_parity(bf16_to_np(y), O.linear(xq, wq.codes, wq.sf, wq.gs), what=f"linear {M}x{K}x{N}")
+
+
+@pytest.mark.parametrize("M", sorted(workloads.DENSE_LINEAR))
+def test_linear_dense_workload_full(M):
+    """The dense Nvfp4Linear workload (K=1536, N=16384, outlier activations), every output checked."""
+    _, K, N = workloads.DENSE_LINEAR[M]
+    x = workloads.activations(M, K, seed=20 + M, device="cpu", outliers=True)
+    wp, sfp, ws2, wq = _weights(N, K, seed=21)
+    y, gs = ops.linear(x.to(DEV), wp, sfp, ws2, N)
+    torch.cuda.synchronize()
+    xq = O.quantize(x.float().numpy())
+    assert gs.item() == float(xq.gs)
+    assert_parity(bf16_to_np(y), O.linear(xq, wq.codes, wq.sf, wq.gs), what=f"dense linear M={M}")
+
+
+def test_linear_static_gs_and_empty():
+    M, K, N = 7, 256, 128
+    x = workloads.activations(M, K, seed=3, device="cpu")
+    wp, sfp, ws2, wq = _weights(N, K, seed=4)
+    gs = torch.tensor([0.0021], dtype=torch.float32, device=DEV)
+    y, g = ops.linear(x.to(DEV), wp, sfp, ws2, N, gs=gs)
+    torch.cuda.synchronize()
+    xq = O.quantize(x.float().numpy(), gs=np.float32(0.0021))
+    assert_parity(bf16_to_np(y), O.linear(xq, wq.codes, wq.sf, wq.gs), what="static gs")
+    y0, _ = ops.linear(torch.empty(0, K, dtype=torch.bfloat16, device=DEV), wp, sfp, ws2, N)
+    torch.cuda.synchronize()
+    assert y0.shape == (0, N)
+
+
+@pytest.mark.parametrize("M", [1024])
+def test_gemm_sweep_sampled_rows(M):
+    """Large GEMM (K = N = 7168): full GPU run; the oracle checks a seeded sample of rows."""
+    _, K, N = workloads.DENSE_GEMM[M]
+    x = workloads.activations(M, K, seed=30 + M, device="cpu")
+    wp, sfp, ws2, wq = _weights(N, K, seed=31)
+    q, sf, gs = ops.quantize_act(x.to(DEV))
+    y = ops.gemm(q, sf, gs, K, wp, sfp, ws2, N)
+    torch.cuda.synchronize()
+    xq = O.quantize(x.float().numpy())
+    rows = np.sort(np.random.default_rng(M).choice(M, 48, replace=False))
+    sub = O.Quantized(xq.codes[rows], xq.sf[rows], xq.gs)
+    assert_parity(bf16_to_np(y)[rows], O.linear(sub, wq.codes, wq.sf, wq.gs), what=f"gemm M={M}")
