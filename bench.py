@@ -1,0 +1,508 @@
+"""Benchmark of the NVFP4 MoE expert path on GB300.
+
+One step = one prefill pass of 4096 tokens through a 384-expert MoE layer
+(hidden 7168, intermediate 2048, top-8 Zipf(1.1) routing, one shared expert),
+fed as 32 sequential chunks of 128 tokens.  Each chunk runs the whole hot path:
+routing + global scale + quantise/permute (dispatch), the w13 grouped GEMM with
+SiLU*up and NVFP4 re-quantisation, the w2 grouped GEMM with the weighted
+scatter-add, and the bf16 conversion.
+
+Prints one JSON line (rank 0).  ``--impl reference`` times the CPU oracle on a
+bounded sample of the same workload instead.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "MoE tokens/s; TFLOPS & HBM GB/s as % of 1×GB300 FP4/HBM roofline"
+UNIT = "tokens/s"
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+FP4_OVER_BF16 = 13.5 / 2.25  # nominal dense ratio
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=20)
+    p.add_argument("--warmup", type=int, default=3)
+    p.add_argument("--impl", default="native", choices=["native", "reference"])
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-secondary", action="store_true")
+    return p.parse_args()
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), float(d.get("bf16_tflops_sustained", d["bf16_tflops"])), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, 1700.0, "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for f in ("gemm.cu", "common.cuh", "internal.h"):
+        with open(os.path.join(ROOT, "nvfp4_block_scaled_quant_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def measured_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch from the committed ncu summary, if taken on the current kernel source."""
+    try:
+        with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
+            d = json.load(f)
+        e = d[kernel][workload]
+        if e.get("source_hash") != kernel_source_hash():
+            return None
+        return float(e["bytes_per_launch"])
+    except (OSError, KeyError, ValueError):
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi clock and throttle-reason samples while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_gpu{index}.csv")
+
+    def start(self):
+        os.makedirs(os.path.dirname(self.path), exist_ok=True)
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"], stdout=self.f,
+                                         stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        self.proc.wait(timeout=10)
+        self.f.close()
+        sm, smax, reasons, power = [], [], set(), []
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    smax.append(float(parts[2]))
+                    power.append(float(parts[3]))
+                except ValueError:
+                    continue
+                for n, v in zip(names, parts[5:9]):
+                    if v.lower().startswith("active"):
+                        reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        pmax = max(power) if power else 0.0
+        loaded = [c for c, p in zip(sm, power) if p >= 0.5 * pmax] or sm
+        return {"sm_mhz": statistics.median(loaded), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+                "samples": len(sm), "power_w_max": max(power) if power else None}
+
+
+# --------------------------------------------------------------------------- workload accounting
+
+def chunk_accounting(ids_cpu, cfg):
+    """Algorithmic bytes and flops of one chunk, from its routing."""
+    T, H, I, k = cfg.T, cfg.H, cfg.I, cfg.topk
+    groups = len(set(ids_cpu.flatten().tolist())) + (1 if cfg.shared else 0)
+    rows = T * k + (T if cfg.shared else 0)
+    nvfp4 = 0.5 + 1.0 / 16.0  # bytes per element incl. scales
+    w13 = groups * 2 * I * H * nvfp4
+    w2 = groups * H * I * nvfp4
+    w13_bytes = w13 + rows * H * nvfp4 + rows * I * nvfp4          # weights + A rows + hq written
+    w2_bytes = w2 + rows * I * nvfp4 + T * H * 4 * 2                  # weights + hq rows + fp32 accumulator r/w
+    dispatch_bytes = T * H * 2 * 2 + rows * H * nvfp4 + T * H * 4     # x read twice, xq rows, zeroing y_acc
+    flops = 2.0 * rows * (2 * I * H + H * I)
+    return dict(groups=groups, rows=rows, w13_bytes=w13_bytes, w2_bytes=w2_bytes,
+                step_bytes=w13_bytes + w2_bytes + dispatch_bytes + T * H * (4 + 2), flops=flops)
+
+
+# --------------------------------------------------------------------------- native arm
+
+def run_native(args, rank: int, world: int, local_rank: int):
+    import torch
+
+    from nvfp4_block_scaled_quant_gb300 import build as B
+    B.build()
+    from nvfp4_block_scaled_quant_gb300 import model, ops, workloads
+
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    cfg = workloads.PREFILL
+    T, H, I, E, k, C = cfg.T, cfg.H, cfg.I, cfg.E, cfg.topk, cfg.chunks
+
+    W = model.make_moe_weights(E, H, I, workloads.BENCH_WEIGHT_SEED, dev, shared=True)
+    chunks = []
+    acct = []
+    for c in range(C):
+        x, ids, w = workloads.prefill_chunk(c, device="cpu")
+        acct.append(chunk_accounting(ids.numpy(), cfg))
+        chunks.append((x.to(dev), ids.to(dev), w.to(dev)))
+    L = ops.moe_workspace_layout(T, H, I, E, k, True)
+    ws = torch.empty(L.total, dtype=torch.uint8, device=dev)
+    a1 = torch.empty(1, dtype=torch.float32, device=dev)
+    ys = [torch.empty(T, H, dtype=torch.bfloat16, device=dev) for _ in range(C)]
+
+    # warm-up calibration of the static scale of the intermediate (page 3: gs from a warm-up pass)
+    h_dbg = torch.empty(L.rows_capacity, I, dtype=torch.float32, device=dev)
+    ones = torch.ones(E + 1, dtype=torch.float32, device=dev)
+    amax = 0.0
+    for c in range(2):
+        x, ids, w = chunks[c]
+        ops.moe_dispatch(x, ids, W, a1, True, ws)
+        h_dbg.zero_()
+        ops.moe_w13(T, k, W, a1, ones, ws, h_debug=h_dbg)
+        amax = max(amax, float(h_dbg.abs().amax().item()))
+    a2 = torch.full((E + 1,), amax / 2688.0, dtype=torch.float32, device=dev)
+    del h_dbg
+
+    stream = torch.cuda.current_stream(dev)
+    # one event quadruple per (step, chunk): w13 and w2 launch durations over the whole timed region
+    ev = [[[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(C)] for _ in range(args.steps)]
+
+    def step(evs):
+        for c in range(C):
+            x, ids, w = chunks[c]
+            ops.moe_dispatch(x, ids, W, a1, True, ws)
+            if evs is not None:
+                evs[c][0].record(stream)
+            ops.moe_w13(T, k, W, a1, a2, ws)
+            if evs is not None:
+                evs[c][1].record(stream)
+                evs[c][2].record(stream)
+            ops.moe_w2(T, k, w, W, a2, ws)
+            if evs is not None:
+                evs[c][3].record(stream)
+            ops.moe_finalize(T, k, W, ys[c], ws)
+
+    for _ in range(args.warmup):
+        step(None)
+    torch.cuda.synchronize()
+    st, flags = ops.device_error()
+    if st != 0:
+        raise RuntimeError(f"device fault flags {flags:#x} after warm-up")
+
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+    clocks = ClockSampler(local_rank)
+    clocks.start()
+    time.sleep(0.5)  # let the sampler start before the timed region
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    start.record(stream)
+    for s in range(args.steps):
+        step(ev[s])
+    stop.record(stream)
+    stop.synchronize()
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    elapsed_ms = start.elapsed_time(stop)
+    clk = clocks.stop()
+    t_w13 = sum(ev[s][c][0].elapsed_time(ev[s][c][1]) for s in range(args.steps) for c in range(C)) / args.steps
+    t_w2 = sum(ev[s][c][2].elapsed_time(ev[s][c][3]) for s in range(args.steps) for c in range(C)) / args.steps
+    if dist:
+        tt = torch.tensor([elapsed_ms], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        elapsed_ms = float(tt.item())
+    st, flags = ops.device_error()
+    if st != 0:
+        raise RuntimeError(f"device fault flags {flags:#x} in the timed region")
+
+    tokens_per_step = T * C
+    value = world * tokens_per_step * args.steps / (elapsed_ms / 1e3)
+    ms_per_step = elapsed_ms / args.steps
+    hbm, bf16, bf16_sus, peak_kind = peaks()
+    fp4_peak = bf16 * FP4_OVER_BF16
+    w13_bytes = sum(a["w13_bytes"] for a in acct)  # per step (one launch per chunk)
+    w2_bytes = sum(a["w2_bytes"] for a in acct)
+    step_bytes = sum(a["step_bytes"] for a in acct)
+    flops = sum(a["flops"] for a in acct)
+    w13_avg_ms = t_w13 / C
+    achieved = (w13_bytes / C) / (w13_avg_ms / 1e3) / 1e9
+    traffic = measured_traffic("w13", cfg.name)
+
+    # ---------------------------------------------------------------- end to end through the public API
+    xh = [torch.empty(T, H, dtype=torch.bfloat16).pin_memory() for _ in range(C)]
+    idh = [torch.empty(T, k, dtype=torch.int32).pin_memory() for _ in range(C)]
+    wh = [torch.empty(T, k, dtype=torch.float32).pin_memory() for _ in range(C)]
+    yh = [torch.empty(T, H, dtype=torch.bfloat16).pin_memory() for _ in range(C)]
+    for c in range(C):
+        xh[c].copy_(chunks[c][0].cpu())
+        idh[c].copy_(chunks[c][1].cpu())
+        wh[c].copy_(chunks[c][2].cpu())
+    xd = torch.empty(T, H, dtype=torch.bfloat16, device=dev)
+    idd = torch.empty(T, k, dtype=torch.int32, device=dev)
+    wd = torch.empty(T, k, dtype=torch.float32, device=dev)
+    yd = torch.empty(T, H, dtype=torch.bfloat16, device=dev)
+
+    def e2e_step():
+        for c in range(C):
+            xd.copy_(xh[c], non_blocking=True)
+            idd.copy_(idh[c], non_blocking=True)
+            wd.copy_(wh[c], non_blocking=True)
+            ops.moe_forward(xd, idd, wd, W, a2, workspace=ws, out=yd)
+            yh[c].copy_(yd, non_blocking=True)
+
+    for _ in range(args.warmup):
+        e2e_step()
+    torch.cuda.synchronize()
+    e_start, e_stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e_start.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    e_stop.record(stream)
+    e_stop.synchronize()
+    e_ms = e_start.elapsed_time(e_stop)
+    if dist:
+        tt = torch.tensor([e_ms], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        e_ms = float(tt.item())
+    h2d = C * (T * H * 2 + T * k * 4 * 2)
+    d2h = C * T * H * 2
+    e2e = {"value": world * tokens_per_step * args.steps / (e_ms / 1e3), "unit": UNIT,
+           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+           "api": "nvfp4_moe_forward (one call per chunk), pinned host buffers"}
+
+    result = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "nvfp4 (e2m1 x e2m1, e4m3 block scales) -> f32 acc",
+        "data": "synthetic (seeded; bf16 N(0,0.02) weights quantised to NVFP4, N(0,1) activations with 1% x20 "
+                "outlier channels, Zipf(1.1) top-8 routing)",
+        "config": {"workload": cfg.name, "tokens_per_step": tokens_per_step, "chunks": C, "chunk_tokens": T,
+                   "hidden": H, "intermediate": I, "experts": E, "topk": k, "shared_expert": True,
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                   "l2": "working set of ~5.6 GB of expert weights per chunk (> 129 MB L2); no flush needed",
+                   "a1_gs": "dynamic per chunk", "a2_gs": "static, warm-up calibrated"},
+        "roofline": {"bound": "hbm", "kernel": "w13 grouped GEMM + SiLU*up + requant",
+                     "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
+                     "traffic": traffic, "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)",
+                     "algorithmic_bytes_per_launch": w13_bytes / C, "avg_launch_ms": w13_avg_ms},
+        "step_roofline": {"hbm_gbs": step_bytes / (ms_per_step / 1e3) / 1e9,
+                          "hbm_frac": step_bytes / (ms_per_step / 1e3) / 1e9 / hbm,
+                          "tflops": flops / (ms_per_step / 1e3) / 1e12,
+                          "tensor_frac_fp4": flops / (ms_per_step / 1e3) / 1e12 / fp4_peak,
+                          "fp4_peak_tflops": fp4_peak, "fp4_peak_source": f"{peak_kind} bf16 x {FP4_OVER_BF16}",
+                          "w2_avg_ms": t_w2 / C,
+                          "w2_gbs": (w2_bytes / C) / (t_w2 / C / 1e3) / 1e9,
+                          "groups_per_chunk_mean": sum(a["groups"] for a in acct) / C},
+        "e2e": e2e,
+        "gpu_launches": args.steps * C * 5,
+        "clocks": clk,
+    }
+    return result, (W, chunks, a2, ws, a1, dev)
+
+
+# --------------------------------------------------------------------------- secondary workloads
+
+def run_secondary(state, args):
+    """Decode steps and the dense linear / GEMM workloads, one line each in 'secondary'."""
+    import torch
+
+    from nvfp4_block_scaled_quant_gb300 import model, ops, workloads
+    W, _, a2, _, _, dev = state
+    hbm, bf16, _, _ = peaks()
+    fp4_peak = bf16 * FP4_OVER_BF16
+    out = []
+    stream = torch.cuda.current_stream(dev)
+
+    def time_fn(fn, iters):
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize()
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s.record(stream)
+        for _ in range(iters):
+            fn()
+        e.record(stream)
+        e.synchronize()
+        return s.elapsed_time(e) / iters
+
+    for T in (1, 8, 64):
+        cfg = workloads.DECODE[T]
+        steps = [workloads.decode_step(T, step=i, device="cpu") for i in range(16)]
+        acct = [chunk_accounting(s[1].numpy(), cfg) for s in steps]
+        dev_steps = [(x.to(dev), i.to(dev), w.to(dev)) for x, i, w in steps]
+        ws = ops.moe_workspace(T, cfg.H, cfg.I, cfg.E, cfg.topk, True, dev)
+        y = torch.empty(T, cfg.H, dtype=torch.bfloat16, device=dev)
+        it = [0]
+
+        def fwd():
+            x, i, w = dev_steps[it[0] % 16]
+            it[0] += 1
+            ops.moe_forward(x, i, w, W, a2, workspace=ws, out=y)
+
+        ms = time_fn(fwd, 64)
+        b = sum(a["step_bytes"] for a in acct) / 16
+        out.append({"workload": cfg.name, "tokens_per_s": T / (ms / 1e3), "ms_per_step": ms,
+                    "hbm_gbs": b / (ms / 1e3) / 1e9, "hbm_frac": b / (ms / 1e3) / 1e9 / hbm,
+                    "groups_mean": sum(a["groups"] for a in acct) / 16,
+                    "note": "16 seeded routings cycled; weights streamed from HBM (> L2)"})
+    # dense linear K=1536 N=16384: 14 MB of weights fit in L2, so rotate 16 weight copies (> L2)
+    K, N = 1536, 16384
+    dws = [model.make_dense_weight(N, K, seed=50 + i, device=dev) for i in range(16)]
+    for M in (1, 32, 128):
+        x = workloads.activations(M, K, seed=60 + M, device=dev, outliers=True)
+        wsl = torch.empty(int(ops.lib().nvfp4_linear_workspace_bytes(M, K)), dtype=torch.uint8, device=dev)
+        y = torch.empty(M, N, dtype=torch.bfloat16, device=dev)
+        gs = torch.empty(1, dtype=torch.float32, device=dev)
+        it = [0]
+
+        def lin():
+            d = dws[it[0] % 16]
+            it[0] += 1
+            ops.call("nvfp4_linear", x.data_ptr(), M, K, N, d.w.data_ptr(), d.sf.data_ptr(), d.ws2.data_ptr(), 0,
+                     gs.data_ptr(), y.data_ptr(), wsl.data_ptr(), wsl.numel(), stream.cuda_stream)
+
+        ms = time_fn(lin, 160)
+        b = N * K * (0.5 + 1 / 16) + M * K * 2 + M * N * 2
+        out.append({"workload": f"dense_linear_M{M}_K{K}_N{N}", "us_per_call": ms * 1e3,
+                    "hbm_gbs": b / (ms / 1e3) / 1e9, "hbm_frac": b / (ms / 1e3) / 1e9 / hbm,
+                    "tflops": 2 * M * N * K / (ms / 1e3) / 1e12,
+                    "note": "quantise + GEMM; 16 weight copies rotated (230 MB > L2)"})
+    del dws
+    K = N = 7168
+    dw = model.make_dense_weight(N, K, seed=70, device=dev)
+    for M in (1024, 4096, 16384):
+        x = workloads.activations(M, K, seed=80 + M, device=dev)
+        q, sf, gs = ops.quantize_act(x)
+        y = torch.empty(M, N, dtype=torch.bfloat16, device=dev)
+        ms = time_fn(lambda: ops.gemm(q, sf, gs, K, dw.w, dw.sf, dw.ws2, N, out=y), 10)
+        fl = 2.0 * M * N * K
+        out.append({"workload": f"dense_gemm_M{M}_K{K}_N{N}", "ms_per_call": ms, "tflops": fl / (ms / 1e3) / 1e12,
+                    "tensor_frac_fp4": fl / (ms / 1e3) / 1e12 / fp4_peak,
+                    "note": "GEMM alone on quantised activations; operands (<= 170 MB) re-read across calls"})
+    return out
+
+
+# --------------------------------------------------------------------------- CPU oracle
+
+def oracle_sample(n_tokens: int, chunk: int = 0, device="cpu"):
+    """Inputs of a bounded sample of the workload for the oracle: n tokens of one prefill chunk."""
+    import numpy as np
+    import torch
+
+    from nvfp4_block_scaled_quant_gb300 import workloads
+    from oracle import nvfp4_oracle as O
+    cfg = workloads.PREFILL
+    x, ids, w = workloads.prefill_chunk(chunk, device="cpu")
+    tokens = list(range(n_tokens))
+    needed = sorted(set(ids[:n_tokens].flatten().tolist()))
+    gdev = device if device != "cpu" and torch.cuda.is_available() else "cpu"
+    experts = {}
+    for e in needed + [cfg.E]:
+        s13, s2 = workloads.expert_seeds(workloads.BENCH_WEIGHT_SEED, e)
+        q13 = O.quantize(workloads.weight(2 * cfg.I, cfg.H, s13, gdev).float().cpu().numpy())
+        q2 = O.quantize(workloads.weight(cfg.H, cfg.I, s2, gdev).float().cpu().numpy())
+        experts[e] = O.Expert(q13.codes, q13.sf, q13.gs, q2.codes, q2.sf, q2.gs)
+    a2 = np.full(cfg.E + 1, np.float32(0.01), dtype=np.float32)
+    return cfg, x.float().numpy(), ids.numpy(), w.numpy(), experts, a2, tokens
+
+
+def time_oracle(n_tokens: int, reps: int, device="cpu"):
+    from oracle import nvfp4_oracle as O
+    cfg, x, ids, w, experts, a2, tokens = oracle_sample(n_tokens, device=device)
+    times = []
+    for _ in range(reps):
+        t0 = time.perf_counter()
+        O.moe_forward(x, ids, w, experts.__getitem__, cfg.E, a2, shared=experts[cfg.E], tokens=tokens)
+        times.append(time.perf_counter() - t0)
+    return cfg, times
+
+
+def cpu_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def cpu_baseline(device):
+    cfg, times = time_oracle(2, 1, device=device)
+    return {"value": 2 / times[0], "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
+            "sample": f"2 tokens of prefill chunk 0 (8 routed experts each + shared), full oracle MoE forward "
+                      f"(fp64 dequant + contractions; numpy BLAS threads up to the {cpu_cores()} cores); "
+                      f"{times[0]:.1f} s",
+            "threads_note": "numpy matmul may use every core in the affinity set"}
+
+
+def run_reference(args, rank: int, world: int):
+    if rank != 0:
+        return None
+    import torch
+    # the weights are drawn on the GPU, like the native arm's; the oracle itself runs on the host cores
+    cfg, times = time_oracle(1, args.warmup + args.steps, device="cuda" if torch.cuda.is_available() else "cpu")
+    timed = times[args.warmup:]
+    total = sum(timed)
+    value = len(timed) / total
+    return {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / len(timed),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64 (oracle)",
+            "data": "synthetic (seeded), same workload", "config": {"workload": cfg.name, "oracle_tokens_per_step": 1},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
+                             "sample": "each step: 1 token of prefill chunk 0 through the full oracle MoE forward"},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main():
+    args = parse()
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args, rank, world)), flush=True)
+        return
+    import torch
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    result, state = run_native(args, rank, world, local_rank)
+    if rank == 0:
+        if not args.no_secondary:
+            result["secondary"] = run_secondary(state, args)
+        if not args.no_cpu_baseline and world == 1:
+            del state
+            torch.cuda.empty_cache()
+            result["cpu_baseline"] = cpu_baseline(device=f"cuda:{local_rank}")
+        print(json.dumps(result), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

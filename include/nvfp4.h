@@ -108,7 +108,8 @@ NVFP4_API size_t nvfp4_sf_bytes(int64_t rows, int64_t K);
  * with the sign of x_i kept on zero codes, and all codes 0 when d == 0 or 1/d
  * overflows.  gs_mode NVFP4_GS_DYNAMIC computes gs = fl32(amax / 2688) over
  * all M*K elements (two launches: block-max partials, then quantize) and
- * stores it to *gs; NVFP4_GS_STATIC reads *gs.  Workspace: amax partials. */
+ * stores it to *gs; NVFP4_GS_STATIC reads *gs.  Workspace: amax partials.
+ * With M == 0 only gs is used (dynamic mode writes 0); x, q and sf may be NULL. */
 NVFP4_API size_t nvfp4_quantize_workspace_bytes(int64_t M, int64_t K);
 NVFP4_API nvfp4_status nvfp4_quantize_act(const void *x, int64_t M, int64_t K, int64_t ldx, int gs_mode,
                                 float *gs, uint8_t *q, uint8_t *sf, int sf_layout, void *ws,

@@ -356,7 +356,7 @@ nvfp4_status nvfp4_quantize_act(const void *x, int64_t M, int64_t K, int64_t ldx
   NV_REQUIRE(gs_mode == NVFP4_GS_DYNAMIC || gs_mode == NVFP4_GS_STATIC, NVFP4_ERR_INVALID_ARG, "gs_mode %d", gs_mode);
   NV_REQUIRE(sf_layout == NVFP4_SF_SWIZZLED || sf_layout == NVFP4_SF_LINEAR, NVFP4_ERR_INVALID_ARG, "sf_layout %d",
              sf_layout);
-  NV_REQUIRE(gs != nullptr && q != nullptr && sf != nullptr && (x != nullptr || M == 0), NVFP4_ERR_INVALID_ARG,
+  NV_REQUIRE(gs != nullptr && ((x != nullptr && q != nullptr && sf != nullptr) || M == 0), NVFP4_ERR_INVALID_ARG,
              "NULL pointer argument");
   NV_REQUIRE(ldx >= K && ldx % 8 == 0, NVFP4_ERR_MISALIGNED, "ldx=%lld must be >= K and a multiple of 8",
              (long long)ldx);

@@ -1,0 +1,72 @@
+"""Run one workload of the path a few times, for a profiler to attach to.
+
+    python -m nvfp4_block_scaled_quant_gb300.profile_case moe --experts 64 --iters 3
+    python -m nvfp4_block_scaled_quant_gb300.profile_case gemm --M 4096 --iters 3
+    python -m nvfp4_block_scaled_quant_gb300.profile_case linear --M 32 --iters 3
+
+``moe`` runs 128-token prefill chunks (hidden 7168, intermediate 2048, top-8
+Zipf(1.1) routing, shared expert) over ``--experts`` experts, so the weights
+held on the device stay a few GB while the per-tile work of every kernel is
+the same as in the 384-expert layer.  The kernels launch in the same order and
+configuration as in the benchmark.
+"""
+
+from __future__ import annotations
+
+import argparse
+import sys
+
+import torch
+
+from . import build as B
+
+
+def main(argv=None):
+    p = argparse.ArgumentParser()
+    p.add_argument("case", choices=["moe", "gemm", "linear"])
+    p.add_argument("--experts", type=int, default=64)
+    p.add_argument("--M", type=int, default=4096)
+    p.add_argument("--iters", type=int, default=3)
+    a = p.parse_args(argv)
+    B.build()
+    from . import model, ops, workloads
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    if a.case == "moe":
+        cfg = workloads.PREFILL
+        E = a.experts
+        W = model.make_moe_weights(E, cfg.H, cfg.I, workloads.BENCH_WEIGHT_SEED, dev, shared=True)
+        sub = workloads.MoEConfig("profile", cfg.T, cfg.H, cfg.I, E, cfg.topk, True, "zipf", True)
+        a2 = torch.full((E + 1,), 0.02, dtype=torch.float32, device=dev)
+        ws = ops.moe_workspace(cfg.T, cfg.H, cfg.I, E, cfg.topk, True, dev)
+        y = torch.empty(cfg.T, cfg.H, dtype=torch.bfloat16, device=dev)
+        for i in range(a.iters):
+            x = workloads.activations(cfg.T, cfg.H, seed=700_000 + i, device=dev, outliers=True)
+            ids, w = workloads.routing(sub, seed=800_000 + i, device=dev)
+            ops.moe_forward(x, ids, w, W, a2, workspace=ws, out=y)
+    elif a.case == "gemm":
+        K = N = 7168
+        dw = model.make_dense_weight(N, K, seed=70, device=dev)
+        x = workloads.activations(a.M, K, seed=80, device=dev)
+        q, sf, gs = ops.quantize_act(x)
+        y = torch.empty(a.M, N, dtype=torch.bfloat16, device=dev)
+        for _ in range(a.iters):
+            ops.gemm(q, sf, gs, K, dw.w, dw.sf, dw.ws2, N, out=y)
+    else:
+        K, N = 1536, 16384
+        dw = model.make_dense_weight(N, K, seed=50, device=dev)
+        x = workloads.activations(a.M, K, seed=60, device=dev, outliers=True)
+        for _ in range(a.iters):
+            ops.linear(x, dw.w, dw.sf, dw.ws2, N)
+    torch.cuda.synchronize()
+    st, flags = ops.device_error()
+    if st != 0:
+        print(f"device fault flags {flags:#x}", file=sys.stderr)
+        return 1
+    print(f"{a.case}: {a.iters} iterations done")
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())
