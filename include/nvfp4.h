@@ -139,6 +139,38 @@ NVFP4_API nvfp4_status nvfp4_linear(const void *x, int64_t M, int64_t K, int64_t
                           const uint8_t *w_sf, const float *ws2, int gs_mode, float *gs, void *y,
                           void *ws, size_t ws_bytes, void *stream);
 
+/* Dense linear that allocates nothing and takes no workspace.  (No counterpart
+ * on the pages: this entry point exists for callers, not for the method.)
+ *
+ * Some callers cannot allocate device memory at the point where they run the
+ * linear.  Examples are a plugin inside a host inference engine that owns all
+ * device memory and forbids allocation while it enqueues work, or a serving
+ * loop that reserved a fixed memory budget at start-up and must not touch an
+ * allocator per request.  Such a caller may also have no workspace to lend.
+ *
+ * This variant computes exactly what nvfp4_linear computes, with the same
+ * arguments minus (ws, ws_bytes).  Its scratch (the quantised activations, their
+ * scales and the amax partials) lives in one file-scope device array of
+ * NVFP4_LINEAR_NOALLOC_MAX_BYTES bytes.  Every GPU that loads the library
+ * holds that array until the process exits.
+ *  - Limit: nvfp4_linear_workspace_bytes(M, K) must not exceed the array size.
+ *    For K = 7168 that is M <= 1025; for K = 1536 it is M <= 4848.  Larger
+ *    calls return NVFP4_ERR_WORKSPACE before anything is enqueued.
+ *  - Set-up: the first call on each device resolves the array's device
+ *    address, with that device current.  Make that first call before any
+ *    stream capture begins.
+ *  - Sharing: all calls on a device use the same array.  It keeps the contents
+ *    of the last call, and nothing in it needs to start at zero, because every
+ *    byte the GEMM reads is rewritten by the call's own quantise step.  Calls
+ *    that overlap on the GPU (different streams without ordering between
+ *    them) race on the array and give wrong results: serialise them.
+ *  - It calls no cudaMalloc, cudaFree or allocating library routine. */
+#define NVFP4_LINEAR_NOALLOC_MAX_BYTES (4u << 20)
+NVFP4_API nvfp4_status nvfp4_linear_noalloc(const void *x, int64_t M, int64_t K, int64_t N,
+                                            const uint8_t *w, const uint8_t *w_sf,
+                                            const float *ws2, int gs_mode, float *gs, void *y,
+                                            void *stream);
+
 /* GEMM alone on already-quantised activations: xq (M, K/2) codes with
  * swizzled scales xsf (nvfp4_sf_bytes(M, K)) and device scalar gs; W and ws2
  * as for nvfp4_linear.  y (M, N) bf16. */

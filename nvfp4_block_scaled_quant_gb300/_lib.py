@@ -33,6 +33,7 @@ PREP_PLAIN = 0
 PREP_W13_INTERLEAVE = 1
 DEVERR_BAD_EXPERT_ID = 1
 DEVERR_PIPELINE_TIMEOUT = 2
+LINEAR_NOALLOC_MAX_BYTES = 4 << 20
 
 
 class MoeWsLayout(Structure):
@@ -55,6 +56,7 @@ _SIGNATURES = {
     "nvfp4_linear_workspace_bytes": (c_size_t, [I64, I64]),
     "nvfp4_linear": (c_int, [P, I64, I64, I64, P, P, P, c_int, P, P, P, c_size_t, P]),
     "nvfp4_gemm": (c_int, [P, P, P, I64, I64, I64, P, P, P, P, P]),
+    "nvfp4_linear_noalloc": (c_int, [P, I64, I64, I64, P, P, P, c_int, P, P, P]),
     "nvfp4_moe_route": (c_int, [P, I64, c_int, I64, P, P, P, P, P]),
     "nvfp4_moe_workspace_layout": (c_int, [I64, I64, I64, I64, c_int, c_int, POINTER(MoeWsLayout)]),
     "nvfp4_moe_workspace_bytes": (c_size_t, [I64, I64, I64, I64, c_int, c_int]),

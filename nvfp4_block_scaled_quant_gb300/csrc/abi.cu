@@ -478,6 +478,63 @@ nvfp4_status nvfp4_linear(const void *x, int64_t M, int64_t K, int64_t N, const 
   return gemm_dense(__func__, d, xq, xsf, gs, M, K, N, w, w_sf, ws2, y, s);
 }
 
+// ---------------------------------------------------------------- no-allocation dense linear
+// Scratch of nvfp4_linear_noalloc: one array per device, alive until the process exits.
+}  // extern "C"
+namespace nvfp4 {
+namespace {
+__device__ __align__(256) uint8_t g_linear_noalloc_scratch[NVFP4_LINEAR_NOALLOC_MAX_BYTES];
+void *g_noalloc_ptr[kMaxDevices] = {nullptr};
+
+// Device address of the scratch array on the current device, resolved once per device.
+nvfp4_status noalloc_scratch(const char *fn, void **out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(fn, e, "cudaGetDevice");
+  std::lock_guard<std::mutex> lock(g_dev_mutex);
+  if (g_noalloc_ptr[dev] == nullptr) {
+    void *p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_linear_noalloc_scratch);
+    if (e != cudaSuccess) return cuda_fail(fn, e, "cudaGetSymbolAddress(no-allocation scratch)");
+    g_noalloc_ptr[dev] = p;
+  }
+  *out = g_noalloc_ptr[dev];
+  return NVFP4_OK;
+}
+}  // namespace
+}  // namespace nvfp4
+extern "C" {
+
+nvfp4_status nvfp4_linear_noalloc(const void *x, int64_t M, int64_t K, int64_t N, const uint8_t *w,
+                                  const uint8_t *w_sf, const float *ws2, int gs_mode, float *gs, void *y,
+                                  void *stream) {
+  NV_CHECK_GEMM_SHAPE(M, K, N);
+  NV_REQUIRE(gs_mode == NVFP4_GS_DYNAMIC || gs_mode == NVFP4_GS_STATIC, NVFP4_ERR_INVALID_ARG, "gs_mode %d", gs_mode);
+  NV_REQUIRE(gs && w && w_sf && ws2 && ((x && y) || M == 0), NVFP4_ERR_INVALID_ARG, "NULL pointer argument");
+  NV_REQUIRE(aligned(x, 16) && aligned(w, 16) && aligned(w_sf, 16) && aligned(y, 16) && aligned(gs, 4) &&
+                 aligned(ws2, 4),
+             NVFP4_ERR_MISALIGNED, "pointers must be 16-byte aligned");
+  const LinearWs L = linear_ws(M, K);
+  NV_REQUIRE(L.total <= NVFP4_LINEAR_NOALLOC_MAX_BYTES, NVFP4_ERR_WORKSPACE,
+             "M=%lld K=%lld needs %zu bytes of scratch, above the %u-byte static array; use nvfp4_linear with a "
+             "caller workspace",
+             (long long)M, (long long)K, L.total, NVFP4_LINEAR_NOALLOC_MAX_BYTES);
+  DeviceInfo *d;
+  nvfp4_status st = device_info(__func__, &d);
+  if (st != NVFP4_OK) return st;
+  void *scratch = nullptr;
+  if ((st = noalloc_scratch(__func__, &scratch)) != NVFP4_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint8_t *xq = at<uint8_t>(scratch, L.xq), *xsf = at<uint8_t>(scratch, L.xsf);
+  const bool dyn = gs_mode == NVFP4_GS_DYNAMIC;
+  const int nparts = amax_partial_count(M, K);
+  uint32_t *partials = dyn ? at<uint32_t>(scratch, L.partials) : nullptr;
+  if (dyn) NV_CUDA(launch_amax_partials(x, M, K, K, partials, nparts, s), "amax kernel launch");
+  NV_CUDA(launch_quantize(x, M, K, K, partials, nparts, gs, gs, xq, xsf, NVFP4_SF_SWIZZLED, s),
+          "quantize kernel launch");
+  return gemm_dense(__func__, d, xq, xsf, gs, M, K, N, w, w_sf, ws2, y, s);
+}
+
 nvfp4_status nvfp4_moe_route(const int32_t *ids, int64_t T, int topk, int64_t E, int32_t *counts, int32_t *offsets,
                              int32_t *sorted_idx, int32_t *inv_idx, void *stream) {
   NV_REQUIRE(T >= 0 && topk > 0 && E > 0, NVFP4_ERR_INVALID_ARG, "T=%lld topk=%d E=%lld", (long long)T, topk,
