@@ -291,7 +291,7 @@ nvfp4_status moe_gemm_impl(const char *fn, DeviceInfo *d, Epi epi, int64_t T, in
     a.topk_w = topk_w;
     a.topk = topk;
   }
-  NV_CUDA(launch_gemm(epi, ta, tb, tbs, a, d->sms, s), "grouped GEMM launch");
+  NV_CUDA(launch_gemm(epi, ta, tb, tbs, a, d->sms * kCtasPerSm, s), "grouped GEMM launch");
   return NVFP4_OK;
 }
 
@@ -427,7 +427,7 @@ static nvfp4_status gemm_dense(const char *fn, DeviceInfo *d, const uint8_t *xq,
   a.out_ld = static_cast<int>(N);
   a.err = d->flags;
   const int64_t tiles = ((M + kBlockM - 1) / kBlockM) * (N / kBlockN);
-  const int grid = static_cast<int>(tiles < d->sms ? tiles : d->sms);
+  const int grid = static_cast<int>(tiles < d->sms * kCtasPerSm ? tiles : d->sms * kCtasPerSm);
   NV_CUDA(launch_gemm(Epi::kLinear, ta, tb, tb, a, grid, s), "GEMM launch");
   return NVFP4_OK;
 }

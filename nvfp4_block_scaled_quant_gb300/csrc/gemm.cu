@@ -6,13 +6,13 @@
 // (tcgen05.mma kind::mxf4nvf4, scale_vec::4X, K = 64 per instruction), operands
 // staged in shared memory by TMA (128-byte swizzle, 256 FP4 elements of K per
 // stage) and the block scales copied from shared memory to TMEM with
-// tcgen05.cp.  One persistent CTA per SM walks the tiles of all groups:
+// tcgen05.cp.  Two persistent CTAs per SM walk the tiles of all groups:
 //   warp 0      TMA producer (one lane): A box rows only as far as the group's
 //               live rows reach, B tile, A/B scale blocks (bulk copies);
 //   warp 1      MMA issuer (one lane), owns the TMEM allocation;
 //   warps 2..5  epilogue, one accumulator row per thread (TMEM lane quarters).
-// Two accumulator buffers let the epilogue of tile i overlap the main loop of
-// tile i+1.  Every wait is bounded (kPipelineTimeoutNs); a role that gives up
+// The two CTAs of an SM overlap each other's epilogues and keep two MMA
+// issuers busy (one accumulator buffer each).  Every wait is bounded (kPipelineTimeoutNs); a role that gives up
 // sets a shared abort flag, the others drain and the CTA frees TMEM and exits
 // with NVFP4_DEVERR_PIPELINE_TIMEOUT raised.
 //
@@ -69,7 +69,7 @@ constexpr uint32_t kIdesc = (1u << 7) | (1u << 10) | ((uint32_t(kBlockN) >> 3) <
 __device__ __forceinline__ float silu_mul(float g, float u) { return g / (1.0f + expf(-g)) * u; }
 
 template <int kEpi>
-__global__ void __launch_bounds__(kGemmThreads, 1)
+__global__ void __launch_bounds__(kGemmThreads, kCtasPerSm)
     nvfp4_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                       const __grid_constant__ CUtensorMap tmB,
                       const __grid_constant__ CUtensorMap tmBs, const GemmArgs args) {
@@ -128,8 +128,17 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   if (warp == 0) {
     if (lane == 0) {
       // ------------------------------------------------------------ TMA producer
-      const uint64_t pol_w = policy_evict_first();  // weights stream through once
-      const uint64_t pol_a = policy_evict_last();   // activations are re-read per n tile
+      const uint64_t pol_stream = policy_evict_first();  // weights of a single-m-tile group: read once
+      const uint64_t pol_reuse = policy_evict_normal();  // weights re-read by later m tiles
+      const uint64_t pol_a = policy_evict_last();        // activations are re-read per n tile
+      // Weight location of (tile, k stage): tensor map, first row, scale bytes.
+      auto b_src = [&](const Tile &t, const CUtensorMap *&mb, int &b_row0, const uint8_t *&sfb) {
+        const bool sh = t.g == args.shared_group;
+        mb = sh ? &tmBs : &tmB;
+        b_row0 = (sh ? 0 : t.g * args.N) + t.nt * kBlockN;
+        sfb = (sh ? args.b_sf_shared : args.b_sf + static_cast<size_t>(t.g) * args.N * (args.K / 16)) +
+              static_cast<size_t>(t.nt) * k_steps * kSfBytesPerKStep;
+      };
       int stage = 0;
       uint32_t phase = 0;
       uint32_t issued = 0;  // bit s: stage s has a load in flight with parity bit (s+8)
@@ -137,13 +146,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       for (int idx = blockIdx.x; ok && idx < total_tiles; idx += gridDim.x) {
         Tile t;
         decode_tile(args, idx, n_tiles, t);
-        const bool sh = t.g == args.shared_group;
-        const CUtensorMap *mb = sh ? &tmBs : &tmB;
-        const int b_row0 = (sh ? 0 : t.g * args.N) + t.nt * kBlockN;
-        const uint8_t *sfb =
-            (sh ? args.b_sf_shared
-                : args.b_sf + static_cast<size_t>(t.g) * args.N * (args.K / 16)) +
-            static_cast<size_t>(t.nt) * k_steps * kSfBytesPerKStep;
+        const CUtensorMap *mb;
+        int b_row0;
+        const uint8_t *sfb;
+        b_src(t, mb, b_row0, sfb);
+        const int group_rows = args.counts ? __ldg(args.counts + t.g) : args.dense_M;
+        const uint64_t pol_w = group_rows > kBlockM ? pol_reuse : pol_stream;
         const uint8_t *sfa =
             args.a_sf + static_cast<size_t>(t.a_row0 / kBlockM) * k_steps * kSfBytesPerKStep;
         const int nbox = (t.rows + kABoxRows - 1) / kABoxRows;
@@ -192,8 +200,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       const uint32_t sA0 = smem_u32(sA), sB0 = smem_u32(sB);
       const uint32_t sSFA0 = smem_u32(sSFA), sSFB0 = smem_u32(sSFB);
       for (int idx = blockIdx.x; ok && idx < total_tiles; idx += gridDim.x, ++it) {
-        const int acc = it & 1;
-        const uint32_t acc_phase = (it >> 1) & 1;
+        const int acc = kAccBufs == 2 ? (it & 1) : 0;
+        const uint32_t acc_phase = kAccBufs == 2 ? ((it >> 1) & 1) : (it & 1);
         if (!mbar_wait_bounded(&tempty[acc], acc_phase ^ 1, abort_flag, args.err,
                                kPipelineTimeoutNs)) {
           ok = false;
@@ -246,8 +254,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     for (int idx = blockIdx.x; idx < total_tiles; idx += gridDim.x, ++it) {
       Tile t;
       decode_tile(args, idx, n_tiles, t);
-      const int acc = it & 1;
-      const uint32_t acc_phase = (it >> 1) & 1;
+      const int acc = kAccBufs == 2 ? (it & 1) : 0;
+      const uint32_t acc_phase = kAccBufs == 2 ? ((it >> 1) & 1) : (it & 1);
       bool ok = mbar_wait_bounded(&tfull[acc], acc_phase, abort_flag, args.err,
                                   kPipelineTimeoutNs);
       ok = __all_sync(0xffffffffu, ok);

@@ -15,21 +15,32 @@ constexpr int kMaxExperts = 1024;       // routing limit (E)
 constexpr int kMaxTopk = 32;
 constexpr uint64_t kPipelineTimeoutNs = 2000000000ull;  // 2 s: no healthy wait comes close
 
-// GEMM tile geometry (one CTA per SM, persistent).
+// GEMM tile geometry: two persistent CTAs per SM, each with its own pipeline.  One
+// MMA-issuing thread per CTA cannot issue the 12 tcgen05 instructions of a stage
+// (8 scale copies + 4 MMAs of 128x128x64) as fast as the weights stream in; two
+// CTAs double the issue rate per SM and the two pipelines overlap each other's
+// epilogues.
 constexpr int kBlockM = 128;            // UMMA M
 constexpr int kBlockN = 128;            // UMMA N and output tile width
 constexpr int kStageK = 256;            // FP4 elements per pipeline stage (128 bytes per row)
 constexpr int kUmmaK = 64;              // K per tcgen05.mma (kind::mxf4nvf4, scale_vec::4X)
-constexpr int kStages = 6;
+#ifndef NVFP4_GEMM_STAGES
+#define NVFP4_GEMM_STAGES 3
+#endif
+constexpr int kStages = NVFP4_GEMM_STAGES;
+constexpr int kCtasPerSm = 2;
+constexpr int kAccBufs = 1;             // TMEM accumulators per CTA
 constexpr int kABoxRows = 32;           // A rows per TMA box (only boxes with live rows load)
 constexpr int kTileBytesA = kBlockM * kStageK / 2;   // 16 KiB
 constexpr int kTileBytesB = kBlockN * kStageK / 2;   // 16 KiB
 constexpr int kSfBytesPerKStep = 512;   // 128 rows x 4 scales
 constexpr int kSfBytesStage = kSfBytesPerKStep * (kStageK / kUmmaK);  // 2 KiB
 constexpr int kGemmThreads = 192;       // warp 0 TMA, warp 1 MMA, warps 2..5 epilogue
-constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kTmemAccCols = 2 * kBlockN;       // two accumulator buffers
+constexpr uint32_t kTmemAccCols = kAccBufs * kBlockN;
 constexpr uint32_t kTmemSfCols = 32;                 // per stage: 16 SFA + 16 SFB columns
+constexpr uint32_t kTmemCols = 256;                  // per CTA: 128 accumulator + 96 scale columns
+static_assert(kTmemAccCols + kStages * kTmemSfCols <= kTmemCols, "TMEM budget");
+static_assert(kCtasPerSm * kTmemCols <= 512, "two CTAs share the SM's 512 TMEM columns");
 
 constexpr size_t kGemmSmemBytes =
     1024 /* alignment slack */ +
