@@ -215,6 +215,7 @@ typedef struct nvfp4_moe_ws_layout {
   size_t tile_offsets;  /* int32 [G+1]      exclusive scan of ceil(counts / 128)     */
   size_t sorted_idx;    /* int32 [T*topk]                                            */
   size_t inv_idx;       /* int32 [T*topk]                                            */
+  size_t dest_rows;     /* int32 [T*topk]   permuted row of each flat entry (-1 dropped) */
   size_t amax_partials; /* uint32 [1024]    block maxima of |x| as bf16 bits         */
   size_t xq;            /* uint8 [rows_capacity, H/2]  x quantised, permuted rows    */
   size_t xsf;           /* uint8 nvfp4_sf_bytes(rows_capacity, H)                    */

@@ -38,7 +38,7 @@ LINEAR_NOALLOC_MAX_BYTES = 4 << 20
 
 class MoeWsLayout(Structure):
     _fields_ = [(n, c_size_t) for n in ("counts", "offsets", "pad_offsets", "tile_offsets", "sorted_idx",
-                                         "inv_idx", "amax_partials", "xq", "xsf", "hq", "hsf", "y_acc", "total")]
+                                         "inv_idx", "dest_rows", "amax_partials", "xq", "xsf", "hq", "hsf", "y_acc", "total")]
     _fields_ += [("rows_capacity", c_int64)]
 
 

@@ -176,6 +176,7 @@ nvfp4_moe_ws_layout moe_layout(int64_t T, int64_t H, int64_t I, int64_t E, int t
   L.tile_offsets = take(static_cast<size_t>(G + 1) * 4);
   L.sorted_idx = take(static_cast<size_t>(Tk > 0 ? Tk : 1) * 4);
   L.inv_idx = take(static_cast<size_t>(Tk > 0 ? Tk : 1) * 4);
+  L.dest_rows = take(static_cast<size_t>(Tk > 0 ? Tk : 1) * 4);
   L.amax_partials = take(kMaxPartials * 4);
   L.xq = take(rc * static_cast<size_t>(H / 2));
   L.xsf = take(sf_bytes(L.rows_capacity, H));
@@ -220,6 +221,7 @@ RouteBufs route_bufs(void *ws, const nvfp4_moe_ws_layout &L) {
   rb.tile_offsets = at<int>(ws, L.tile_offsets);
   rb.sorted_idx = at<int>(ws, L.sorted_idx);
   rb.inv_idx = at<int>(ws, L.inv_idx);
+  rb.dest_rows = at<int>(ws, L.dest_rows);
   return rb;
 }
 
@@ -291,7 +293,7 @@ nvfp4_status moe_gemm_impl(const char *fn, DeviceInfo *d, Epi epi, int64_t T, in
     a.topk_w = topk_w;
     a.topk = topk;
   }
-  NV_CUDA(launch_gemm(epi, ta, tb, tbs, a, d->sms * kCtasPerSm, s), "grouped GEMM launch");
+  NV_CUDA(launch_gemm(epi, ta, tb, tbs, a, d->sms * kCtasPerSm, false, s), "grouped GEMM launch");
   return NVFP4_OK;
 }
 
@@ -428,7 +430,7 @@ static nvfp4_status gemm_dense(const char *fn, DeviceInfo *d, const uint8_t *xq,
   a.err = d->flags;
   const int64_t tiles = ((M + kBlockM - 1) / kBlockM) * (N / kBlockN);
   const int grid = static_cast<int>(tiles < d->sms * kCtasPerSm ? tiles : d->sms * kCtasPerSm);
-  NV_CUDA(launch_gemm(Epi::kLinear, ta, tb, tb, a, grid, s), "GEMM launch");
+  NV_CUDA(launch_gemm(Epi::kLinear, ta, tb, tb, a, grid, grid <= d->sms, s), "GEMM launch");
   return NVFP4_OK;
 }
 
@@ -549,7 +551,7 @@ nvfp4_status nvfp4_moe_route(const int32_t *ids, int64_t T, int topk, int64_t E,
   DeviceInfo *d;
   nvfp4_status st = device_info(__func__, &d);
   if (st != NVFP4_OK) return st;
-  RouteBufs rb{counts, offsets, nullptr, nullptr, sorted_idx, inv_idx};
+  RouteBufs rb{counts, offsets, nullptr, nullptr, sorted_idx, inv_idx, nullptr};
   NV_CUDA(launch_route_amax(ids, static_cast<int>(T), topk, static_cast<int>(E), 0, rb, nullptr, 0, nullptr, 0,
                             nullptr, d->flags, static_cast<cudaStream_t>(stream)),
           "route kernel launch");

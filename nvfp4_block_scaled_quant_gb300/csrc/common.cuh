@@ -30,6 +30,11 @@ __device__ __forceinline__ void raise_device_error(uint32_t *err, uint32_t flag)
   if (err) atomicOr(err, flag);
 }
 
+// Programmatic dependent launch: wait for the previous grid on the stream to complete
+// (and its writes to be visible); allow the next grid to start launching.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // ---------------------------------------------------------------- mbarrier
 
 __device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {

@@ -89,6 +89,7 @@ __global__ void __launch_bounds__(kGemmThreads, kCtasPerSm)
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_holder + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  pdl_trigger();
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
@@ -117,6 +118,8 @@ __global__ void __launch_bounds__(kGemmThreads, kCtasPerSm)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_holder;
+  // everything above overlaps the previous kernel; inputs are read only after it completes
+  pdl_wait();
 
   const int n_tiles = args.N / kBlockN;
   const int k_steps = args.K / kUmmaK;
@@ -375,6 +378,8 @@ __global__ void __launch_bounds__(kGemmThreads, kCtasPerSm)
 // Bounded-wait probe: one thread waits on a barrier that never completes.
 __global__ void wait_timeout_probe_kernel(uint64_t timeout_ns, uint32_t *err) {
   __shared__ uint64_t bar;
+  pdl_trigger();
+  pdl_wait();
   __shared__ int abort_flag;
   if (threadIdx.x == 0) {
     mbar_init(&bar, 1);
@@ -390,32 +395,35 @@ __global__ void wait_timeout_probe_kernel(uint64_t timeout_ns, uint32_t *err) {
 
 template <int kEpi>
 cudaError_t launch_gemm_t(const CUtensorMap &ta, const CUtensorMap &tb, const CUtensorMap &tbs,
-                          const GemmArgs &args, int grid, cudaStream_t s) {
+                          const GemmArgs &args, int grid, bool one_per_sm, cudaStream_t s) {
   static bool attr_done[64] = {false};
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 64 && !attr_done[dev]) {
     cudaError_t e = cudaFuncSetAttribute(nvfp4_gemm_kernel<kEpi>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(kGemmSmemBytes));
+                                         static_cast<int>(kGemmSmemBytesSolo));
     if (e != cudaSuccess) return e;
     attr_done[dev] = true;
   }
-  nvfp4_gemm_kernel<kEpi><<<grid, kGemmThreads, kGemmSmemBytes, s>>>(ta, tb, tbs, args);
-  return cudaGetLastError();
+  // A grid no larger than the SM count asks for enough shared memory to keep one CTA per
+  // SM, so its tiles spread over as many SMs as there are tiles.
+  return launch_pdl(nvfp4_gemm_kernel<kEpi>, dim3(grid), dim3(kGemmThreads),
+                    one_per_sm ? kGemmSmemBytesSolo : kGemmSmemBytes, s, ta, tb, tbs, args);
 }
 
 }  // namespace
 
 cudaError_t launch_gemm(Epi epi, const CUtensorMap &ta, const CUtensorMap &tb,
-                        const CUtensorMap &tbs, const GemmArgs &args, int grid, cudaStream_t s) {
+                        const CUtensorMap &tbs, const GemmArgs &args, int grid, bool one_per_sm,
+                        cudaStream_t s) {
   switch (epi) {
     case Epi::kLinear:
-      return launch_gemm_t<static_cast<int>(Epi::kLinear)>(ta, tb, tbs, args, grid, s);
+      return launch_gemm_t<static_cast<int>(Epi::kLinear)>(ta, tb, tbs, args, grid, one_per_sm, s);
     case Epi::kW13:
-      return launch_gemm_t<static_cast<int>(Epi::kW13)>(ta, tb, tbs, args, grid, s);
+      return launch_gemm_t<static_cast<int>(Epi::kW13)>(ta, tb, tbs, args, grid, one_per_sm, s);
     case Epi::kW2:
-      return launch_gemm_t<static_cast<int>(Epi::kW2)>(ta, tb, tbs, args, grid, s);
+      return launch_gemm_t<static_cast<int>(Epi::kW2)>(ta, tb, tbs, args, grid, one_per_sm, s);
   }
   return cudaErrorInvalidValue;
 }

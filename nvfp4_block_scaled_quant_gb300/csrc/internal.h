@@ -46,6 +46,9 @@ constexpr size_t kGemmSmemBytes =
     1024 /* alignment slack */ +
     static_cast<size_t>(kStages) * (kTileBytesA + kTileBytesB + 2 * kSfBytesStage) +
     256 /* barriers and flags */;
+// Requested (not used) by launches that want one CTA per SM: two of these do not fit.
+constexpr size_t kGemmSmemBytesSolo = 2 * kGemmSmemBytes;
+static_assert(kGemmSmemBytesSolo <= 232448, "per-block shared memory limit");
 
 enum class Epi : int { kLinear = 0, kW13 = 1, kW2 = 2 };
 
@@ -80,6 +83,26 @@ struct GemmArgs {
   uint32_t *err;            // device fault flags
 };
 
+// Launch with programmatic dependent launch allowed: the kernel may start while the
+// previous kernel on the stream is finishing.  Every kernel of the library therefore
+// runs griddepcontrol.wait before it reads any global input, and triggers its own
+// dependents at its start.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                       Args &&...args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
 // launchers (return cudaError_t of the launch)
 cudaError_t launch_amax_partials(const void *x, int64_t M, int64_t K, int64_t ldx,
                                  uint32_t *partials, int nparts, cudaStream_t s);
@@ -92,7 +115,7 @@ cudaError_t launch_prepare(const uint8_t *w, const uint8_t *sf, int64_t G, int64
                            int flags, uint8_t *w_out, uint8_t *sf_out, cudaStream_t s);
 
 struct RouteBufs {
-  int *counts, *offsets, *pad_offsets, *tile_offsets, *sorted_idx, *inv_idx;
+  int *counts, *offsets, *pad_offsets, *tile_offsets, *sorted_idx, *inv_idx, *dest_rows;
 };
 cudaError_t launch_route_amax(const int32_t *ids, int T, int topk, int E, int has_shared,
                               RouteBufs rb, const void *x, int64_t H, uint32_t *partials,
@@ -103,7 +126,8 @@ cudaError_t launch_dispatch_quant(const void *x, int T, int64_t H, int topk, int
                                   float *gs_out, uint8_t *xq, uint8_t *xsf, cudaStream_t s);
 cudaError_t launch_finalize(const float *y_acc, int64_t n, void *y, cudaStream_t s);
 cudaError_t launch_gemm(Epi epi, const CUtensorMap &ta, const CUtensorMap &tb,
-                        const CUtensorMap &tbs, const GemmArgs &args, int grid, cudaStream_t s);
+                        const CUtensorMap &tbs, const GemmArgs &args, int grid, bool one_per_sm,
+                        cudaStream_t s);
 cudaError_t launch_wait_timeout_probe(uint32_t timeout_us, uint32_t *err, cudaStream_t s);
 
 }  // namespace nvfp4

@@ -41,6 +41,8 @@ __global__ void __launch_bounds__(kAmaxThreads) amax_partials_kernel(const uint1
                                                                      int64_t ldx,
                                                                      uint32_t *__restrict__ partials) {
   __shared__ uint32_t scratch[32];
+  pdl_trigger();
+  pdl_wait();
   const int64_t chunks = K / 8;
   uint32_t m = 0;
   for (int64_t r = blockIdx.x; r < M; r += gridDim.x) {
@@ -63,6 +65,8 @@ __global__ void __launch_bounds__(kQuantThreads) quantize_kernel(
     float *__restrict__ gs_out, uint8_t *__restrict__ q, uint8_t *__restrict__ sf,
     int sf_layout, int64_t rows_total) {
   __shared__ uint32_t scratch[32];
+  pdl_trigger();
+  pdl_wait();
   float gs;
   if (partials) {
     gs = gs_from_partials(partials, nparts, scratch);
@@ -117,6 +121,8 @@ __device__ __forceinline__ int64_t interleave_src_row(int64_t n, int64_t N, int 
 __global__ void prepare_kernel(const uint8_t *__restrict__ w, const uint8_t *__restrict__ sf,
                                int64_t G, int64_t N, int64_t K, int flags,
                                uint8_t *__restrict__ w_out, uint8_t *__restrict__ sf_out) {
+  pdl_trigger();
+  pdl_wait();
   const int64_t row_chunks = K / 32;              // 16-byte chunks per packed row
   const int64_t code_items = G * N * row_chunks;
   const int64_t words_per_group = N * K / 64;     // 4 scales per word
@@ -153,9 +159,8 @@ int amax_partial_count(int64_t M, int64_t K) {
 
 cudaError_t launch_amax_partials(const void *x, int64_t M, int64_t K, int64_t ldx,
                                  uint32_t *partials, int nparts, cudaStream_t s) {
-  amax_partials_kernel<<<nparts, kAmaxThreads, 0, s>>>(static_cast<const uint16_t *>(x), M, K,
-                                                       ldx, partials);
-  return cudaGetLastError();
+  return launch_pdl(amax_partials_kernel, dim3(nparts), dim3(kAmaxThreads), 0, s,
+                    static_cast<const uint16_t *>(x), M, K, ldx, partials);
 }
 
 cudaError_t launch_quantize(const void *x, int64_t M, int64_t K, int64_t ldx,
@@ -165,10 +170,9 @@ cudaError_t launch_quantize(const void *x, int64_t M, int64_t K, int64_t ldx,
   const int64_t rows_total = sf_layout == NVFP4_SF_LINEAR ? M : ((M + 127) / 128) * 128;
   const int64_t items = rows_total * (K / 16);
   const int64_t blocks = items > 0 ? (items + kQuantThreads - 1) / kQuantThreads : 1;
-  quantize_kernel<<<static_cast<unsigned>(blocks), kQuantThreads, 0, s>>>(
-      static_cast<const uint16_t *>(x), M, K, ldx, partials, nparts, gs_static, gs_out, q, sf,
-      sf_layout, rows_total);
-  return cudaGetLastError();
+  return launch_pdl(quantize_kernel, dim3(static_cast<unsigned>(blocks)), dim3(kQuantThreads), 0, s,
+                    static_cast<const uint16_t *>(x), M, K, ldx, partials, nparts, gs_static, gs_out, q, sf,
+                    sf_layout, rows_total);
 }
 
 cudaError_t launch_prepare(const uint8_t *w, const uint8_t *sf, int64_t G, int64_t N, int64_t K,
@@ -176,8 +180,7 @@ cudaError_t launch_prepare(const uint8_t *w, const uint8_t *sf, int64_t G, int64
   int dev = 0, sms = 148;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  prepare_kernel<<<sms * 8, 256, 0, s>>>(w, sf, G, N, K, flags, w_out, sf_out);
-  return cudaGetLastError();
+  return launch_pdl(prepare_kernel, dim3(sms * 8), dim3(256), 0, s, w, sf, G, N, K, flags, w_out, sf_out);
 }
 
 }  // namespace nvfp4

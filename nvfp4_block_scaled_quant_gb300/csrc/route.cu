@@ -9,6 +9,7 @@ namespace {
 
 constexpr int kRouteThreads = 512;
 constexpr int kDispatchThreads = 256;
+constexpr int kRouteChunk = 2048;  // ids staged in shared memory per ranking pass
 
 // Block-wide exclusive scan of three int sequences of length n (n <= 4 * blockDim).
 // Writes out_x[0..n] (n+1 entries, the last one the total; n >= 1); out_pad and
@@ -93,10 +94,14 @@ __global__ void __launch_bounds__(kRouteThreads) route_amax_kernel(
     const int32_t *__restrict__ ids, int T, int topk, int E, int has_shared, RouteBufs rb,
     const uint16_t *__restrict__ x, int64_t H, uint32_t *__restrict__ partials, int nparts,
     float *__restrict__ y_acc, uint32_t *err) {
+  pdl_trigger();
+  pdl_wait();
   if (blockIdx.x == 0) {
     __shared__ int s_cnt[kMaxExperts + 1];
     __shared__ int s_cursor[kMaxExperts];
+    __shared__ int s_delta[kMaxExperts];  // padded row - sorted position, per expert
     __shared__ int s_tmp[96];
+    __shared__ int s_ids[kRouteChunk];
     const int G = E + (has_shared ? 1 : 0);
     const int Tk = T * topk;
     for (int g = threadIdx.x; g < G; g += blockDim.x) s_cnt[g] = 0;
@@ -113,34 +118,48 @@ __global__ void __launch_bounds__(kRouteThreads) route_amax_kernel(
     for (int g = threadIdx.x; g < G; g += blockDim.x) rb.counts[g] = s_cnt[g];
     block_scan3(s_cnt, G, rb.offsets, rb.pad_offsets, rb.tile_offsets, s_tmp);
     __syncthreads();
-    for (int e = threadIdx.x; e < E; e += blockDim.x) s_cursor[e] = rb.offsets[e];
+    for (int e = threadIdx.x; e < E; e += blockDim.x) {
+      s_cursor[e] = rb.offsets[e];
+      s_delta[e] = rb.pad_offsets ? rb.pad_offsets[e] - rb.offsets[e] : 0;
+    }
     __syncthreads();
-    // Stable ranking: one warp walks the entries in order, 32 at a time; lanes
-    // holding the same expert get consecutive positions in flat order.
-    if (threadIdx.x < 32) {
-      const int lane = threadIdx.x;
-      for (int base = 0; base < Tk; base += 32) {
-        const int f = base + lane;
-        int e = f < Tk ? ids[f] : -1;
-        if (e < 0 || e >= E) e = -1;
-        const unsigned peers = __match_any_sync(0xffffffffu, e);
-        const int leader = __ffs(peers) - 1;
-        const int rank = __popc(peers & ((1u << lane) - 1u));
-        int start = 0;
-        if (lane == leader && e >= 0) {
-          start = s_cursor[e];
-          s_cursor[e] = start + __popc(peers);
-        }
-        start = __shfl_sync(0xffffffffu, start, leader);
-        if (f < Tk) {
-          if (e >= 0) {
-            rb.sorted_idx[start + rank] = f;
-            rb.inv_idx[f] = start + rank;
-          } else {
-            rb.inv_idx[f] = -1;
+    // Stable ranking: the ids are staged in shared memory chunk by chunk; one warp
+    // walks each chunk in order, 32 entries at a time, and lanes holding the same
+    // expert get consecutive positions in flat order.
+    for (int base = 0; base < Tk; base += kRouteChunk) {
+      const int n = min(kRouteChunk, Tk - base);
+      for (int i = threadIdx.x; i < n; i += blockDim.x) s_ids[i] = ids[base + i];
+      __syncthreads();
+      if (threadIdx.x < 32) {
+        const int lane = threadIdx.x;
+        for (int b = 0; b < n; b += 32) {
+          const int fl = b + lane;
+          int e = fl < n ? s_ids[fl] : -1;
+          if (e < 0 || e >= E) e = -1;
+          const unsigned peers = __match_any_sync(0xffffffffu, e);
+          const int leader = __ffs(peers) - 1;
+          const int rank = __popc(peers & ((1u << lane) - 1u));
+          int start = 0;
+          if (lane == leader && e >= 0) {
+            start = s_cursor[e];
+            s_cursor[e] = start + __popc(peers);
+          }
+          start = __shfl_sync(0xffffffffu, start, leader);
+          if (fl < n) {
+            const int f = base + fl;
+            if (e >= 0) {
+              const int pos = start + rank;
+              rb.sorted_idx[pos] = f;
+              rb.inv_idx[f] = pos;
+              if (rb.dest_rows) rb.dest_rows[f] = s_delta[e] + pos;
+            } else {
+              rb.inv_idx[f] = -1;
+              if (rb.dest_rows) rb.dest_rows[f] = -1;
+            }
           }
         }
       }
+      __syncthreads();
     }
     return;
   }
@@ -185,6 +204,8 @@ __global__ void __launch_bounds__(kDispatchThreads) dispatch_quant_kernel(
     int nparts, const float *__restrict__ gs_static, float *__restrict__ gs_out,
     uint8_t *__restrict__ xq, uint8_t *__restrict__ xsf) {
   __shared__ uint32_t scratch[32];
+  pdl_trigger();
+  pdl_wait();
   float gs;
   if (partials) {
     gs = gs_from_partials(partials, nparts, scratch);
@@ -218,17 +239,17 @@ __global__ void __launch_bounds__(kDispatchThreads) dispatch_quant_kernel(
   if (!valid) return;
   const uint2 cv = make_uint2(codes[0], codes[1]);
   const bool sf_writer = (lane & 3) == 0;
+  // destination rows: routed entries from the routing kernel, then the shared segment
+  const int *dest = rb.dest_rows + t * topk;
+#pragma unroll 4
   for (int j = 0; j <= topk; ++j) {
     int64_t p;
     if (j < topk) {
-      const int64_t f = t * topk + j;
-      const int pos = rb.inv_idx[f];
-      if (pos < 0) continue;
-      const int e = ids[f];
-      p = static_cast<int64_t>(rb.pad_offsets[e]) + (pos - rb.offsets[e]);
+      p = __ldg(dest + j);
+      if (p < 0) continue;
     } else {
       if (!has_shared) break;
-      p = static_cast<int64_t>(rb.pad_offsets[E]) + t;
+      p = static_cast<int64_t>(__ldg(rb.pad_offsets + E)) + t;
     }
     *reinterpret_cast<uint2 *>(xq + p * (H / 2) + c * 8) = cv;
     if (sf_writer) *reinterpret_cast<uint32_t *>(xsf + sf_word_offset(p, c >> 2, kb >> 2)) = word;
@@ -236,6 +257,8 @@ __global__ void __launch_bounds__(kDispatchThreads) dispatch_quant_kernel(
 }
 
 __global__ void finalize_kernel(const float4 *__restrict__ acc, int64_t n4, uint2 *__restrict__ y) {
+  pdl_trigger();
+  pdl_wait();
   for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n4;
        i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
     const float4 v = acc[i];
@@ -257,10 +280,8 @@ cudaError_t launch_route_amax(const int32_t *ids, int T, int topk, int E, int ha
   if (partials && helpers < nparts) helpers = nparts;
   if (helpers < 1) helpers = 1;
   if (helpers > 1024) helpers = 1024;
-  route_amax_kernel<<<1 + helpers, kRouteThreads, 0, s>>>(
-      ids, T, topk, E, has_shared, rb, static_cast<const uint16_t *>(x), H, partials, nparts,
-      y_acc, err);
-  return cudaGetLastError();
+  return launch_pdl(route_amax_kernel, dim3(1 + helpers), dim3(kRouteThreads), 0, s, ids, T, topk, E,
+                    has_shared, rb, static_cast<const uint16_t *>(x), H, partials, nparts, y_acc, err);
 }
 
 cudaError_t launch_dispatch_quant(const void *x, int T, int64_t H, int topk, int E,
@@ -269,10 +290,9 @@ cudaError_t launch_dispatch_quant(const void *x, int T, int64_t H, int topk, int
                                   float *gs_out, uint8_t *xq, uint8_t *xsf, cudaStream_t s) {
   const int64_t items = static_cast<int64_t>(T) * (H / 16);
   const int64_t blocks = items > 0 ? (items + kDispatchThreads - 1) / kDispatchThreads : 1;
-  dispatch_quant_kernel<<<static_cast<unsigned>(blocks), kDispatchThreads, 0, s>>>(
-      static_cast<const uint16_t *>(x), T, H, topk, E, has_shared, ids, rb, partials, nparts,
-      gs_static, gs_out, xq, xsf);
-  return cudaGetLastError();
+  return launch_pdl(dispatch_quant_kernel, dim3(static_cast<unsigned>(blocks)), dim3(kDispatchThreads), 0, s,
+                    static_cast<const uint16_t *>(x), T, H, topk, E, has_shared, ids, rb, partials, nparts,
+                    gs_static, gs_out, xq, xsf);
 }
 
 cudaError_t launch_finalize(const float *y_acc, int64_t n, void *y, cudaStream_t s) {
@@ -280,9 +300,8 @@ cudaError_t launch_finalize(const float *y_acc, int64_t n, void *y, cudaStream_t
   int64_t blocks = (n4 + 255) / 256;
   if (blocks < 1) blocks = 1;
   if (blocks > 4096) blocks = 4096;
-  finalize_kernel<<<static_cast<unsigned>(blocks), 256, 0, s>>>(
-      reinterpret_cast<const float4 *>(y_acc), n4, static_cast<uint2 *>(y));
-  return cudaGetLastError();
+  return launch_pdl(finalize_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, s,
+                    reinterpret_cast<const float4 *>(y_acc), n4, static_cast<uint2 *>(y));
 }
 
 }  // namespace nvfp4

@@ -95,7 +95,7 @@ def test_valid_call_without_a_gpu_fails_cleanly(L):
 def test_moe_workspace_layout(L, T, H, I, E, k, sh):
     lay = _lib.MoeWsLayout()
     assert L.nvfp4_moe_workspace_layout(T, H, I, E, k, sh, ctypes.byref(lay)) == 0
-    fields = ["counts", "offsets", "pad_offsets", "tile_offsets", "sorted_idx", "inv_idx", "amax_partials", "xq",
+    fields = ["counts", "offsets", "pad_offsets", "tile_offsets", "sorted_idx", "inv_idx", "dest_rows", "amax_partials", "xq",
               "xsf", "hq", "hsf", "y_acc", "total"]
     offs = [getattr(lay, f) for f in fields]
     assert offs == sorted(offs) and all(o % 256 == 0 for o in offs)

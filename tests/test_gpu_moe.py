@@ -72,6 +72,9 @@ def run_moe_check(x, ids, w, W: ops.MoEWeights, oe, tokens, shared: bool, strict
     np.testing.assert_array_equal(tiles, np.concatenate([[0], np.cumsum((want_counts + 127) // 128)]))
     np.testing.assert_array_equal(sorted_idx, ref.routing.sorted_idx)
     np.testing.assert_array_equal(inv_idx, ref.routing.inv_idx)
+    dest_rows = _region(ws, L.dest_rows, T * k, torch.int32).cpu().numpy()
+    flat_e = idsnp.reshape(-1)
+    np.testing.assert_array_equal(dest_rows, pad[flat_e] + ref.routing.inv_idx - offsets[flat_e])
 
     rc = L.rows_capacity
     xq = _region(ws, L.xq, rc * H // 2, torch.uint8).view(rc, H // 2)
