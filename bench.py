@@ -369,6 +369,21 @@ def run_secondary(state, args):
                     "hbm_gbs": b / (ms / 1e3) / 1e9, "hbm_frac": b / (ms / 1e3) / 1e9 / hbm,
                     "groups_mean": sum(a["groups"] for a in acct) / 16,
                     "note": "16 seeded routings cycled; weights streamed from HBM (> L2)"})
+    # whole prefill in one call: the 32 chunks' 4096 tokens at once (hot experts span many m tiles)
+    cfg = workloads.PREFILL_WHOLE
+    x, ids, w = workloads.prefill_whole(device="cpu")
+    acct = chunk_accounting(ids.numpy(), cfg)
+    xd, idd, wd = x.to(dev), ids.to(dev), w.to(dev)
+    wsw = ops.moe_workspace(cfg.T, cfg.H, cfg.I, cfg.E, cfg.topk, True, dev)
+    yw = torch.empty(cfg.T, cfg.H, dtype=torch.bfloat16, device=dev)
+    ms = time_fn(lambda: ops.moe_forward(xd, idd, wd, W, a2, workspace=wsw, out=yw), 10)
+    out.append({"workload": cfg.name, "tokens_per_s": cfg.T / (ms / 1e3), "ms_per_call": ms,
+                "hbm_gbs": acct["step_bytes"] / (ms / 1e3) / 1e9,
+                "hbm_frac": acct["step_bytes"] / (ms / 1e3) / 1e9 / hbm,
+                "tflops": acct["flops"] / (ms / 1e3) / 1e12,
+                "tensor_frac_fp4": acct["flops"] / (ms / 1e3) / 1e12 / fp4_peak, "groups": acct["groups"],
+                "note": "one call over the same 4096 tokens as the 32-chunk step"})
+    del wsw, xd, idd, wd, yw
     # dense linear K=1536 N=16384: 14 MB of weights fit in L2, so rotate 16 weight copies (> L2)
     K, N = 1536, 16384
     dws = [model.make_dense_weight(N, K, seed=50 + i, device=dev) for i in range(16)]

@@ -21,7 +21,13 @@
  *    *_workspace_bytes query returns; its contents need no initialisation.
  *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default
  *    stream).  Work is enqueued asynchronously; no call synchronises the host
- *    except nvfp4_get_device_error.
+ *    except nvfp4_get_device_error.  Kernels use programmatic dependent launch:
+ *    a kernel may start while the previous kernel on the stream finishes, and
+ *    reads its inputs only after that kernel completed.  The one exception is
+ *    that the GEMMs of nvfp4_linear and of the MoE stages read the weights and
+ *    the routing arrays one launch early.  Those must therefore be final before
+ *    the call that opens the chain (nvfp4_linear, nvfp4_moe_forward or
+ *    nvfp4_moe_dispatch) is enqueued, which ordinary stream order gives.
  *  - bf16 tensors are passed as void* to raw bf16 storage (row-major).
  *  - Scale-factor buffers in the "swizzled" tensor-core layout hold
  *    nvfp4_sf_bytes(rows, K) bytes: rows padded to a multiple of 128 and scale

@@ -281,6 +281,7 @@ nvfp4_status moe_gemm_impl(const char *fn, DeviceInfo *d, Epi epi, int64_t T, in
   a.ws2_shared = sh_ws2 ? sh_ws2 + (w13 ? 0 : 1) : nullptr;
   a.gs_out = gs_out;
   a.err = d->flags;
+  a.early_b = 1;  // dispatch (or w13) precedes this launch; routing and weights are older
   if (w13) {
     a.out = at<uint8_t>(ws, L.hq);
     a.out_sf = at<uint8_t>(ws, L.hsf);
@@ -408,7 +409,7 @@ size_t nvfp4_linear_workspace_bytes(int64_t M, int64_t K) {
 
 static nvfp4_status gemm_dense(const char *fn, DeviceInfo *d, const uint8_t *xq, const uint8_t *xsf, const float *gs,
                                int64_t M, int64_t K, int64_t N, const uint8_t *w, const uint8_t *w_sf,
-                               const float *ws2, void *y, cudaStream_t s) {
+                               const float *ws2, void *y, cudaStream_t s, int early_b = 0) {
   if (M == 0) return NVFP4_OK;
   CUtensorMap ta, tb;
   nvfp4_status st = make_map(fn, &ta, xq, K / 2, M, K / 2, kABoxRows);
@@ -428,6 +429,7 @@ static nvfp4_status gemm_dense(const char *fn, DeviceInfo *d, const uint8_t *xq,
   a.out = y;
   a.out_ld = static_cast<int>(N);
   a.err = d->flags;
+  a.early_b = early_b;
   const int64_t tiles = ((M + kBlockM - 1) / kBlockM) * (N / kBlockN);
   const int grid = static_cast<int>(tiles < d->sms * kCtasPerSm ? tiles : d->sms * kCtasPerSm);
   NV_CUDA(launch_gemm(Epi::kLinear, ta, tb, tb, a, grid, grid <= d->sms, s), "GEMM launch");
@@ -477,7 +479,8 @@ nvfp4_status nvfp4_linear(const void *x, int64_t M, int64_t K, int64_t N, const 
   if (dyn) NV_CUDA(launch_amax_partials(x, M, K, K, partials, nparts, s), "amax kernel launch");
   NV_CUDA(launch_quantize(x, M, K, K, partials, nparts, gs, gs, xq, xsf, NVFP4_SF_SWIZZLED, s),
           "quantize kernel launch");
-  return gemm_dense(__func__, d, xq, xsf, gs, M, K, N, w, w_sf, ws2, y, s);
+  // the quantise launch just before this GEMM runs after everything that wrote W
+  return gemm_dense(__func__, d, xq, xsf, gs, M, K, N, w, w_sf, ws2, y, s, 1);
 }
 
 // ---------------------------------------------------------------- no-allocation dense linear
@@ -534,7 +537,8 @@ nvfp4_status nvfp4_linear_noalloc(const void *x, int64_t M, int64_t K, int64_t N
   if (dyn) NV_CUDA(launch_amax_partials(x, M, K, K, partials, nparts, s), "amax kernel launch");
   NV_CUDA(launch_quantize(x, M, K, K, partials, nparts, gs, gs, xq, xsf, NVFP4_SF_SWIZZLED, s),
           "quantize kernel launch");
-  return gemm_dense(__func__, d, xq, xsf, gs, M, K, N, w, w_sf, ws2, y, s);
+  // the quantise launch just before this GEMM runs after everything that wrote W
+  return gemm_dense(__func__, d, xq, xsf, gs, M, K, N, w, w_sf, ws2, y, s, 1);
 }
 
 nvfp4_status nvfp4_moe_route(const int32_t *ids, int64_t T, int topk, int64_t E, int32_t *counts, int32_t *offsets,

@@ -31,7 +31,9 @@ __device__ __forceinline__ void raise_device_error(uint32_t *err, uint32_t flag)
 }
 
 // Programmatic dependent launch: wait for the previous grid on the stream to complete
-// (and its writes to be visible); allow the next grid to start launching.
+// (and its writes to be visible); allow the next grid to start launching.  Every kernel
+// of the library triggers only after its own wait returned, so when a library kernel
+// starts, every grid two or more launches back on the stream has completed.
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
@@ -52,6 +54,13 @@ __device__ __forceinline__ void fence_proxy_async_shared() {
 
 __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes) {
   asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+               "r"(bytes)
+               : "memory");
+}
+
+// Raise the expected transaction bytes of the current phase without arriving.
+__device__ __forceinline__ void mbar_expect_tx(uint64_t *bar, uint32_t bytes) {
+  asm volatile("mbarrier.expect_tx.relaxed.cta.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)),
                "r"(bytes)
                : "memory");
 }

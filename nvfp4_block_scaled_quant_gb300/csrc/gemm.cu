@@ -89,7 +89,6 @@ __global__ void __launch_bounds__(kGemmThreads, kCtasPerSm)
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_holder + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  pdl_trigger();
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
@@ -118,8 +117,13 @@ __global__ void __launch_bounds__(kGemmThreads, kCtasPerSm)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_holder;
-  // everything above overlaps the previous kernel; inputs are read only after it completes
-  pdl_wait();
+  // Everything above overlaps the previous kernel.  Its outputs (the A operand, the
+  // activation scale) are read only after pdl_wait; with early_b the producer first
+  // streams the weights of its first stages, which the calling chain wrote earlier.
+  if (!args.early_b || threadIdx.x != 0) {
+    pdl_wait();
+    pdl_trigger();
+  }
 
   const int n_tiles = args.N / kBlockN;
   const int k_steps = args.K / kUmmaK;
@@ -142,9 +146,34 @@ __global__ void __launch_bounds__(kGemmThreads, kCtasPerSm)
         sfb = (sh ? args.b_sf_shared : args.b_sf + static_cast<size_t>(t.g) * args.N * (args.K / 16)) +
               static_cast<size_t>(t.nt) * k_steps * kSfBytesPerKStep;
       };
+      // Weights of the first stages of this CTA's first tile, before the previous kernel ends.
+      int early = 0;
+      if (args.early_b) {
+        if (static_cast<int>(blockIdx.x) < total_tiles) {
+          Tile t;
+          decode_tile(args, blockIdx.x, n_tiles, t);
+          const CUtensorMap *mb;
+          int b_row0;
+          const uint8_t *sfb;
+          b_src(t, mb, b_row0, sfb);
+          const int group_rows = args.counts ? __ldg(args.counts + t.g) : args.dense_M;
+          const uint64_t pol_w = group_rows > kBlockM ? pol_reuse : pol_stream;
+          early = min(kStages, k_stages);
+          for (int s = 0; s < early; ++s) {
+            const int kv = min(4, k_steps - 4 * s);
+            mbar_expect_tx(&full[s], kTileBytesB + kv * kSfBytesPerKStep);
+            tma_load_2d(sB + s * kTileBytesB, mb, s * (kStageK / 2), b_row0, &full[s], pol_w);
+            bulk_load(sSFB + s * kSfBytesStage, sfb + static_cast<size_t>(s) * kSfBytesStage,
+                      kv * kSfBytesPerKStep, &full[s], pol_w);
+          }
+        }
+        pdl_wait();
+        pdl_trigger();
+      }
       int stage = 0;
       uint32_t phase = 0;
       uint32_t issued = 0;  // bit s: stage s has a load in flight with parity bit (s+8)
+      int n_issued = 0;     // stages issued so far (the first `early` already hold their B)
       bool ok = true;
       for (int idx = blockIdx.x; ok && idx < total_tiles; idx += gridDim.x) {
         Tile t;
@@ -165,18 +194,23 @@ __global__ void __launch_bounds__(kGemmThreads, kCtasPerSm)
             ok = false;
             break;
           }
-          mbar_arrive_expect_tx(&full[stage], nbox * (kABoxRows * kStageK / 2) + kTileBytesB +
-                                                  2 * kv * kSfBytesPerKStep);
+          const bool b_done = n_issued < early;
+          mbar_arrive_expect_tx(&full[stage],
+                                nbox * (kABoxRows * kStageK / 2) + kv * kSfBytesPerKStep +
+                                    (b_done ? 0 : kTileBytesB + kv * kSfBytesPerKStep));
           uint8_t *a_dst = sA + stage * kTileBytesA;
           for (int b = 0; b < nbox; ++b)
             tma_load_2d(a_dst + b * (kABoxRows * kStageK / 2), &tmA, ks * (kStageK / 2),
                         t.a_row0 + b * kABoxRows, &full[stage], pol_a);
-          tma_load_2d(sB + stage * kTileBytesB, mb, ks * (kStageK / 2), b_row0, &full[stage],
-                      pol_w);
           bulk_load(sSFA + stage * kSfBytesStage, sfa + static_cast<size_t>(ks) * kSfBytesStage,
                     kv * kSfBytesPerKStep, &full[stage], pol_a);
-          bulk_load(sSFB + stage * kSfBytesStage, sfb + static_cast<size_t>(ks) * kSfBytesStage,
-                    kv * kSfBytesPerKStep, &full[stage], pol_w);
+          if (!b_done) {
+            tma_load_2d(sB + stage * kTileBytesB, mb, ks * (kStageK / 2), b_row0, &full[stage],
+                        pol_w);
+            bulk_load(sSFB + stage * kSfBytesStage, sfb + static_cast<size_t>(ks) * kSfBytesStage,
+                      kv * kSfBytesPerKStep, &full[stage], pol_w);
+          }
+          ++n_issued;
           issued = (issued & ~(0x101u << stage)) | (1u << stage) | (phase << (stage + 8));
           if (++stage == kStages) {
             stage = 0;
@@ -269,8 +303,12 @@ __global__ void __launch_bounds__(kGemmThreads, kCtasPerSm)
       const bool row_ok = m < t.rows;
       const bool sh = t.g == args.shared_group;
       const float ws2 = sh ? __ldg(args.ws2_shared) : __ldg(args.ws2 + t.g);
+      // A warp whose 32 accumulator rows are all padding (a group's last m tile) has
+      // nothing to read or store; it only releases the accumulator.
+      const bool warp_live = quarter * 32 < t.rows;
 
-      if constexpr (kEpi == static_cast<int>(Epi::kLinear)) {
+      if (!warp_live) {
+      } else if constexpr (kEpi == static_cast<int>(Epi::kLinear)) {
         const float alpha = gs_scalar * ws2;
         const int64_t row = t.a_row0 + m;
         __nv_bfloat16 *y = static_cast<__nv_bfloat16 *>(args.out) +
@@ -378,8 +416,8 @@ __global__ void __launch_bounds__(kGemmThreads, kCtasPerSm)
 // Bounded-wait probe: one thread waits on a barrier that never completes.
 __global__ void wait_timeout_probe_kernel(uint64_t timeout_ns, uint32_t *err) {
   __shared__ uint64_t bar;
-  pdl_trigger();
   pdl_wait();
+  pdl_trigger();
   __shared__ int abort_flag;
   if (threadIdx.x == 0) {
     mbar_init(&bar, 1);

@@ -81,6 +81,9 @@ struct GemmArgs {
   const float *topk_w;      // W2
   int topk;                 // W2
   uint32_t *err;            // device fault flags
+  int early_b;              // 1: B tiles and the tile schedule may be read before the
+                            // previous kernel completes (the caller's chain guarantees
+                            // they were written two or more launches back)
 };
 
 // Launch with programmatic dependent launch allowed: the kernel may start while the

@@ -41,8 +41,8 @@ __global__ void __launch_bounds__(kAmaxThreads) amax_partials_kernel(const uint1
                                                                      int64_t ldx,
                                                                      uint32_t *__restrict__ partials) {
   __shared__ uint32_t scratch[32];
-  pdl_trigger();
   pdl_wait();
+  pdl_trigger();
   const int64_t chunks = K / 8;
   uint32_t m = 0;
   for (int64_t r = blockIdx.x; r < M; r += gridDim.x) {
@@ -65,8 +65,8 @@ __global__ void __launch_bounds__(kQuantThreads) quantize_kernel(
     float *__restrict__ gs_out, uint8_t *__restrict__ q, uint8_t *__restrict__ sf,
     int sf_layout, int64_t rows_total) {
   __shared__ uint32_t scratch[32];
-  pdl_trigger();
   pdl_wait();
+  pdl_trigger();
   float gs;
   if (partials) {
     gs = gs_from_partials(partials, nparts, scratch);
@@ -121,8 +121,8 @@ __device__ __forceinline__ int64_t interleave_src_row(int64_t n, int64_t N, int 
 __global__ void prepare_kernel(const uint8_t *__restrict__ w, const uint8_t *__restrict__ sf,
                                int64_t G, int64_t N, int64_t K, int flags,
                                uint8_t *__restrict__ w_out, uint8_t *__restrict__ sf_out) {
-  pdl_trigger();
   pdl_wait();
+  pdl_trigger();
   const int64_t row_chunks = K / 32;              // 16-byte chunks per packed row
   const int64_t code_items = G * N * row_chunks;
   const int64_t words_per_group = N * K / 64;     // 4 scales per word

@@ -94,8 +94,8 @@ __global__ void __launch_bounds__(kRouteThreads) route_amax_kernel(
     const int32_t *__restrict__ ids, int T, int topk, int E, int has_shared, RouteBufs rb,
     const uint16_t *__restrict__ x, int64_t H, uint32_t *__restrict__ partials, int nparts,
     float *__restrict__ y_acc, uint32_t *err) {
-  pdl_trigger();
   pdl_wait();
+  pdl_trigger();
   if (blockIdx.x == 0) {
     __shared__ int s_cnt[kMaxExperts + 1];
     __shared__ int s_cursor[kMaxExperts];
@@ -204,8 +204,8 @@ __global__ void __launch_bounds__(kDispatchThreads) dispatch_quant_kernel(
     int nparts, const float *__restrict__ gs_static, float *__restrict__ gs_out,
     uint8_t *__restrict__ xq, uint8_t *__restrict__ xsf) {
   __shared__ uint32_t scratch[32];
-  pdl_trigger();
   pdl_wait();
+  pdl_trigger();
   float gs;
   if (partials) {
     gs = gs_from_partials(partials, nparts, scratch);
@@ -257,8 +257,8 @@ __global__ void __launch_bounds__(kDispatchThreads) dispatch_quant_kernel(
 }
 
 __global__ void finalize_kernel(const float4 *__restrict__ acc, int64_t n4, uint2 *__restrict__ y) {
-  pdl_trigger();
   pdl_wait();
+  pdl_trigger();
   for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n4;
        i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
     const float4 v = acc[i];

@@ -1,6 +1,7 @@
 """Run one workload of the path a few times, for a profiler to attach to.
 
     python -m nvfp4_block_scaled_quant_gb300.profile_case moe --experts 64 --iters 3
+    python -m nvfp4_block_scaled_quant_gb300.profile_case decode --T 1 --experts 384 --iters 8
     python -m nvfp4_block_scaled_quant_gb300.profile_case gemm --M 4096 --iters 3
     python -m nvfp4_block_scaled_quant_gb300.profile_case linear --M 32 --iters 3
 
@@ -23,7 +24,8 @@ from . import build as B
 
 def main(argv=None):
     p = argparse.ArgumentParser()
-    p.add_argument("case", choices=["moe", "gemm", "linear"])
+    p.add_argument("case", choices=["moe", "decode", "gemm", "linear"])
+    p.add_argument("--T", type=int, default=1)
     p.add_argument("--experts", type=int, default=64)
     p.add_argument("--M", type=int, default=4096)
     p.add_argument("--iters", type=int, default=3)
@@ -44,6 +46,18 @@ def main(argv=None):
         for i in range(a.iters):
             x = workloads.activations(cfg.T, cfg.H, seed=700_000 + i, device=dev, outliers=True)
             ids, w = workloads.routing(sub, seed=800_000 + i, device=dev)
+            ops.moe_forward(x, ids, w, W, a2, workspace=ws, out=y)
+    elif a.case == "decode":
+        cfg = workloads.DECODE[a.T]
+        E = a.experts
+        W = model.make_moe_weights(E, cfg.H, cfg.I, workloads.BENCH_WEIGHT_SEED, dev, shared=True)
+        sub = workloads.MoEConfig("profile", a.T, cfg.H, cfg.I, E, cfg.topk, True, "uniform", False)
+        a2 = torch.full((E + 1,), 0.02, dtype=torch.float32, device=dev)
+        ws = ops.moe_workspace(a.T, cfg.H, cfg.I, E, cfg.topk, True, dev)
+        y = torch.empty(a.T, cfg.H, dtype=torch.bfloat16, device=dev)
+        for i in range(a.iters):
+            x = workloads.activations(a.T, cfg.H, seed=900_000 + i, device=dev)
+            ids, w = workloads.routing(sub, seed=950_000 + i, device=dev)
             ops.moe_forward(x, ids, w, W, a2, workspace=ws, out=y)
     elif a.case == "gemm":
         K = N = 7168

@@ -16,8 +16,9 @@ Recipes
 * routing ``uniform``: k distinct experts per token (seeded permutation
   prefix), weights softmax of N(0, 1) over the k slots;
 * routing ``zipf``: k distinct experts per token drawn by Gumbel-top-k from
-  p_e proportional to rank(e)^-s (rank a seeded permutation of the ids),
-  weights softmax of N(0, 1) over the k slots.
+  p_e proportional to rank(e)^-s (rank one seeded permutation of the ids per
+  workload, so the popular experts stay popular from chunk to chunk), weights
+  softmax of N(0, 1) over the k slots.
 """
 
 from __future__ import annotations
@@ -78,9 +79,12 @@ def routing_uniform(T: int, E: int, k: int, seed: int, device="cpu"):
     return ids.to(torch.int32).contiguous(), _slot_weights(T, k, g, device)
 
 
+ZIPF_RANK_SEED = 4242  # one expert-popularity ranking per workload, shared by all its chunks
+
+
 def routing_zipf(T: int, E: int, k: int, seed: int, device="cpu", s: float = 1.1):
+    rank = torch.randperm(E, generator=_gen(ZIPF_RANK_SEED, device), device=device).to(torch.float64) + 1.0
     g = _gen(seed, device)
-    rank = torch.randperm(E, generator=g, device=device).to(torch.float64) + 1.0
     logp = -s * torch.log(rank)
     u = torch.rand(T, E, generator=g, device=device, dtype=torch.float64).clamp_min(1e-300)
     gumbel = -torch.log(-torch.log(u))
@@ -136,3 +140,14 @@ def decode_step(T: int, step: int = 0, device="cpu"):
     x = activations(T, cfg.H, seed=900_000 + 100 * T + step, device=device)
     ids, w = routing(cfg, seed=950_000 + 100 * T + step, device=device)
     return x, ids, w
+
+
+PREFILL_WHOLE = MoEConfig("prefill_whole_moe_T4096_H7168_I2048_E384_k8_zipf1.1", 4096, 7168, 2048, 384, 8, True,
+                          "zipf", True)
+
+
+def prefill_whole(device="cpu"):
+    """The 32 prefill chunks' tokens and routings in one 4096-token call."""
+    parts = [prefill_chunk(c, device) for c in range(PREFILL.chunks)]
+    return (torch.cat([p[0] for p in parts]).contiguous(), torch.cat([p[1] for p in parts]).contiguous(),
+            torch.cat([p[2] for p in parts]).contiguous())

@@ -204,3 +204,51 @@ def test_moe_prefill_bench_chunk_sampled(big_weights, chunk):
     W, oe = big_weights
     x, ids, w = workloads.prefill_chunk(chunk, device="cpu")
     run_moe_check(x, ids, w, W, oe, [3, 127], True)
+
+
+def test_moe_prefill_whole_4096_sampled(big_weights):
+    """4096 tokens in one call: hot experts span many m tiles (their weights are re-read from L2)."""
+    W, oe = big_weights
+    x, ids, w = workloads.prefill_whole(device="cpu")
+    counts = np.bincount(ids.numpy().ravel(), minlength=384)
+    assert counts.max() > 1000  # the hottest expert spans 8+ m tiles
+    hot = int(np.argmax(counts))
+    tok_hot = int(np.nonzero((ids.numpy() == hot).any(axis=1))[0][-1])  # last row of the hottest expert
+    run_moe_check(x, ids, w, W, oe, [0, tok_hot], True)
+
+
+def test_moe_forward_cuda_graph_replay():
+    """nvfp4_moe_forward captured in a CUDA graph and replayed matches eager execution."""
+    cfg = workloads.TINY_SHARED
+    W = model.make_moe_weights(cfg.E, cfg.H, cfg.I, 108, DEV, shared=True)
+    ws = ops.moe_workspace(cfg.T, cfg.H, cfg.I, cfg.E, cfg.topk, True, DEV)
+    a2 = torch.full((cfg.E + 1,), 0.004, device=DEV)
+    x = workloads.activations(cfg.T, cfg.H, seed=1, device=DEV)
+    ids, w = workloads.routing(cfg, seed=2, device=DEV)
+    y = torch.empty(cfg.T, cfg.H, dtype=torch.bfloat16, device=DEV)
+    gs = torch.empty(1, device=DEV)
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        for _ in range(2):  # warm-up outside the capture (per-device set-up, kernel attributes)
+            ops.moe_forward(x, ids, w, W, a2, workspace=ws, out=y)
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    eager = y.clone()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        ops.moe_forward(x, ids, w, W, a2, workspace=ws, out=y)
+    y.zero_()
+    for _ in range(3):
+        g.replay()
+    torch.cuda.synchronize()
+    assert ops.device_error() == (0, 0)
+    # replays differ from eager only in the fp32 atomic summation order
+    np.testing.assert_allclose(bf16_to_np(y), bf16_to_np(eager), rtol=1e-2, atol=1e-3 * float(eager.float().abs().max()))
+    # new inputs in the captured buffers flow through the replay
+    x.copy_(workloads.activations(cfg.T, cfg.H, seed=3, device=DEV))
+    g.replay()
+    y2 = y.clone()
+    ops.moe_forward(x, ids, w, W, a2, workspace=ws, out=y)
+    torch.cuda.synchronize()
+    np.testing.assert_allclose(bf16_to_np(y2), bf16_to_np(y), rtol=1e-2, atol=1e-3 * float(y.float().abs().max()))
