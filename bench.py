@@ -407,6 +407,29 @@ def run_secondary(state, args):
                     "tflops": 2 * M * N * K / (ms / 1e3) / 1e12,
                     "note": "quantise + GEMM; 16 weight copies rotated (230 MB > L2)"})
     del dws
+    # fixed-group linear (grouped o-projection): 8 x (4096 -> 1024); 16 weight copies rotated (> L2)
+    for M in sorted(workloads.GROUPED_LINEAR):
+        _, G, K, N = workloads.GROUPED_LINEAR[M]
+        gws = [model.make_grouped_weight(G, N, K, seed=90 + i, device=dev) for i in range(16)]
+        x = workloads.activations(M, G * K, seed=95 + M, device=dev, outliers=True)
+        wsg = torch.empty(int(ops.lib().nvfp4_grouped_linear_workspace_bytes(M, G, K)), dtype=torch.uint8, device=dev)
+        y = torch.empty(M, G * N, dtype=torch.bfloat16, device=dev)
+        gs = torch.empty(1, dtype=torch.float32, device=dev)
+        it = [0]
+
+        def grp():
+            d = gws[it[0] % 16]
+            it[0] += 1
+            ops.call("nvfp4_grouped_linear", x.data_ptr(), M, G, K, N, d.w.data_ptr(), d.sf.data_ptr(),
+                     d.ws2.data_ptr(), 0, gs.data_ptr(), y.data_ptr(), wsg.data_ptr(), wsg.numel(), stream.cuda_stream)
+
+        ms = time_fn(grp, 160)
+        b = G * N * K * (0.5 + 1 / 16) + M * G * K * 2 + M * G * N * 2
+        out.append({"workload": f"grouped_linear_M{M}_G{G}_K{K}_N{N}", "us_per_call": ms * 1e3,
+                    "hbm_gbs": b / (ms / 1e3) / 1e9, "hbm_frac": b / (ms / 1e3) / 1e9 / hbm,
+                    "tflops": 2 * M * G * N * K / (ms / 1e3) / 1e12,
+                    "note": "quantise + grouped GEMM; 16 weight copies rotated (300 MB > L2)"})
+        del gws
     K = N = 7168
     dw = model.make_dense_weight(N, K, seed=70, device=dev)
     for M in (1024, 4096, 16384):

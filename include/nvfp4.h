@@ -184,6 +184,22 @@ NVFP4_API nvfp4_status nvfp4_gemm(const uint8_t *xq, const uint8_t *xsf, const f
                         int64_t K, int64_t N, const uint8_t *w, const uint8_t *w_sf,
                         const float *ws2, void *y, void *stream);
 
+/* ----------------------------------------------------- fixed-group linear
+ * The input features of x (M, G*K) bf16 split into G equal groups of K; group g
+ * multiplies its K columns by its own NVFP4 weight W_g (N, K/2) with ws2[g]:
+ *   y[:, g*N:(g+1)*N] = (gs * ws2[g]) * deq(xq[:, g*K:(g+1)*K]) @ deq(W_g)^T
+ * with one activation gs over all of x (gs_mode as for nvfp4_quantize_act).
+ * This is the grouped o-projection of page 3 (paragraph "The BF16 wo_a path was
+ * calling self.wo_a": a per-group BMM with in_features 4096; paragraph "Instead of
+ * fighting DeepGEMM": an NVFP4 grouped linear with n_local_groups = 8).  w is
+ * (G, N, K/2) prepared with NVFP4_PREP_PLAIN and w_sf G blocks of
+ * nvfp4_sf_bytes(N, K); ws2 (G) fp32; y (M, G*N) bf16.  K % 64 == 0, N % 128 == 0. */
+NVFP4_API size_t nvfp4_grouped_linear_workspace_bytes(int64_t M, int64_t G, int64_t K);
+NVFP4_API nvfp4_status nvfp4_grouped_linear(const void *x, int64_t M, int64_t G, int64_t K, int64_t N,
+                                            const uint8_t *w, const uint8_t *w_sf, const float *ws2,
+                                            int gs_mode, float *gs, void *y, void *ws,
+                                            size_t ws_bytes, void *stream);
+
 /* -------------------------------------------------------------- (b) routing
  * Groups the T*topk flat entries f = t*topk + j of ids (T, topk) int32 by
  * expert: counts[e] (E), offsets (E+1, exclusive prefix sum, int32 as the

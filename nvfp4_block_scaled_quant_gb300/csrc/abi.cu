@@ -274,6 +274,7 @@ nvfp4_status moe_gemm_impl(const char *fn, DeviceInfo *d, Epi epi, int64_t T, in
   a.tile_offsets = at<int>(ws, L.tile_offsets);
   a.shared_group = has_shared ? static_cast<int>(E) : -1;
   a.a_sf = at<uint8_t>(ws, w13 ? L.xsf : L.hsf);
+  a.a_kc_total = static_cast<int>(K / 64);
   a.b_sf = w_sf;
   a.b_sf_shared = sh_sf;
   a.gs_a = gs_a;
@@ -407,30 +408,35 @@ size_t nvfp4_linear_workspace_bytes(int64_t M, int64_t K) {
   return linear_ws(M, K).total;
 }
 
+// Dense GEMM, or G uniform groups where group g multiplies columns [gK, (g+1)K) of the
+// quantised activations with its own weight (G, N, K/2) into output columns [gN, (g+1)N).
 static nvfp4_status gemm_dense(const char *fn, DeviceInfo *d, const uint8_t *xq, const uint8_t *xsf, const float *gs,
                                int64_t M, int64_t K, int64_t N, const uint8_t *w, const uint8_t *w_sf,
-                               const float *ws2, void *y, cudaStream_t s, int early_b = 0) {
+                               const float *ws2, void *y, cudaStream_t s, int early_b = 0, int64_t G = 1) {
   if (M == 0) return NVFP4_OK;
   CUtensorMap ta, tb;
-  nvfp4_status st = make_map(fn, &ta, xq, K / 2, M, K / 2, kABoxRows);
+  nvfp4_status st = make_map(fn, &ta, xq, G * K / 2, M, G * K / 2, kABoxRows);
   if (st != NVFP4_OK) return st;
-  if ((st = make_map(fn, &tb, w, K / 2, N, K / 2, kBlockN)) != NVFP4_OK) return st;
+  if ((st = make_map(fn, &tb, w, K / 2, G * N, K / 2, kBlockN)) != NVFP4_OK) return st;
   GemmArgs a;
   std::memset(&a, 0, sizeof(a));
-  a.G = 1;
+  a.G = static_cast<int>(G);
   a.N = static_cast<int>(N);
   a.K = static_cast<int>(K);
   a.dense_M = static_cast<int>(M);
   a.shared_group = -1;
   a.a_sf = xsf;
+  a.a_kc_total = static_cast<int>(G * K / 64);
+  a.a_group_koff = G > 1 ? static_cast<int>(K / 64) : 0;
   a.b_sf = w_sf;
   a.gs_a = gs;
   a.ws2 = ws2;
   a.out = y;
-  a.out_ld = static_cast<int>(N);
+  a.out_ld = static_cast<int>(G * N);
+  a.out_group_cols = static_cast<int>(N);
   a.err = d->flags;
   a.early_b = early_b;
-  const int64_t tiles = ((M + kBlockM - 1) / kBlockM) * (N / kBlockN);
+  const int64_t tiles = G * ((M + kBlockM - 1) / kBlockM) * (N / kBlockN);
   const int grid = static_cast<int>(tiles < d->sms * kCtasPerSm ? tiles : d->sms * kCtasPerSm);
   NV_CUDA(launch_gemm(Epi::kLinear, ta, tb, tb, a, grid, grid <= d->sms, s), "GEMM launch");
   return NVFP4_OK;
@@ -539,6 +545,39 @@ nvfp4_status nvfp4_linear_noalloc(const void *x, int64_t M, int64_t K, int64_t N
           "quantize kernel launch");
   // the quantise launch just before this GEMM runs after everything that wrote W
   return gemm_dense(__func__, d, xq, xsf, gs, M, K, N, w, w_sf, ws2, y, s, 1);
+}
+
+size_t nvfp4_grouped_linear_workspace_bytes(int64_t M, int64_t G, int64_t K) {
+  if (M < 0 || G <= 0 || K < 0) return 0;
+  return linear_ws(M, G * K).total;
+}
+
+nvfp4_status nvfp4_grouped_linear(const void *x, int64_t M, int64_t G, int64_t K, int64_t N, const uint8_t *w,
+                                  const uint8_t *w_sf, const float *ws2, int gs_mode, float *gs, void *y, void *ws,
+                                  size_t ws_bytes, void *stream) {
+  NV_REQUIRE(G >= 1 && G <= 4096, NVFP4_ERR_INVALID_ARG, "G=%lld", (long long)G);
+  NV_CHECK_GEMM_SHAPE(M, G * K, G * N);
+  NV_REQUIRE(K % 64 == 0 && N % 128 == 0, NVFP4_ERR_UNSUPPORTED_SHAPE,
+             "K=%lld must be a multiple of 64 and N=%lld of 128", (long long)K, (long long)N);
+  NV_REQUIRE(gs_mode == NVFP4_GS_DYNAMIC || gs_mode == NVFP4_GS_STATIC, NVFP4_ERR_INVALID_ARG, "gs_mode %d", gs_mode);
+  NV_REQUIRE(gs && w && w_sf && ws2 && ((x && y) || M == 0), NVFP4_ERR_INVALID_ARG, "NULL pointer argument");
+  NV_REQUIRE(aligned(x, 16) && aligned(w, 16) && aligned(w_sf, 16) && aligned(y, 16) && aligned(gs, 4) &&
+                 aligned(ws2, 4),
+             NVFP4_ERR_MISALIGNED, "pointers must be 16-byte aligned");
+  const LinearWs L = linear_ws(M, G * K);
+  nvfp4_status st = check_ws(__func__, ws, ws_bytes, L.total);
+  if (st != NVFP4_OK) return st;
+  DeviceInfo *d;
+  if ((st = device_info(__func__, &d)) != NVFP4_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint8_t *xq = at<uint8_t>(ws, L.xq), *xsf = at<uint8_t>(ws, L.xsf);
+  const bool dyn = gs_mode == NVFP4_GS_DYNAMIC;
+  const int nparts = amax_partial_count(M, G * K);
+  uint32_t *partials = dyn ? at<uint32_t>(ws, L.partials) : nullptr;
+  if (dyn) NV_CUDA(launch_amax_partials(x, M, G * K, G * K, partials, nparts, s), "amax kernel launch");
+  NV_CUDA(launch_quantize(x, M, G * K, G * K, partials, nparts, gs, gs, xq, xsf, NVFP4_SF_SWIZZLED, s),
+          "quantize kernel launch");
+  return gemm_dense(__func__, d, xq, xsf, gs, M, K, N, w, w_sf, ws2, y, s, 1, G);
 }
 
 nvfp4_status nvfp4_moe_route(const int32_t *ids, int64_t T, int topk, int64_t E, int32_t *counts, int32_t *offsets,

@@ -40,11 +40,12 @@ struct Tile {
 __device__ __forceinline__ void decode_tile(const GemmArgs &a, int idx, int n_tiles, Tile &t) {
   const int mtg = idx / n_tiles;
   t.nt = idx - mtg * n_tiles;
-  if (a.counts == nullptr) {
-    t.g = 0;
-    t.mt = mtg;
-    t.rows = min(kBlockM, a.dense_M - mtg * kBlockM);
-    t.a_row0 = mtg * kBlockM;
+  if (a.counts == nullptr) {  // every group has dense_M rows (G == 1: a dense GEMM)
+    const int mt_per_group = (a.dense_M + kBlockM - 1) / kBlockM;
+    t.g = mtg / mt_per_group;
+    t.mt = mtg - t.g * mt_per_group;
+    t.rows = min(kBlockM, a.dense_M - t.mt * kBlockM);
+    t.a_row0 = t.mt * kBlockM;
     return;
   }
   // largest g with tile_offsets[g] <= mtg (empty groups have equal neighbours)
@@ -129,7 +130,7 @@ __global__ void __launch_bounds__(kGemmThreads, kCtasPerSm)
   const int k_steps = args.K / kUmmaK;
   const int k_stages = (k_steps + 3) / 4;
   const int total_mtiles = args.counts ? __ldg(args.tile_offsets + args.G)
-                                       : (args.dense_M + kBlockM - 1) / kBlockM;
+                                       : args.G * ((args.dense_M + kBlockM - 1) / kBlockM);
   const int total_tiles = total_mtiles * n_tiles;
 
   if (warp == 0) {
@@ -185,7 +186,9 @@ __global__ void __launch_bounds__(kGemmThreads, kCtasPerSm)
         const int group_rows = args.counts ? __ldg(args.counts + t.g) : args.dense_M;
         const uint64_t pol_w = group_rows > kBlockM ? pol_reuse : pol_stream;
         const uint8_t *sfa =
-            args.a_sf + static_cast<size_t>(t.a_row0 / kBlockM) * k_steps * kSfBytesPerKStep;
+            args.a_sf + (static_cast<size_t>(t.a_row0 / kBlockM) * args.a_kc_total +
+                         static_cast<size_t>(t.g) * args.a_group_koff) * kSfBytesPerKStep;
+        const int a_x0 = t.g * args.a_group_koff * (kUmmaK / 2);  // A byte column of this group
         const int nbox = (t.rows + kABoxRows - 1) / kABoxRows;
         for (int ks = 0; ks < k_stages; ++ks) {
           const int kv = min(4, k_steps - 4 * ks);
@@ -200,7 +203,7 @@ __global__ void __launch_bounds__(kGemmThreads, kCtasPerSm)
                                     (b_done ? 0 : kTileBytesB + kv * kSfBytesPerKStep));
           uint8_t *a_dst = sA + stage * kTileBytesA;
           for (int b = 0; b < nbox; ++b)
-            tma_load_2d(a_dst + b * (kABoxRows * kStageK / 2), &tmA, ks * (kStageK / 2),
+            tma_load_2d(a_dst + b * (kABoxRows * kStageK / 2), &tmA, a_x0 + ks * (kStageK / 2),
                         t.a_row0 + b * kABoxRows, &full[stage], pol_a);
           bulk_load(sSFA + stage * kSfBytesStage, sfa + static_cast<size_t>(ks) * kSfBytesStage,
                     kv * kSfBytesPerKStep, &full[stage], pol_a);
@@ -312,7 +315,8 @@ __global__ void __launch_bounds__(kGemmThreads, kCtasPerSm)
         const float alpha = gs_scalar * ws2;
         const int64_t row = t.a_row0 + m;
         __nv_bfloat16 *y = static_cast<__nv_bfloat16 *>(args.out) +
-                           row * static_cast<int64_t>(args.out_ld) + t.nt * kBlockN;
+                           row * static_cast<int64_t>(args.out_ld) +
+                           static_cast<int64_t>(t.g) * args.out_group_cols + t.nt * kBlockN;
 #pragma unroll 1
         for (int c = 0; c < kBlockN / 16; ++c) {
           uint32_t r[16];

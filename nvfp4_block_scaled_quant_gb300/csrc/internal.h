@@ -57,7 +57,7 @@ struct GemmArgs {
   int G;              // groups (1 for a dense GEMM)
   int N;              // output width per group, multiple of 128
   int K;              // reduction length, multiple of 64
-  int dense_M;        // rows of a dense GEMM (counts == nullptr)
+  int dense_M;        // rows of every group when counts == nullptr (dense / uniform groups)
   // grouped segments (device arrays written by the routing kernel)
   const int *counts;        // [G]
   const int *offsets;       // [G+1] unpadded (sorted order)
@@ -81,6 +81,10 @@ struct GemmArgs {
   const float *topk_w;      // W2
   int topk;                 // W2
   uint32_t *err;            // device fault flags
+  int a_kc_total;           // 64-element K steps per row in A's scale layout (>= K/64)
+  int a_group_koff;         // K steps of A skipped per group index (uniform groups splitting
+                            // A's columns); 0 when groups own separate A rows
+  int out_group_cols;       // Linear: output columns skipped per group index
   int early_b;              // 1: B tiles and the tile schedule may be read before the
                             // previous kernel completes (the caller's chain guarantees
                             // they were written two or more launches back)

@@ -69,3 +69,28 @@ def make_moe_weights(E: int, H: int, I: int, base_seed: int, device, shared: boo
         W.sh_w2, W.sh_w2_sf = ops.prepare_weights(q2, sf2, H, I, interleave_w13=False)
         W.sh_ws2 = torch.cat([g13, g2]).contiguous()
     return W
+
+
+@dataclass
+class GroupedWeight:
+    G: int
+    N: int
+    K: int
+    w: torch.Tensor       # prepared codes (G, N, K/2)
+    sf: torch.Tensor      # G swizzled scale blocks
+    ws2: torch.Tensor     # (G,) fp32
+
+
+def make_grouped_weight(G: int, N: int, K: int, seed: int, device) -> GroupedWeight:
+    """G independent bf16 N(0, 0.02) matrices (N, K), each quantised with its own ws2, then prepared."""
+    dev = torch.device(device)
+    ck = torch.empty(G, N, K // 2, dtype=torch.uint8, device=dev)
+    sf = torch.empty(G, N, K // 16, dtype=torch.uint8, device=dev)
+    ws2 = torch.empty(G, dtype=torch.float32, device=dev)
+    for g in range(G):
+        q, s, w2 = quantize_weight(workloads.weight(N, K, seed * 1009 + g, dev))
+        ck[g].copy_(q)
+        sf[g].copy_(s.view(N, K // 16))
+        ws2[g:g + 1].copy_(w2)
+    wp, sfp = ops.prepare_weights(ck, sf, N, K)
+    return GroupedWeight(G, N, K, wp, sfp, ws2)

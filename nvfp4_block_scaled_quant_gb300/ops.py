@@ -99,6 +99,24 @@ def linear(x: torch.Tensor, w: torch.Tensor, w_sf: torch.Tensor, ws2: torch.Tens
     return y, gs_t
 
 
+def grouped_linear(x: torch.Tensor, w: torch.Tensor, w_sf: torch.Tensor, ws2: torch.Tensor, G: int, N: int,
+                   gs: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
+                   stream=None) -> Tuple[torch.Tensor, torch.Tensor]:
+    """x (M, G*K) bf16, W (G, N, K/2) prepared -> y (M, G*N) bf16; group g uses x's K columns g."""
+    _cuda(x, w, w_sf, ws2, gs, workspace)
+    M, GK = x.shape
+    K = GK // G
+    y = torch.empty(M, G * N, dtype=torch.bfloat16, device=x.device)
+    dyn = gs is None
+    gs_t = torch.empty(1, dtype=torch.float32, device=x.device) if dyn else gs
+    ws_n = int(lib().nvfp4_grouped_linear_workspace_bytes(M, G, K))
+    ws = workspace if workspace is not None else _u8(ws_n, device=x.device)
+    call("nvfp4_grouped_linear", x.data_ptr(), M, G, K, N, w.data_ptr(), w_sf.data_ptr(), ws2.data_ptr(),
+         _lib.GS_DYNAMIC if dyn else _lib.GS_STATIC, gs_t.data_ptr(), y.data_ptr(), ws.data_ptr(), ws.numel(),
+         _stream(stream))
+    return y, gs_t
+
+
 def gemm(xq: torch.Tensor, xsf: torch.Tensor, gs: torch.Tensor, K: int, w: torch.Tensor, w_sf: torch.Tensor,
          ws2: torch.Tensor, N: int, out: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
     """GEMM alone on quantised activations xq (M, K/2) + swizzled xsf."""

@@ -151,3 +151,8 @@ def prefill_whole(device="cpu"):
     parts = [prefill_chunk(c, device) for c in range(PREFILL.chunks)]
     return (torch.cat([p[0] for p in parts]).contiguous(), torch.cat([p[1] for p in parts]).contiguous(),
             torch.cat([p[2] for p in parts]).contiguous())
+
+
+# Fixed-group linear (grouped o-projection): 8 groups of 4096 inputs each; the output width per
+# group is not printed on the pages, 1024 is taken (a multiple of the 128-wide tile).
+GROUPED_LINEAR = {M: (M, 8, 4096, 1024) for M in (1, 128)}   # (M, G, K, N)

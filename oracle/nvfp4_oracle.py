@@ -263,6 +263,24 @@ def linear(xq: Quantized, w_codes: np.ndarray, w_sf: np.ndarray, ws2: float) -> 
     return a @ b.T
 
 
+def grouped_linear(xq: Quantized, w_codes: Sequence[np.ndarray], w_sf: Sequence[np.ndarray],
+                   ws2: Sequence[float]) -> np.ndarray:
+    """Fixed-group linear: the input features split into G equal groups, group g of x times W_g.
+
+    y[:, g*N:(g+1)*N] = deq(xq[:, g*K:(g+1)*K]) @ deq(W_g)^T with W_g's own ws2 and the
+    activation's single gs (page 3, paragraph "The BF16 wo_a path was calling self.wo_a": wo_a is
+    a per-group BMM with in_features 4096 per group; paragraph "Instead of fighting DeepGEMM":
+    an NVFP4 grouped linear with n_local_groups = 8).
+    """
+    G = len(w_codes)
+    K = xq.codes.shape[1] // G
+    outs = []
+    for g in range(G):
+        xg = Quantized(xq.codes[:, g * K:(g + 1) * K], xq.sf[:, g * (K // BLOCK):(g + 1) * (K // BLOCK)], xq.gs)
+        outs.append(linear(xg, w_codes[g], w_sf[g], ws2[g]))
+    return np.concatenate(outs, axis=1)
+
+
 # ---------------------------------------------------------------------------
 # Routing
 # ---------------------------------------------------------------------------

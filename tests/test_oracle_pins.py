@@ -259,6 +259,21 @@ def test_ws2_is_weight_side_only():
     assert 1.0 / float(xq.gs) > 500  # with N(0,1) activations the error is a ~10^3x shrink
 
 
+def test_grouped_linear_is_block_diagonal_linear():
+    """G groups of K inputs -> N outputs each equal one linear with a block-diagonal weight."""
+    rng = np.random.default_rng(12)
+    M, G, K, N = 5, 3, 64, 32
+    xq = O.quantize(rng.standard_normal((M, G * K)).astype(np.float32))
+    ws = [O.quantize((rng.standard_normal((N, K)) * 0.02).astype(np.float32)) for _ in range(G)]
+    got = O.grouped_linear(xq, [w.codes for w in ws], [w.sf for w in ws], [w.gs for w in ws])
+    big = np.zeros((G * N, G * K))
+    for g, w in enumerate(ws):
+        big[g * N:(g + 1) * N, g * K:(g + 1) * K] = O.dequantize(w.codes, w.sf, w.gs)
+    want = O.dequantize(xq.codes, xq.sf, xq.gs) @ big.T
+    np.testing.assert_allclose(got, want, rtol=1e-12, atol=1e-15)
+    assert got.shape == (M, G * N)
+
+
 # --------------------------------------------------------------------------- SiLU
 
 def test_silu_closed_form_and_library():
