@@ -121,6 +121,26 @@ NVFP4_API nvfp4_status nvfp4_quantize_act(const void *x, int64_t M, int64_t K, i
                                 float *gs, uint8_t *q, uint8_t *sf, int sf_layout, void *ws,
                                 size_t ws_bytes, void *stream);
 
+/* -------------------------------------------------- RMSNorm -> quantize
+ * RMSNorm feeding the activation quantiser (the fused "P4" path of page 1, paragraph
+ * "Added --ab-compare flag", whose A/B harness compares x_normed, the global scale, the
+ * FP4 data and the GEMM outputs of the fused and unfused paths).  Per row r:
+ *   inv_r = 1 / sqrt(fl32(sum_k x^2) / K + eps)        (correctly rounded sqrt, divide)
+ *   x_normed[r,k] = bf16(fl32(fl32(x[r,k] * inv_r) * gamma[k]))
+ * gamma is a bf16 vector of K.  nvfp4_rmsnorm writes x_normed (M, K) bf16 (the unfused
+ * path; quantise it with nvfp4_quantize_act).  nvfp4_rmsnorm_quantize quantises x_normed
+ * without a round trip through memory, with the same arguments and results as
+ * nvfp4_quantize_act applied to nvfp4_rmsnorm's output (codes, scales and dynamic gs
+ * bit-identical); x_normed, if not NULL, also receives the normalised rows.  Two launches.
+ * Workspace: amax partials and the per-row inv_r. */
+NVFP4_API size_t nvfp4_rmsnorm_quantize_workspace_bytes(int64_t M, int64_t K);
+NVFP4_API nvfp4_status nvfp4_rmsnorm(const void *x, int64_t M, int64_t K, int64_t ldx, const void *gamma,
+                                     float eps, void *y, void *stream);
+NVFP4_API nvfp4_status nvfp4_rmsnorm_quantize(const void *x, int64_t M, int64_t K, int64_t ldx,
+                                              const void *gamma, float eps, int gs_mode, float *gs,
+                                              uint8_t *q, uint8_t *sf, int sf_layout, void *x_normed,
+                                              void *ws, size_t ws_bytes, void *stream);
+
 /* ------------------------------------------------------------ weight prepare
  * Checkpoint-layout weights of G groups (experts): codes w (G, N, K/2) and
  * row-major E4M3 scales sf (G, N, K/16) used as stored, no transpose (page 2,

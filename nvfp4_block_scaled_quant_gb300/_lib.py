@@ -9,7 +9,7 @@ import ctypes
 import os
 import re
 import threading
-from ctypes import POINTER, Structure, c_char_p, c_int, c_int32, c_int64, c_size_t, c_uint32, c_void_p
+from ctypes import POINTER, Structure, c_char_p, c_float, c_int, c_int32, c_int64, c_size_t, c_uint32, c_void_p
 
 HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(HERE, "libnvfp4_gb300.so")
@@ -53,6 +53,9 @@ _SIGNATURES = {
     "nvfp4_quantize_workspace_bytes": (c_size_t, [I64, I64]),
     "nvfp4_quantize_act": (c_int, [P, I64, I64, I64, c_int, P, P, P, c_int, P, c_size_t, P]),
     "nvfp4_prepare_weights": (c_int, [P, P, I64, I64, I64, c_int, P, P, P]),
+    "nvfp4_rmsnorm_quantize_workspace_bytes": (c_size_t, [I64, I64]),
+    "nvfp4_rmsnorm": (c_int, [P, I64, I64, I64, P, c_float, P, P]),
+    "nvfp4_rmsnorm_quantize": (c_int, [P, I64, I64, I64, P, c_float, c_int, P, P, P, c_int, P, P, c_size_t, P]),
     "nvfp4_linear_workspace_bytes": (c_size_t, [I64, I64]),
     "nvfp4_linear": (c_int, [P, I64, I64, I64, P, P, P, c_int, P, P, P, c_size_t, P]),
     "nvfp4_gemm": (c_int, [P, P, P, I64, I64, I64, P, P, P, P, P]),

@@ -383,6 +383,69 @@ nvfp4_status nvfp4_quantize_act(const void *x, int64_t M, int64_t K, int64_t ldx
   return NVFP4_OK;
 }
 
+size_t nvfp4_rmsnorm_quantize_workspace_bytes(int64_t M, int64_t K) {
+  (void)K;
+  if (M < 0) return 0;
+  return align256(kMaxPartials * sizeof(uint32_t)) + align256(static_cast<size_t>(M) * sizeof(float));
+}
+
+static nvfp4_status check_norm_args(const char *fn, const void *x, int64_t M, int64_t K, int64_t ldx,
+                                    const void *gamma, float eps) {
+  if (!(M >= 0 && K > 0)) return fail(NVFP4_ERR_INVALID_ARG, fn, "M=%lld K=%lld", (long long)M, (long long)K);
+  if (K % 64) return fail(NVFP4_ERR_UNSUPPORTED_SHAPE, fn, "K=%lld must be a multiple of 64", (long long)K);
+  if (!gamma || (!x && M > 0)) return fail(NVFP4_ERR_INVALID_ARG, fn, "NULL pointer argument");
+  if (!(eps >= 0.f) || !(eps < 1e30f)) return fail(NVFP4_ERR_INVALID_ARG, fn, "eps must be finite and >= 0");
+  if (ldx < K || ldx % 8) return fail(NVFP4_ERR_MISALIGNED, fn, "ldx=%lld must be >= K and a multiple of 8",
+                                      (long long)ldx);
+  if (!aligned(x, 16) || !aligned(gamma, 16)) return fail(NVFP4_ERR_MISALIGNED, fn, "x and gamma must be 16-byte aligned");
+  return NVFP4_OK;
+}
+
+nvfp4_status nvfp4_rmsnorm(const void *x, int64_t M, int64_t K, int64_t ldx, const void *gamma, float eps, void *y,
+                           void *stream) {
+  nvfp4_status st = check_norm_args(__func__, x, M, K, ldx, gamma, eps);
+  if (st != NVFP4_OK) return st;
+  NV_REQUIRE(y || M == 0, NVFP4_ERR_INVALID_ARG, "y is NULL");
+  NV_REQUIRE(aligned(y, 16), NVFP4_ERR_MISALIGNED, "y must be 16-byte aligned");
+  DeviceInfo *d;
+  if ((st = device_info(__func__, &d)) != NVFP4_OK) return st;
+  if (M == 0) return NVFP4_OK;
+  NV_CUDA(launch_rmsnorm_stats(x, M, K, ldx, gamma, eps, nullptr, nullptr, amax_partial_count(M, K), y,
+                               static_cast<cudaStream_t>(stream)),
+          "rmsnorm kernel launch");
+  return NVFP4_OK;
+}
+
+nvfp4_status nvfp4_rmsnorm_quantize(const void *x, int64_t M, int64_t K, int64_t ldx, const void *gamma, float eps,
+                                    int gs_mode, float *gs, uint8_t *q, uint8_t *sf, int sf_layout, void *x_normed,
+                                    void *ws, size_t ws_bytes, void *stream) {
+  nvfp4_status st = check_norm_args(__func__, x, M, K, ldx, gamma, eps);
+  if (st != NVFP4_OK) return st;
+  NV_REQUIRE(gs_mode == NVFP4_GS_DYNAMIC || gs_mode == NVFP4_GS_STATIC, NVFP4_ERR_INVALID_ARG, "gs_mode %d", gs_mode);
+  NV_REQUIRE(sf_layout == NVFP4_SF_SWIZZLED || sf_layout == NVFP4_SF_LINEAR, NVFP4_ERR_INVALID_ARG, "sf_layout %d",
+             sf_layout);
+  NV_REQUIRE(gs && ((q && sf) || M == 0), NVFP4_ERR_INVALID_ARG, "NULL pointer argument");
+  NV_REQUIRE(aligned(q, 16) && aligned(sf, 16) && aligned(x_normed, 16) && aligned(gs, 4), NVFP4_ERR_MISALIGNED,
+             "q, sf and x_normed must be 16-byte aligned");
+  if ((st = check_ws(__func__, ws, ws_bytes, nvfp4_rmsnorm_quantize_workspace_bytes(M, K))) != NVFP4_OK) return st;
+  DeviceInfo *d;
+  if ((st = device_info(__func__, &d)) != NVFP4_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const bool dyn = gs_mode == NVFP4_GS_DYNAMIC;
+  const int nparts = amax_partial_count(M, K);
+  uint32_t *partials = dyn ? static_cast<uint32_t *>(ws) : nullptr;
+  float *inv_rms = at<float>(ws, align256(kMaxPartials * sizeof(uint32_t)));
+  if (M > 0)
+    NV_CUDA(launch_rmsnorm_stats(x, M, K, ldx, gamma, eps, inv_rms, partials, nparts, x_normed, s),
+            "rmsnorm statistics kernel launch");
+  else if (dyn)
+    NV_CUDA(launch_amax_partials(x, 0, K, ldx, partials, 1, s), "amax kernel launch");
+  NV_CUDA(launch_rmsnorm_quantize(x, M, K, ldx, gamma, inv_rms, partials, M > 0 ? nparts : 1, gs, gs, q, sf, sf_layout,
+                                  s),
+          "rmsnorm quantize kernel launch");
+  return NVFP4_OK;
+}
+
 nvfp4_status nvfp4_prepare_weights(const uint8_t *w, const uint8_t *sf, int64_t G, int64_t N, int64_t K, int flags,
                                    uint8_t *w_out, uint8_t *sf_out, void *stream) {
   NV_REQUIRE(w && sf && w_out && sf_out, NVFP4_ERR_INVALID_ARG, "NULL pointer argument");

@@ -118,6 +118,12 @@ cudaError_t launch_quantize(const void *x, int64_t M, int64_t K, int64_t ldx,
                             const uint32_t *partials, int nparts, const float *gs_static,
                             float *gs_out, uint8_t *q, uint8_t *sf, int sf_layout,
                             cudaStream_t s);
+cudaError_t launch_rmsnorm_stats(const void *x, int64_t M, int64_t K, int64_t ldx, const void *gamma, float eps,
+                                 float *inv_rms, uint32_t *partials, int nparts, void *y, cudaStream_t s);
+cudaError_t launch_rmsnorm_quantize(const void *x, int64_t M, int64_t K, int64_t ldx, const void *gamma,
+                                    const float *inv_rms, const uint32_t *partials, int nparts,
+                                    const float *gs_static, float *gs_out, uint8_t *q, uint8_t *sf, int sf_layout,
+                                    cudaStream_t s);
 cudaError_t launch_prepare(const uint8_t *w, const uint8_t *sf, int64_t G, int64_t N, int64_t K,
                            int flags, uint8_t *w_out, uint8_t *sf_out, cudaStream_t s);
 

@@ -1,0 +1,171 @@
+// RMSNorm feeding the NVFP4 activation quantiser.
+//
+// Per row r:  inv_r = 1 / sqrt(fl32(sum_k x^2) / K + eps)   (IEEE sqrt and division)
+//             y[r,k] = bf16( fl32( fl32(x[r,k] * inv_r) * gamma[k] ) )
+// The per-row statistics kernel computes inv_r (fp32 sum in a fixed order: each thread over
+// its strided 8-element chunks, then a butterfly warp reduction and a warp-0 reduction of
+// the warp sums), the block maxima of |y| for the dynamic global scale, and optionally
+// writes y.  The fused quantiser recomputes y from x, inv_r and gamma with the same
+// operations, so the fused path (stats -> normalise+quantise) and the unfused path
+// (stats writing y -> quantise y) produce identical codes, scales and gs.
+#include "common.cuh"
+
+namespace nvfp4 {
+
+namespace {
+
+constexpr int kNormThreads = 256;
+
+__device__ __forceinline__ float bf16_round(float v) {
+  return __bfloat162float(__float2bfloat16_rn(v));
+}
+
+__device__ __forceinline__ float normed(float x, float inv, float g) {
+  return bf16_round(__fmul_rn(__fmul_rn(x, inv), g));
+}
+
+__global__ void __launch_bounds__(kNormThreads) rmsnorm_stats_kernel(
+    const uint16_t *__restrict__ x, int64_t M, int64_t K, int64_t ldx, const uint16_t *__restrict__ gamma,
+    float eps, float *__restrict__ inv_rms, uint32_t *__restrict__ partials, uint16_t *__restrict__ y) {
+  __shared__ float red[32];
+  __shared__ float s_inv;
+  pdl_wait();
+  pdl_trigger();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nwarps = blockDim.x >> 5;
+  const int64_t chunks = K / 8;
+  uint32_t m = 0;
+  for (int64_t r = blockIdx.x; r < M; r += gridDim.x) {
+    const uint4 *row = reinterpret_cast<const uint4 *>(x + r * ldx);
+    float acc = 0.f;
+    for (int64_t c = threadIdx.x; c < chunks; c += blockDim.x) {
+      const uint4 v = __ldg(row + c);
+      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float a = __uint_as_float(w[i] << 16), b = __uint_as_float(w[i] & 0xFFFF0000u);
+        acc = __fadd_rn(acc, __fmul_rn(a, a));
+        acc = __fadd_rn(acc, __fmul_rn(b, b));
+      }
+    }
+#pragma unroll
+    for (int o = 16; o; o >>= 1) acc = __fadd_rn(acc, __shfl_xor_sync(0xffffffffu, acc, o));
+    if (lane == 0) red[warp] = acc;
+    __syncthreads();
+    if (warp == 0) {
+      float s = lane < nwarps ? red[lane] : 0.f;
+#pragma unroll
+      for (int o = 16; o; o >>= 1) s = __fadd_rn(s, __shfl_xor_sync(0xffffffffu, s, o));
+      if (lane == 0) {
+        const float mean = __fdiv_rn(s, static_cast<float>(K));
+        const float inv = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(mean, eps)));
+        s_inv = inv;
+        if (inv_rms) inv_rms[r] = inv;
+      }
+    }
+    __syncthreads();
+    const float inv = s_inv;
+    const uint4 *grow = reinterpret_cast<const uint4 *>(gamma);
+    for (int64_t c = threadIdx.x; c < chunks; c += blockDim.x) {
+      const uint4 v = __ldg(row + c), gv = __ldg(grow + c);
+      const uint32_t w[4] = {v.x, v.y, v.z, v.w}, gw[4] = {gv.x, gv.y, gv.z, gv.w};
+      uint32_t o[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float lo = normed(__uint_as_float(w[i] << 16), inv, __uint_as_float(gw[i] << 16));
+        const float hi = normed(__uint_as_float(w[i] & 0xFFFF0000u), inv, __uint_as_float(gw[i] & 0xFFFF0000u));
+        const uint32_t bl = __float_as_uint(lo) >> 16, bh = __float_as_uint(hi) >> 16;
+        m = max(m, max(bl & 0x7FFFu, bh & 0x7FFFu));
+        o[i] = bl | (bh << 16);
+      }
+      if (y) reinterpret_cast<uint4 *>(y + r * K)[c] = make_uint4(o[0], o[1], o[2], o[3]);
+    }
+    __syncthreads();  // red / s_inv are reused by the next row
+  }
+  if (partials) {
+    __shared__ uint32_t mred[32];
+#pragma unroll
+    for (int o = 16; o; o >>= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, o));
+    if (lane == 0) mred[warp] = m;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      for (int i = 1; i < nwarps; ++i) m = max(m, mred[i]);
+      partials[blockIdx.x] = m;
+    }
+  }
+}
+
+// One thread per 16-element block of the normalised rows; layout as the plain quantiser.
+__global__ void __launch_bounds__(kNormThreads) rmsnorm_quantize_kernel(
+    const uint16_t *__restrict__ x, int64_t M, int64_t K, int64_t ldx, const uint16_t *__restrict__ gamma,
+    const float *__restrict__ inv_rms, const uint32_t *__restrict__ partials, int nparts,
+    const float *__restrict__ gs_static, float *__restrict__ gs_out, uint8_t *__restrict__ q,
+    uint8_t *__restrict__ sf, int sf_layout, int64_t rows_total) {
+  __shared__ uint32_t scratch[32];
+  pdl_wait();
+  pdl_trigger();
+  float gs;
+  if (partials) {
+    gs = gs_from_partials(partials, nparts, scratch);
+    if (blockIdx.x == 0 && threadIdx.x == 0) *gs_out = gs;
+  } else {
+    gs = *gs_static;
+  }
+  const float six_gs = __fmul_rn(6.0f, gs);
+  const int64_t kb = K / 16;
+  const int64_t gb = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const bool valid = gb < rows_total * kb;
+  const int64_t r = valid ? gb / kb : 0;
+  const int64_t c = valid ? gb - r * kb : 0;
+  const bool live = valid && r < M;
+  uint32_t sfb = 0;
+  if (live) {
+    const uint4 *src = reinterpret_cast<const uint4 *>(x + r * ldx + c * 16);
+    const uint4 *gsrc = reinterpret_cast<const uint4 *>(gamma + c * 16);
+    const uint4 a = __ldg(src), b = __ldg(src + 1), ga = __ldg(gsrc), gb2 = __ldg(gsrc + 1);
+    const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+    const uint32_t g[8] = {ga.x, ga.y, ga.z, ga.w, gb2.x, gb2.y, gb2.z, gb2.w};
+    const float inv = __ldg(inv_rms + r);
+    float v[16];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      v[2 * i] = normed(__uint_as_float(w[i] << 16), inv, __uint_as_float(g[i] << 16));
+      v[2 * i + 1] = normed(__uint_as_float(w[i] & 0xFFFF0000u), inv, __uint_as_float(g[i] & 0xFFFF0000u));
+    }
+    uint32_t codes[2];
+    sfb = encode_block16(v, gs, six_gs, codes);
+    *reinterpret_cast<uint2 *>(q + r * (K / 2) + c * 8) = make_uint2(codes[0], codes[1]);
+  }
+  if (sf_layout == NVFP4_SF_LINEAR) {
+    if (live) sf[r * kb + c] = static_cast<uint8_t>(sfb);
+  } else {
+    const int lane = threadIdx.x & 31;
+    uint32_t word = sfb << ((lane & 3) * 8);
+    word |= __shfl_xor_sync(0xffffffffu, word, 1);
+    word |= __shfl_xor_sync(0xffffffffu, word, 2);
+    if (valid && (lane & 3) == 0)
+      *reinterpret_cast<uint32_t *>(sf + sf_word_offset(r, c >> 2, kb >> 2)) = word;
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_rmsnorm_stats(const void *x, int64_t M, int64_t K, int64_t ldx, const void *gamma, float eps,
+                                 float *inv_rms, uint32_t *partials, int nparts, void *y, cudaStream_t s) {
+  return launch_pdl(rmsnorm_stats_kernel, dim3(nparts), dim3(kNormThreads), 0, s, static_cast<const uint16_t *>(x),
+                    M, K, ldx, static_cast<const uint16_t *>(gamma), eps, inv_rms, partials,
+                    static_cast<uint16_t *>(y));
+}
+
+cudaError_t launch_rmsnorm_quantize(const void *x, int64_t M, int64_t K, int64_t ldx, const void *gamma,
+                                    const float *inv_rms, const uint32_t *partials, int nparts,
+                                    const float *gs_static, float *gs_out, uint8_t *q, uint8_t *sf, int sf_layout,
+                                    cudaStream_t s) {
+  const int64_t rows_total = sf_layout == NVFP4_SF_LINEAR ? M : ((M + 127) / 128) * 128;
+  const int64_t items = rows_total * (K / 16);
+  const int64_t blocks = items > 0 ? (items + kNormThreads - 1) / kNormThreads : 1;
+  return launch_pdl(rmsnorm_quantize_kernel, dim3(static_cast<unsigned>(blocks)), dim3(kNormThreads), 0, s,
+                    static_cast<const uint16_t *>(x), M, K, ldx, static_cast<const uint16_t *>(gamma), inv_rms,
+                    partials, nparts, gs_static, gs_out, q, sf, sf_layout, rows_total);
+}
+
+}  // namespace nvfp4

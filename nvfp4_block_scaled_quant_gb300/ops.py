@@ -67,6 +67,34 @@ def quantize_act(x: torch.Tensor, gs: Optional[torch.Tensor] = None, sf_layout: 
     return q, sf, gs_t
 
 
+def rmsnorm(x: torch.Tensor, gamma: torch.Tensor, eps: float = 1e-6, stream=None) -> torch.Tensor:
+    """x (M, K) bf16 -> x / rms(x) * gamma, bf16 (the unfused normalisation)."""
+    _cuda(x, gamma)
+    M, K = x.shape
+    y = torch.empty_like(x)
+    call("nvfp4_rmsnorm", x.data_ptr(), M, K, K, gamma.data_ptr(), eps, y.data_ptr(), _stream(stream))
+    return y
+
+
+def rmsnorm_quantize(x: torch.Tensor, gamma: torch.Tensor, eps: float = 1e-6, gs: Optional[torch.Tensor] = None,
+                     sf_layout: str = "swizzled", want_normed: bool = False, stream=None):
+    """Fused RMSNorm -> NVFP4: returns (q, sf, gs, x_normed or None)."""
+    _cuda(x, gamma, gs)
+    M, K = x.shape
+    layout = _lib.SF_SWIZZLED if sf_layout == "swizzled" else _lib.SF_LINEAR
+    q = _u8(M, K // 2, device=x.device)
+    sf = _u8(sf_bytes(M, K) if layout == _lib.SF_SWIZZLED else M * (K // 16), device=x.device)
+    dyn = gs is None
+    gs_t = torch.empty(1, dtype=torch.float32, device=x.device) if dyn else gs
+    xn = torch.empty_like(x) if want_normed else None
+    ws_n = int(lib().nvfp4_rmsnorm_quantize_workspace_bytes(M, K))
+    ws = _u8(ws_n, device=x.device)
+    call("nvfp4_rmsnorm_quantize", x.data_ptr(), M, K, K, gamma.data_ptr(), eps,
+         _lib.GS_DYNAMIC if dyn else _lib.GS_STATIC, gs_t.data_ptr(), q.data_ptr(), sf.data_ptr(), layout,
+         _ptr(xn), ws.data_ptr(), ws_n, _stream(stream))
+    return q, sf, gs_t, xn
+
+
 def prepare_weights(w: torch.Tensor, sf: torch.Tensor, N: int, K: int, interleave_w13: bool = False,
                     stream=None) -> Tuple[torch.Tensor, torch.Tensor]:
     """Checkpoint codes (G, N, K/2) + row-major scales (G, N, K/16) -> prepared codes + swizzled scales."""

@@ -156,3 +156,12 @@ def prefill_whole(device="cpu"):
 # Fixed-group linear (grouped o-projection): 8 groups of 4096 inputs each; the output width per
 # group is not printed on the pages, 1024 is taken (a multiple of the 128-wide tile).
 GROUPED_LINEAR = {M: (M, 8, 4096, 1024) for M in (1, 128)}   # (M, G, K, N)
+
+
+RMSNORM_EPS = 1e-6
+
+
+def norm_weight(K: int, seed: int, device="cpu") -> torch.Tensor:
+    """RMSNorm gain: bf16 1 + 0.1 N(0, 1)."""
+    g = _gen(seed, device)
+    return (1.0 + 0.1 * torch.randn(K, generator=g, device=device)).to(torch.bfloat16)

@@ -249,6 +249,24 @@ def unswizzle_sf(buf: np.ndarray, rows: int, K: int) -> np.ndarray:
 
 
 # ---------------------------------------------------------------------------
+# RMSNorm feeding the activation quantiser
+# ---------------------------------------------------------------------------
+
+def rmsnorm(x: np.ndarray, gamma: np.ndarray, eps: float):
+    """RMSNorm of each row: y = x / sqrt(mean(x^2) + eps) * gamma, in fp64.
+
+    Returns (y rounded to bf16 through fp32, as fp32 values; y in fp64; inv_rms fp64).  The
+    normalised activations that feed the NVFP4 quantiser are bf16, as the unfused path of page 1
+    (paragraph "Added --ab-compare flag") hands x_normed to the quantiser.
+    """
+    x64 = np.asarray(x, dtype=np.float64)
+    inv = 1.0 / np.sqrt(np.mean(x64 * x64, axis=1) + eps)
+    y = x64 * inv[:, None] * np.asarray(gamma, dtype=np.float64)[None, :]
+    yb = bf16_bits_to_f32(f32_to_bf16_bits(y.astype(np.float32)))
+    return yb, y, inv
+
+
+# ---------------------------------------------------------------------------
 # Dense NVFP4 linear
 # ---------------------------------------------------------------------------
 

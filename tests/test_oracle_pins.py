@@ -274,6 +274,27 @@ def test_grouped_linear_is_block_diagonal_linear():
     assert got.shape == (M, G * N)
 
 
+# --------------------------------------------------------------------------- RMSNorm
+
+def test_rmsnorm_against_library_and_closed_forms():
+    rng = np.random.default_rng(13)
+    x = (rng.standard_normal((6, 256)) * 3).astype(np.float32)
+    gamma = (1 + 0.1 * rng.standard_normal(256)).astype(np.float32)
+    eps = 1e-6
+    yb, y, inv = O.rmsnorm(x, gamma, eps)
+    want = torch.nn.functional.rms_norm(torch.from_numpy(x).double(), (256,), torch.from_numpy(gamma).double(), eps)
+    np.testing.assert_allclose(y, want.numpy(), rtol=1e-13)
+    # bf16 rounding of the fp64 value: within half a bf16 ulp (2^-8 relative) plus the fp32 step
+    assert np.all(np.abs(yb - y) <= np.abs(y) * (2.0 ** -8) * 1.0001 + 1e-30)
+    # a constant row c normalises to sign(c) * gamma / sqrt(1 + eps / c^2)
+    c = np.full((1, 256), -2.5, np.float32)
+    _, yc, _ = O.rmsnorm(c, gamma, eps)
+    np.testing.assert_allclose(yc[0], -gamma / np.sqrt(1 + eps / 6.25), rtol=1e-15)
+    # scale invariance away from eps
+    _, y2, _ = O.rmsnorm(x * 64, gamma, eps)
+    np.testing.assert_allclose(y2, y, rtol=2e-7)  # differs by ~eps / (2 mean(x^2)) ~ 6e-8
+
+
 # --------------------------------------------------------------------------- SiLU
 
 def test_silu_closed_form_and_library():
