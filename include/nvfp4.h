@@ -220,6 +220,26 @@ NVFP4_API nvfp4_status nvfp4_grouped_linear(const void *x, int64_t M, int64_t G,
                                             int gs_mode, float *gs, void *y, void *ws,
                                             size_t ws_bytes, void *stream);
 
+/* --------------------------------------------------------------- router gate
+ * The dense router of page 1 (paragraph "Router gate: FP8_E4M3 quantize"): the NVFP4 gate
+ * weight (E, H/2) codes with row-major scales (E, H/16) and device scalar ws2 is
+ * dequantised to bf16, quantised to FP8-E4M3 with one per-tensor scale s = amax / 448 and
+ * dequantised back to bf16 (nvfp4_router_prepare, once):
+ *   w = bf16(fl32(fl32(e2m1 * e4m3) * ws2)),  q = E4M3(fl32(w * fl32(1/s))),
+ *   wg = bf16(fl32(e4m3(q) * s))                       (wg all zero when s == 0)
+ * Per call (nvfp4_router): logits = x (T, H) bf16 @ wg^T in fp32, softmax over the E
+ * experts, the topk largest probabilities (lower expert id first on ties) as ids (T, topk)
+ * int32 and weights (T, topk) fp32 renormalised to sum 1 -- the inputs of the routing
+ * stage.  logits (T, E) fp32 may be given to receive the logits; otherwise the workspace
+ * holds them.  E <= 1024, topk <= min(32, E), H % 64 == 0. */
+NVFP4_API size_t nvfp4_router_prepare_workspace_bytes(int64_t E, int64_t H);
+NVFP4_API nvfp4_status nvfp4_router_prepare(const uint8_t *w, const uint8_t *w_sf, const float *ws2, int64_t E,
+                                            int64_t H, void *wg, void *ws, size_t ws_bytes, void *stream);
+NVFP4_API size_t nvfp4_router_workspace_bytes(int64_t T, int64_t E);
+NVFP4_API nvfp4_status nvfp4_router(const void *x, int64_t T, int64_t H, const void *wg, int64_t E, int topk,
+                                    int32_t *ids, float *weights, float *logits, void *ws, size_t ws_bytes,
+                                    void *stream);
+
 /* -------------------------------------------------------------- (b) routing
  * Groups the T*topk flat entries f = t*topk + j of ids (T, topk) int32 by
  * expert: counts[e] (E), offsets (E+1, exclusive prefix sum, int32 as the

@@ -63,6 +63,10 @@ _SIGNATURES = {
     "nvfp4_grouped_linear_workspace_bytes": (c_size_t, [I64, I64, I64]),
     "nvfp4_grouped_linear": (c_int, [P, I64, I64, I64, I64, P, P, P, c_int, P, P, P, c_size_t, P]),
     "nvfp4_moe_route": (c_int, [P, I64, c_int, I64, P, P, P, P, P]),
+    "nvfp4_router_prepare_workspace_bytes": (c_size_t, [I64, I64]),
+    "nvfp4_router_prepare": (c_int, [P, P, P, I64, I64, P, P, c_size_t, P]),
+    "nvfp4_router_workspace_bytes": (c_size_t, [I64, I64]),
+    "nvfp4_router": (c_int, [P, I64, I64, P, I64, c_int, P, P, P, P, c_size_t, P]),
     "nvfp4_moe_workspace_layout": (c_int, [I64, I64, I64, I64, c_int, c_int, POINTER(MoeWsLayout)]),
     "nvfp4_moe_workspace_bytes": (c_size_t, [I64, I64, I64, I64, c_int, c_int]),
     "nvfp4_moe_forward": (c_int, [P, I64, I64, I64, I64, c_int, P, P, P, P, P, P, P, P, P, P, P, P, P, c_int, P, P,

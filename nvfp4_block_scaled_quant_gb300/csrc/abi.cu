@@ -643,6 +643,52 @@ nvfp4_status nvfp4_grouped_linear(const void *x, int64_t M, int64_t G, int64_t K
   return gemm_dense(__func__, d, xq, xsf, gs, M, K, N, w, w_sf, ws2, y, s, 1, G);
 }
 
+size_t nvfp4_router_prepare_workspace_bytes(int64_t E, int64_t H) {
+  (void)E;
+  (void)H;
+  return kMaxPartials * sizeof(uint32_t);
+}
+
+nvfp4_status nvfp4_router_prepare(const uint8_t *w, const uint8_t *w_sf, const float *ws2, int64_t E, int64_t H,
+                                  void *wg, void *ws, size_t ws_bytes, void *stream) {
+  NV_REQUIRE(w && w_sf && ws2 && wg, NVFP4_ERR_INVALID_ARG, "NULL pointer argument");
+  NV_REQUIRE(E > 0 && H > 0, NVFP4_ERR_INVALID_ARG, "E=%lld H=%lld", (long long)E, (long long)H);
+  NV_REQUIRE(H % 64 == 0 && E <= kMaxExperts, NVFP4_ERR_UNSUPPORTED_SHAPE, "H %% 64 == 0 and E <= %d", kMaxExperts);
+  NV_REQUIRE(aligned(w, 16) && aligned(w_sf, 16) && aligned(wg, 16) && aligned(ws2, 4), NVFP4_ERR_MISALIGNED,
+             "pointers must be 16-byte aligned");
+  nvfp4_status st = check_ws(__func__, ws, ws_bytes, nvfp4_router_prepare_workspace_bytes(E, H));
+  if (st != NVFP4_OK) return st;
+  DeviceInfo *d;
+  if ((st = device_info(__func__, &d)) != NVFP4_OK) return st;
+  NV_CUDA(launch_router_prepare(w, w_sf, ws2, E, H, static_cast<uint32_t *>(ws), wg, static_cast<cudaStream_t>(stream)),
+          "router prepare launch");
+  return NVFP4_OK;
+}
+
+size_t nvfp4_router_workspace_bytes(int64_t T, int64_t E) {
+  if (T < 0 || E < 0) return 0;
+  return align256(static_cast<size_t>(T) * static_cast<size_t>(E) * sizeof(float));
+}
+
+nvfp4_status nvfp4_router(const void *x, int64_t T, int64_t H, const void *wg, int64_t E, int topk, int32_t *ids,
+                          float *weights, float *logits, void *ws, size_t ws_bytes, void *stream) {
+  NV_REQUIRE(T >= 0 && H > 0 && E > 0 && topk > 0, NVFP4_ERR_INVALID_ARG, "T=%lld H=%lld E=%lld topk=%d",
+             (long long)T, (long long)H, (long long)E, topk);
+  NV_REQUIRE(H % 64 == 0 && E <= kMaxExperts && topk <= kMaxTopk && topk <= E, NVFP4_ERR_UNSUPPORTED_SHAPE,
+             "H %% 64 == 0, E <= %d, topk <= min(%d, E)", kMaxExperts, kMaxTopk);
+  NV_REQUIRE(wg && ((x && ids && weights) || T == 0), NVFP4_ERR_INVALID_ARG, "NULL pointer argument");
+  NV_REQUIRE(aligned(x, 16) && aligned(wg, 16) && aligned(ids, 4) && aligned(weights, 4) && aligned(logits, 4),
+             NVFP4_ERR_MISALIGNED, "x and wg must be 16-byte aligned");
+  nvfp4_status st = NVFP4_OK;
+  if (!logits && (st = check_ws(__func__, ws, ws_bytes, nvfp4_router_workspace_bytes(T, E))) != NVFP4_OK) return st;
+  DeviceInfo *d;
+  if ((st = device_info(__func__, &d)) != NVFP4_OK) return st;
+  if (T == 0) return NVFP4_OK;
+  float *lg = logits ? logits : static_cast<float *>(ws);
+  NV_CUDA(launch_router(x, T, H, wg, E, topk, ids, weights, lg, static_cast<cudaStream_t>(stream)), "router launch");
+  return NVFP4_OK;
+}
+
 nvfp4_status nvfp4_moe_route(const int32_t *ids, int64_t T, int topk, int64_t E, int32_t *counts, int32_t *offsets,
                              int32_t *sorted_idx, int32_t *inv_idx, void *stream) {
   NV_REQUIRE(T >= 0 && topk > 0 && E > 0, NVFP4_ERR_INVALID_ARG, "T=%lld topk=%d E=%lld", (long long)T, topk,

@@ -124,6 +124,11 @@ cudaError_t launch_rmsnorm_quantize(const void *x, int64_t M, int64_t K, int64_t
                                     const float *inv_rms, const uint32_t *partials, int nparts,
                                     const float *gs_static, float *gs_out, uint8_t *q, uint8_t *sf, int sf_layout,
                                     cudaStream_t s);
+int router_partial_count(int64_t nblocks);
+cudaError_t launch_router_prepare(const uint8_t *w, const uint8_t *sf, const float *ws2, int64_t E, int64_t H,
+                                  uint32_t *partials, void *wg, cudaStream_t s);
+cudaError_t launch_router(const void *x, int64_t T, int64_t H, const void *wg, int64_t E, int topk, int32_t *ids,
+                          float *weights, float *logits, cudaStream_t s);
 cudaError_t launch_prepare(const uint8_t *w, const uint8_t *sf, int64_t G, int64_t N, int64_t K,
                            int flags, uint8_t *w_out, uint8_t *sf_out, cudaStream_t s);
 

@@ -156,6 +156,35 @@ def gemm(xq: torch.Tensor, xsf: torch.Tensor, gs: torch.Tensor, K: int, w: torch
     return y
 
 
+# --------------------------------------------------------------------------- router gate
+
+def router_prepare(w: torch.Tensor, w_sf_linear: torch.Tensor, ws2: torch.Tensor, E: int, H: int,
+                   stream=None) -> torch.Tensor:
+    """NVFP4 gate weight (E, H/2) + row-major scales -> bf16 weight after the FP8-E4M3 round trip."""
+    _cuda(w, w_sf_linear, ws2)
+    wg = torch.empty(E, H, dtype=torch.bfloat16, device=w.device)
+    n = int(lib().nvfp4_router_prepare_workspace_bytes(E, H))
+    ws = _u8(n, device=w.device)
+    call("nvfp4_router_prepare", w.data_ptr(), w_sf_linear.data_ptr(), ws2.data_ptr(), E, H, wg.data_ptr(),
+         ws.data_ptr(), n, _stream(stream))
+    return wg
+
+
+def router(x: torch.Tensor, wg: torch.Tensor, topk: int, want_logits: bool = False, stream=None):
+    """Dense router: (ids (T, topk) int32, weights (T, topk) fp32, logits (T, E) fp32 or None)."""
+    _cuda(x, wg)
+    T, H = x.shape
+    E = wg.shape[0]
+    ids = torch.empty(T, topk, dtype=torch.int32, device=x.device)
+    w = torch.empty(T, topk, dtype=torch.float32, device=x.device)
+    logits = torch.empty(T, E, dtype=torch.float32, device=x.device) if want_logits else None
+    n = int(lib().nvfp4_router_workspace_bytes(T, E))
+    ws = None if want_logits else _u8(max(n, 256), device=x.device)
+    call("nvfp4_router", x.data_ptr(), T, H, wg.data_ptr(), E, topk, ids.data_ptr(), w.data_ptr(), _ptr(logits),
+         _ptr(ws), 0 if ws is None else ws.numel(), _stream(stream))
+    return ids, w, logits
+
+
 # --------------------------------------------------------------------------- (b) routing
 
 def moe_route(ids: torch.Tensor, E: int, stream=None):

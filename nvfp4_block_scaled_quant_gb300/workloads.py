@@ -165,3 +165,8 @@ def norm_weight(K: int, seed: int, device="cpu") -> torch.Tensor:
     """RMSNorm gain: bf16 1 + 0.1 N(0, 1)."""
     g = _gen(seed, device)
     return (1.0 + 0.1 * torch.randn(K, generator=g, device=device)).to(torch.bfloat16)
+
+
+# Router gate of the 384-expert layer: gate weight (E, H) bf16 N(0, 0.02) stored as NVFP4.
+ROUTER = {T: (T, 7168, 384, 8) for T in (1, 128)}   # (T, H, E, topk)
+ROUTER_WEIGHT_SEED = 31337

@@ -300,6 +300,56 @@ def grouped_linear(xq: Quantized, w_codes: Sequence[np.ndarray], w_sf: Sequence[
 
 
 # ---------------------------------------------------------------------------
+# Router gate (FP8-E4M3 round trip of the gate weight, linear, softmax, top-k)
+# ---------------------------------------------------------------------------
+
+def e4m3_encode_signed(v: np.ndarray) -> np.ndarray:
+    """Signed E4M3 (FN) byte: sign bit 7 plus the unsigned nearest-even, saturating encoding of |v|."""
+    v = np.asarray(v, dtype=np.float32)
+    return ue4m3_encode(np.abs(v)) | (np.signbit(v).astype(np.uint8) << 7)
+
+
+def e4m3_decode_signed(b: np.ndarray) -> np.ndarray:
+    b = np.asarray(b).astype(np.int64)
+    mag = ue4m3_decode(b & 0x7F)
+    return np.where((b & 0x80) != 0, -mag, mag)
+
+
+def router_weight(w_codes: np.ndarray, w_sf: np.ndarray, ws2: float) -> np.ndarray:
+    """Gate weight as the router uses it (page 1, paragraph "Router gate: FP8_E4M3 quantize"):
+    dequantise the NVFP4 checkpoint to bf16, quantise to FP8-E4M3 with one per-tensor scale
+    s = amax / 448, dequantise back to bf16.  Steps in fp32:
+      w  = bf16(fl32(fl32(e2m1 * e4m3) * ws2))
+      s  = fl32(amax(|w|) / 448),  q = E4M3(fl32(w * fl32(1 / s)))   (all zero when s == 0)
+      wg = bf16(fl32(e4m3(q) * s))
+    Returns wg as fp32 values (exactly bf16-representable).
+    """
+    scale = np.repeat(ue4m3_decode(w_sf), BLOCK, axis=1)[:, : w_codes.shape[1]].astype(np.float32)
+    prod = (e2m1_decode(w_codes).astype(np.float32) * scale).astype(np.float32)
+    w = bf16_bits_to_f32(f32_to_bf16_bits((prod * F32(ws2)).astype(np.float32)))
+    amax = F32(np.max(np.abs(w))) if w.size else F32(0)
+    s = F32(amax / F32(448.0))
+    if s == 0:
+        return np.zeros_like(w)
+    r = F32(F32(1.0) / s)
+    q = e4m3_encode_signed((w * r).astype(np.float32))
+    deq = (e4m3_decode_signed(q).astype(np.float32) * s).astype(np.float32)
+    return bf16_bits_to_f32(f32_to_bf16_bits(deq))
+
+
+def router(x: np.ndarray, wg: np.ndarray, topk: int):
+    """Dense router: logits = x @ wg^T (fp64), softmax over the experts, top-k (ties to the
+    lower expert id), weights renormalised over the k chosen.  Returns (ids, weights, probs)."""
+    logits = np.asarray(x, dtype=np.float64) @ np.asarray(wg, dtype=np.float64).T
+    z = logits - logits.max(axis=1, keepdims=True)
+    p = np.exp(z)
+    p /= p.sum(axis=1, keepdims=True)
+    order = np.argsort(-p, axis=1, kind="stable")[:, :topk]
+    w = np.take_along_axis(p, order, axis=1)
+    return order.astype(np.int32), w / w.sum(axis=1, keepdims=True), p
+
+
+# ---------------------------------------------------------------------------
 # Routing
 # ---------------------------------------------------------------------------
 

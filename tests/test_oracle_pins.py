@@ -295,6 +295,46 @@ def test_rmsnorm_against_library_and_closed_forms():
     np.testing.assert_allclose(y2, y, rtol=2e-7)  # differs by ~eps / (2 mean(x^2)) ~ 6e-8
 
 
+# --------------------------------------------------------------------------- router
+
+def test_signed_e4m3_matches_torch_float8():
+    rng = np.random.default_rng(14)
+    v = np.concatenate([rng.standard_normal(20000) * np.exp2(rng.uniform(-12, 9, 20000)),
+                        [0.0, -0.0, 448.0, -448.0, 500.0, -1e9]]).astype(np.float32)
+    want = torch.from_numpy(np.clip(v, -448, 448)).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    got = O.e4m3_encode_signed(v)
+    np.testing.assert_array_equal(got[v != 0], want[v != 0])  # torch maps -0 to 0x80 as well; zeros checked below
+    assert got[-6 + 0] == 0 and got[-5] == 0x80
+    back = torch.from_numpy(want.copy()).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    np.testing.assert_array_equal(O.e4m3_decode_signed(want), back)
+
+
+def test_router_weight_fp8_roundtrip_precision(golden):
+    """The gate's FP8 round trip keeps cosine ~0.9997 to the bf16 weight (page 1's FP8 figure)."""
+    rng = np.random.default_rng(15)
+    wq = O.quantize((rng.standard_normal((384, 7168)) * 0.02).astype(np.float32))
+    wg = O.router_weight(wq.codes, wq.sf, wq.gs)
+    w = O.dequantize(wq.codes, wq.sf, wq.gs)
+    c = O.cosine(wg, w)
+    assert abs(c - golden("page_precision.json")["fp8_e4m3_roundtrip_cosine"]) < 2e-4
+    np.testing.assert_array_equal(O.bf16_bits_to_f32(O.f32_to_bf16_bits(wg.astype(np.float32))), wg)  # bf16 values
+
+
+def test_router_topk_against_library():
+    rng = np.random.default_rng(16)
+    x = rng.standard_normal((40, 64))
+    wg = rng.standard_normal((24, 64)) * 0.1
+    ids, w, p = O.router(x, wg, 5)
+    tp = torch.softmax(torch.from_numpy(x @ wg.T), dim=1)
+    tv, ti = torch.topk(tp, 5, dim=1)
+    np.testing.assert_array_equal(ids, ti.numpy())
+    np.testing.assert_allclose(w, (tv / tv.sum(1, keepdim=True)).numpy(), rtol=1e-14)
+    np.testing.assert_allclose(w.sum(1), 1.0, rtol=1e-15)
+    # ties go to the lower expert id
+    ids2, _, _ = O.router(np.zeros((1, 64)), np.zeros((24, 64)), 3)
+    np.testing.assert_array_equal(ids2[0], [0, 1, 2])
+
+
 # --------------------------------------------------------------------------- SiLU
 
 def test_silu_closed_form_and_library():
