@@ -5,12 +5,15 @@
 // with one fp32 accumulator tile of 128 x 128 in TMEM per output tile
 // (tcgen05.mma kind::mxf4nvf4, scale_vec::4X, K = 64 per instruction), operands
 // staged in shared memory by TMA (128-byte swizzle, 256 FP4 elements of K per
-// stage) and the block scales copied from shared memory to TMEM with
-// tcgen05.cp.  Two persistent CTAs per SM walk the tiles of all groups:
+// stage) and the block scales written to TMEM with tcgen05.st by the epilogue
+// warps, which leaves the tensor pipe to the MMAs alone.  Two persistent CTAs
+// per SM walk the tiles of all groups:
 //   warp 0      TMA producer (one lane): A box rows only as far as the group's
 //               live rows reach, B tile, A/B scale blocks (bulk copies);
 //   warp 1      MMA issuer (one lane), owns the TMEM allocation;
-//   warps 2..5  epilogue, one accumulator row per thread (TMEM lane quarters).
+//   warps 2..5  scale staging for every stage of a tile (each warp its TMEM
+//               lane quarter: A and B scales of rows 32q..32q+31), then the
+//               epilogue, one accumulator row per thread.
 // The two CTAs of an SM overlap each other's epilogues and keep two MMA
 // issuers busy (one accumulator buffer each).  Every wait is bounded (kPipelineTimeoutNs); a role that gives up
 // sets a shared abort flag, the others drain and the CTA frees TMEM and exits
@@ -85,7 +88,8 @@ __global__ void __launch_bounds__(kGemmThreads, kCtasPerSm)
   uint64_t *empty = full + kStages;
   uint64_t *tfull = empty + kStages;
   uint64_t *tempty = tfull + 2;
-  uint64_t *drain = tempty + 2;
+  uint64_t *sf_ready = tempty + 2;
+  uint64_t *drain = sf_ready + kStages;
   uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(drain + 1);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_holder + 1);
 
@@ -95,6 +99,7 @@ __global__ void __launch_bounds__(kGemmThreads, kCtasPerSm)
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
+      mbar_init(&sf_ready[s], 4);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&tfull[i], 1);
@@ -238,7 +243,6 @@ __global__ void __launch_bounds__(kGemmThreads, kCtasPerSm)
       int it = 0;
       bool ok = true;
       const uint32_t sA0 = smem_u32(sA), sB0 = smem_u32(sB);
-      const uint32_t sSFA0 = smem_u32(sSFA), sSFB0 = smem_u32(sSFB);
       for (int idx = blockIdx.x; ok && idx < total_tiles; idx += gridDim.x, ++it) {
         const int acc = kAccBufs == 2 ? (it & 1) : 0;
         const uint32_t acc_phase = kAccBufs == 2 ? ((it >> 1) & 1) : (it & 1);
@@ -256,14 +260,14 @@ __global__ void __launch_bounds__(kGemmThreads, kCtasPerSm)
             ok = false;
             break;
           }
+          // the stage's scales are in TMEM once the four epilogue warps arrived
+          if (!mbar_wait_bounded(&sf_ready[stage], phase, abort_flag, args.err,
+                                 kPipelineTimeoutNs)) {
+            ok = false;
+            break;
+          }
           tc_fence_after();
           const uint32_t sf_col = tmem_base + kTmemAccCols + stage * kTmemSfCols;
-          for (int j = 0; j < kv; ++j) {
-            tc_cp_sf(sf_col + j * 4,
-                     smem_desc(sSFA0 + stage * kSfBytesStage + j * kSfBytesPerKStep, 0, 128, 0));
-            tc_cp_sf(sf_col + 16 + j * 4,
-                     smem_desc(sSFB0 + stage * kSfBytesStage + j * kSfBytesPerKStep, 0, 128, 0));
-          }
           const uint64_t adesc = smem_desc(sA0 + stage * kTileBytesA, 16, 1024, 2);
           const uint64_t bdesc = smem_desc(sB0 + stage * kTileBytesB, 16, 1024, 2);
           for (int j = 0; j < kv; ++j) {
@@ -290,14 +294,52 @@ __global__ void __launch_bounds__(kGemmThreads, kCtasPerSm)
     const int quarter = warp & 3;  // TMEM lanes [32*quarter, 32*quarter + 32)
     const int m = quarter * 32 + lane;
     const float gs_scalar = (kEpi == static_cast<int>(Epi::kW2)) ? 0.f : __ldg(args.gs_a);
+    // Scale staging.  Each K step's 512-byte swizzled block holds, at 16 r + 4 c, the
+    // four UE4M3 scales (64 K) of operand row 32 c + r.  Every 32-lane quarter of TMEM
+    // receives the same copy of the block: lane 32 q + r, column (scale address + c)
+    // holds the word of row 32 c + r, the arrangement the MMA reads scales from.  This
+    // warp writes its own quarter; lane r loads the 16 bytes at 16 r.
+    const uint32_t sf_lane = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + kTmemAccCols;
+    const int sf_off = lane * 16;
+    int sstage = 0;
+    uint32_t sphase = 0;
     int it = 0;
     for (int idx = blockIdx.x; idx < total_tiles; idx += gridDim.x, ++it) {
       Tile t;
       decode_tile(args, idx, n_tiles, t);
       const int acc = kAccBufs == 2 ? (it & 1) : 0;
       const uint32_t acc_phase = kAccBufs == 2 ? ((it >> 1) & 1) : (it & 1);
-      bool ok = mbar_wait_bounded(&tfull[acc], acc_phase, abort_flag, args.err,
-                                  kPipelineTimeoutNs);
+      bool ok = true;
+      for (int ks = 0; ks < k_stages; ++ks) {
+        const int kv = min(4, k_steps - 4 * ks);
+        ok = mbar_wait_bounded(&full[sstage], sphase, abort_flag, args.err, kPipelineTimeoutNs);
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) break;
+        const uint8_t *pa = sSFA + sstage * kSfBytesStage + sf_off;
+        const uint8_t *pb = sSFB + sstage * kSfBytesStage + sf_off;
+        uint32_t ra[16], rb[16];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const uint4 wa = j < kv ? *reinterpret_cast<const uint4 *>(pa + j * kSfBytesPerKStep)
+                                  : make_uint4(0u, 0u, 0u, 0u);
+          const uint4 wb = j < kv ? *reinterpret_cast<const uint4 *>(pb + j * kSfBytesPerKStep)
+                                  : make_uint4(0u, 0u, 0u, 0u);
+          ra[4 * j] = wa.x, ra[4 * j + 1] = wa.y, ra[4 * j + 2] = wa.z, ra[4 * j + 3] = wa.w;
+          rb[4 * j] = wb.x, rb[4 * j + 1] = wb.y, rb[4 * j + 2] = wb.z, rb[4 * j + 3] = wb.w;
+        }
+        tmem_st16(sf_lane + sstage * kTmemSfCols, ra);
+        tmem_st16(sf_lane + sstage * kTmemSfCols + 16, rb);
+        tmem_st_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sf_ready[sstage]);
+        if (++sstage == kStages) {
+          sstage = 0;
+          sphase ^= 1;
+        }
+      }
+      if (!ok) break;
+      ok = mbar_wait_bounded(&tfull[acc], acc_phase, abort_flag, args.err, kPipelineTimeoutNs);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       tc_fence_after();

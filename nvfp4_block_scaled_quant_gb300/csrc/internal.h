@@ -15,11 +15,10 @@ constexpr int kMaxExperts = 1024;       // routing limit (E)
 constexpr int kMaxTopk = 32;
 constexpr uint64_t kPipelineTimeoutNs = 2000000000ull;  // 2 s: no healthy wait comes close
 
-// GEMM tile geometry: two persistent CTAs per SM, each with its own pipeline.  One
-// MMA-issuing thread per CTA cannot issue the 12 tcgen05 instructions of a stage
-// (8 scale copies + 4 MMAs of 128x128x64) as fast as the weights stream in; two
-// CTAs double the issue rate per SM and the two pipelines overlap each other's
-// epilogues.
+// GEMM tile geometry: two persistent CTAs per SM, each with its own pipeline.  Two
+// CTAs double the MMA issue rate per SM and the two pipelines overlap each other's
+// epilogues.  The block scales reach TMEM through tcgen05.st from the epilogue
+// warps, so the tensor pipe runs only the 4 MMAs (128x128x64) of a stage.
 constexpr int kBlockM = 128;            // UMMA M
 constexpr int kBlockN = 128;            // UMMA N and output tile width
 constexpr int kStageK = 256;            // FP4 elements per pipeline stage (128 bytes per row)
@@ -42,10 +41,13 @@ constexpr uint32_t kTmemCols = 256;                  // per CTA: 128 accumulator
 static_assert(kTmemAccCols + kStages * kTmemSfCols <= kTmemCols, "TMEM budget");
 static_assert(kCtasPerSm * kTmemCols <= 512, "two CTAs share the SM's 512 TMEM columns");
 
+// full, empty, sf_ready per stage; two tfull/tempty; drain; TMEM address; abort flag
+constexpr size_t kGemmBarrierBytes = 256;
+static_assert((3 * kStages + 5) * 8 + 8 <= kGemmBarrierBytes, "barrier region");
 constexpr size_t kGemmSmemBytes =
     1024 /* alignment slack */ +
     static_cast<size_t>(kStages) * (kTileBytesA + kTileBytesB + 2 * kSfBytesStage) +
-    256 /* barriers and flags */;
+    kGemmBarrierBytes;
 // Requested (not used) by launches that want one CTA per SM: two of these do not fit.
 constexpr size_t kGemmSmemBytesSolo = 2 * kGemmSmemBytes;
 static_assert(kGemmSmemBytesSolo <= 232448, "per-block shared memory limit");
