@@ -36,9 +36,12 @@ DEVERR_PIPELINE_TIMEOUT = 2
 LINEAR_NOALLOC_MAX_BYTES = 4 << 20
 
 
+ABI_VERSION = 2  # NVFP4_ABI_VERSION of the header these signatures follow
+
+
 class MoeWsLayout(Structure):
     _fields_ = [(n, c_size_t) for n in ("counts", "offsets", "pad_offsets", "tile_offsets", "sorted_idx",
-                                         "inv_idx", "dest_rows", "amax_partials", "xq", "xsf", "hq", "hsf", "y_acc", "total")]
+                                         "inv_idx", "dest_rows", "tile_table", "amax_partials", "xq", "xsf", "hq", "hsf", "y_acc", "total")]
     _fields_ += [("rows_capacity", c_int64)]
 
 

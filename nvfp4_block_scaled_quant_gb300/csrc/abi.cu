@@ -177,6 +177,7 @@ nvfp4_moe_ws_layout moe_layout(int64_t T, int64_t H, int64_t I, int64_t E, int t
   L.sorted_idx = take(static_cast<size_t>(Tk > 0 ? Tk : 1) * 4);
   L.inv_idx = take(static_cast<size_t>(Tk > 0 ? Tk : 1) * 4);
   L.dest_rows = take(static_cast<size_t>(Tk > 0 ? Tk : 1) * 4);
+  L.tile_table = take(rc / kBlockM * 16 + 16);
   L.amax_partials = take(kMaxPartials * 4);
   L.xq = take(rc * static_cast<size_t>(H / 2));
   L.xsf = take(sf_bytes(L.rows_capacity, H));
@@ -222,6 +223,7 @@ RouteBufs route_bufs(void *ws, const nvfp4_moe_ws_layout &L) {
   rb.sorted_idx = at<int>(ws, L.sorted_idx);
   rb.inv_idx = at<int>(ws, L.inv_idx);
   rb.dest_rows = at<int>(ws, L.dest_rows);
+  rb.tile_table = at<int4>(ws, L.tile_table);
   return rb;
 }
 
@@ -272,6 +274,7 @@ nvfp4_status moe_gemm_impl(const char *fn, DeviceInfo *d, Epi epi, int64_t T, in
   a.offsets = at<int>(ws, L.offsets);
   a.pad_offsets = at<int>(ws, L.pad_offsets);
   a.tile_offsets = at<int>(ws, L.tile_offsets);
+  a.tile_table = at<const int4>(ws, L.tile_table);
   a.shared_group = has_shared ? static_cast<int>(E) : -1;
   a.a_sf = at<uint8_t>(ws, w13 ? L.xsf : L.hsf);
   a.a_kc_total = static_cast<int>(K / 64);
@@ -703,7 +706,7 @@ nvfp4_status nvfp4_moe_route(const int32_t *ids, int64_t T, int topk, int64_t E,
   DeviceInfo *d;
   nvfp4_status st = device_info(__func__, &d);
   if (st != NVFP4_OK) return st;
-  RouteBufs rb{counts, offsets, nullptr, nullptr, sorted_idx, inv_idx, nullptr};
+  RouteBufs rb{counts, offsets, nullptr, nullptr, sorted_idx, inv_idx, nullptr, nullptr};
   NV_CUDA(launch_route_amax(ids, static_cast<int>(T), topk, static_cast<int>(E), 0, rb, nullptr, 0, nullptr, 0,
                             nullptr, d->flags, static_cast<cudaStream_t>(stream)),
           "route kernel launch");

@@ -40,37 +40,37 @@ struct Tile {
   int a_row0;  // first A row (permuted/padded row index)
 };
 
-__device__ __forceinline__ void decode_tile(const GemmArgs &a, int idx, int n_tiles, Tile &t) {
-  const int mtg = idx / n_tiles;
-  t.nt = idx - mtg * n_tiles;
-  if (a.counts == nullptr) {  // every group has dense_M rows (G == 1: a dense GEMM)
-    const int mt_per_group = (a.dense_M + kBlockM - 1) / kBlockM;
-    t.g = mtg / mt_per_group;
-    t.mt = mtg - t.g * mt_per_group;
-    t.rows = min(kBlockM, a.dense_M - t.mt * kBlockM);
-    t.a_row0 = t.mt * kBlockM;
-    return;
-  }
-  // largest g with tile_offsets[g] <= mtg (empty groups have equal neighbours)
-  int lo = 0, hi = a.G - 1;
-  while (lo < hi) {
-    const int mid = (lo + hi + 1) >> 1;
-    if (__ldg(a.tile_offsets + mid) <= mtg)
-      lo = mid;
-    else
-      hi = mid - 1;
-  }
-  t.g = lo;
-  t.mt = mtg - __ldg(a.tile_offsets + lo);
-  t.rows = min(kBlockM, __ldg(a.counts + lo) - t.mt * kBlockM);
-  t.a_row0 = __ldg(a.pad_offsets + lo) + t.mt * kBlockM;
+// Schedule entry of m tile mtg: group, m tile inside the group, live rows, first A row.
+// Grouped problems read the table the routing kernel wrote; uniform groups compute it.
+// Callers fetch the entry of their next tile one tile ahead, so the load's latency
+// overlaps the current tile.
+__device__ __forceinline__ int4 tile_entry(const GemmArgs &a, int mtg) {
+  if (a.tile_table != nullptr) return __ldg(a.tile_table + mtg);
+  const int mt_per_group = (a.dense_M + kBlockM - 1) / kBlockM;
+  const int g = mtg / mt_per_group;
+  const int mt = mtg - g * mt_per_group;
+  return make_int4(g, mt, min(kBlockM, a.dense_M - mt * kBlockM), mt * kBlockM);
+}
+
+__device__ __forceinline__ Tile make_tile(const int4 e, int idx, int n_tiles) {
+  Tile t;
+  t.g = e.x;
+  t.mt = e.y;
+  t.rows = e.z;
+  t.a_row0 = e.w;
+  t.nt = idx - (idx / n_tiles) * n_tiles;
+  return t;
 }
 
 // instruction descriptor: E2M1 x E2M1, UE4M3 scales, K-major A and B, M=128, N=128
 constexpr uint32_t kIdesc = (1u << 7) | (1u << 10) | ((uint32_t(kBlockN) >> 3) << 17) |
                             ((uint32_t(kBlockM) >> 4) << 24);
 
-__device__ __forceinline__ float silu_mul(float g, float u) { return g / (1.0f + expf(-g)) * u; }
+// SiLU(g) * u with the fast exponential and divide (relative error ~1e-6; for g below
+// about -88, exp(-g) is +inf and the quotient is 0).
+__device__ __forceinline__ float silu_mul(float g, float u) {
+  return __fdividef(g, 1.0f + __expf(-g)) * u;
+}
 
 template <int kEpi>
 __global__ void __launch_bounds__(kGemmThreads, kCtasPerSm)
@@ -156,14 +156,12 @@ __global__ void __launch_bounds__(kGemmThreads, kCtasPerSm)
       int early = 0;
       if (args.early_b) {
         if (static_cast<int>(blockIdx.x) < total_tiles) {
-          Tile t;
-          decode_tile(args, blockIdx.x, n_tiles, t);
+          const Tile t = make_tile(tile_entry(args, blockIdx.x / n_tiles), blockIdx.x, n_tiles);
           const CUtensorMap *mb;
           int b_row0;
           const uint8_t *sfb;
           b_src(t, mb, b_row0, sfb);
-          const int group_rows = args.counts ? __ldg(args.counts + t.g) : args.dense_M;
-          const uint64_t pol_w = group_rows > kBlockM ? pol_reuse : pol_stream;
+          const uint64_t pol_w = (t.mt > 0 || t.rows == kBlockM) ? pol_reuse : pol_stream;
           early = min(kStages, k_stages);
           for (int s = 0; s < early; ++s) {
             const int kv = min(4, k_steps - 4 * s);
@@ -181,15 +179,18 @@ __global__ void __launch_bounds__(kGemmThreads, kCtasPerSm)
       uint32_t issued = 0;  // bit s: stage s has a load in flight with parity bit (s+8)
       int n_issued = 0;     // stages issued so far (the first `early` already hold their B)
       bool ok = true;
+      int4 next = static_cast<int>(blockIdx.x) < total_tiles ? tile_entry(args, blockIdx.x / n_tiles)
+                                                             : make_int4(0, 0, 0, 0);
       for (int idx = blockIdx.x; ok && idx < total_tiles; idx += gridDim.x) {
-        Tile t;
-        decode_tile(args, idx, n_tiles, t);
+        const Tile t = make_tile(next, idx, n_tiles);
+        if (idx + static_cast<int>(gridDim.x) < total_tiles)
+          next = tile_entry(args, (idx + gridDim.x) / n_tiles);
         const CUtensorMap *mb;
         int b_row0;
         const uint8_t *sfb;
         b_src(t, mb, b_row0, sfb);
-        const int group_rows = args.counts ? __ldg(args.counts + t.g) : args.dense_M;
-        const uint64_t pol_w = group_rows > kBlockM ? pol_reuse : pol_stream;
+        // weights of a group with further m tiles are read again by them
+        const uint64_t pol_w = (t.mt > 0 || t.rows == kBlockM) ? pol_reuse : pol_stream;
         const uint8_t *sfa =
             args.a_sf + (static_cast<size_t>(t.a_row0 / kBlockM) * args.a_kc_total +
                          static_cast<size_t>(t.g) * args.a_group_koff) * kSfBytesPerKStep;
@@ -304,11 +305,26 @@ __global__ void __launch_bounds__(kGemmThreads, kCtasPerSm)
     int sstage = 0;
     uint32_t sphase = 0;
     int it = 0;
+    int4 next = static_cast<int>(blockIdx.x) < total_tiles ? tile_entry(args, blockIdx.x / n_tiles)
+                                                           : make_int4(0, 0, 0, 0);
     for (int idx = blockIdx.x; idx < total_tiles; idx += gridDim.x, ++it) {
-      Tile t;
-      decode_tile(args, idx, n_tiles, t);
+      const Tile t = make_tile(next, idx, n_tiles);
+      if (idx + static_cast<int>(gridDim.x) < total_tiles)
+        next = tile_entry(args, (idx + gridDim.x) / n_tiles);
       const int acc = kAccBufs == 2 ? (it & 1) : 0;
       const uint32_t acc_phase = kAccBufs == 2 ? ((it >> 1) & 1) : (it & 1);
+      // Per-tile epilogue scalars, loaded before this tile's main loop so that their
+      // latency is hidden behind it.
+      const bool sh = t.g == args.shared_group;
+      const float ws2 = sh ? __ldg(args.ws2_shared) : __ldg(args.ws2 + t.g);
+      float g_aux = 0.f;  // W13: static scale of h; W2: global scale of the w2 input
+      int seg_base = 0;   // W2: first sorted entry of the group
+      if constexpr (kEpi == static_cast<int>(Epi::kW13)) g_aux = __ldg(args.gs_out + t.g);
+      if constexpr (kEpi == static_cast<int>(Epi::kW2)) {
+        g_aux = __ldg(args.gs_a + t.g);
+        if (!sh) seg_base = __ldg(args.offsets + t.g);
+      }
+      const bool row_ok = m < t.rows;
       bool ok = true;
       for (int ks = 0; ks < k_stages; ++ks) {
         const int kv = min(4, k_steps - 4 * ks);
@@ -339,20 +355,42 @@ __global__ void __launch_bounds__(kGemmThreads, kCtasPerSm)
         }
       }
       if (!ok) break;
+      // W2: token and routing weight of this thread's row, while the last MMAs run
+      float w2_scale = 0.f;
+      int64_t w2_tok = 0;
+      if constexpr (kEpi == static_cast<int>(Epi::kW2)) {
+        if (row_ok) {
+          const int seg_row = t.mt * kBlockM + m;
+          float w = 1.f;
+          if (sh) {
+            w2_tok = seg_row;
+          } else {
+            const int f = __ldg(args.sorted_idx + seg_base + seg_row);
+            w2_tok = f / args.topk;
+            w = __ldg(args.topk_w + f);
+          }
+          w2_scale = g_aux * ws2 * w;
+        }
+      }
       ok = mbar_wait_bounded(&tfull[acc], acc_phase, abort_flag, args.err, kPipelineTimeoutNs);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       tc_fence_after();
       const uint32_t tbase = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
                              static_cast<uint32_t>(acc * kBlockN);
-      const bool row_ok = m < t.rows;
-      const bool sh = t.g == args.shared_group;
-      const float ws2 = sh ? __ldg(args.ws2_shared) : __ldg(args.ws2 + t.g);
       // A warp whose 32 accumulator rows are all padding (a group's last m tile) has
       // nothing to read or store; it only releases the accumulator.
       const bool warp_live = quarter * 32 < t.rows;
+      // Each warp hands its accumulator lanes back to the MMA as soon as it has read
+      // them, so the next tile's MMAs overlap this tile's global stores.
+      auto release = [&]() {
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&tempty[acc]);
+      };
 
       if (!warp_live) {
+        release();
       } else if constexpr (kEpi == static_cast<int>(Epi::kLinear)) {
         const float alpha = gs_scalar * ws2;
         const int64_t row = t.a_row0 + m;
@@ -364,6 +402,7 @@ __global__ void __launch_bounds__(kGemmThreads, kCtasPerSm)
           uint32_t r[16];
           tmem_ld16(tbase + c * 16, r);
           tmem_ld_wait();
+          if (c == kBlockN / 16 - 1) release();
           if (row_ok) {
             uint32_t packed[8];
 #pragma unroll
@@ -379,7 +418,7 @@ __global__ void __launch_bounds__(kGemmThreads, kCtasPerSm)
         }
       } else if constexpr (kEpi == static_cast<int>(Epi::kW13)) {
         const float alpha = gs_scalar * ws2;
-        const float gs2 = __ldg(args.gs_out + t.g);
+        const float gs2 = g_aux;
         const float six_gs2 = __fmul_rn(6.0f, gs2);
         const int64_t p = t.a_row0 + m;
         const int I = args.out_ld * 2;
@@ -407,6 +446,7 @@ __global__ void __launch_bounds__(kGemmThreads, kCtasPerSm)
           codes[2 * c + 1] = cw[1];
           sfw |= sfb << (8 * c);
         }
+        release();
         if (row_ok) {
           uint4 *dst = reinterpret_cast<uint4 *>(static_cast<uint8_t *>(args.out) +
                                                  p * args.out_ld + t.nt * 32);
@@ -415,41 +455,30 @@ __global__ void __launch_bounds__(kGemmThreads, kCtasPerSm)
           *reinterpret_cast<uint32_t *>(args.out_sf + sf_word_offset(p, t.nt, I / 64)) = sfw;
         }
       } else {  // kW2
-        float scale = 0.f;
-        int64_t tok = 0;
-        if (row_ok) {
-          const int seg_row = t.mt * kBlockM + m;
-          float w = 1.f;
-          if (sh) {
-            tok = seg_row;
-          } else {
-            const int f = __ldg(args.sorted_idx + __ldg(args.offsets + t.g) + seg_row);
-            tok = f / args.topk;
-            w = __ldg(args.topk_w + f);
-          }
-          scale = __ldg(args.gs_a + t.g) * ws2 * w;
-        }
+        const float scale = w2_scale;
+        const int64_t tok = w2_tok;
         float4 *dst = reinterpret_cast<float4 *>(static_cast<float *>(args.out) +
                                                  tok * args.out_ld + t.nt * kBlockN);
-#pragma unroll 1
-        for (int c = 0; c < kBlockN / 16; ++c) {
-          uint32_t r[16];
-          tmem_ld16(tbase + c * 16, r);
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          uint32_t r[4][16];
+#pragma unroll
+          for (int q = 0; q < 4; ++q) tmem_ld16(tbase + h * 64 + q * 16, r[q]);
           tmem_ld_wait();
+          if (h == 1) release();
           if (row_ok) {
 #pragma unroll
-            for (int i = 0; i < 4; ++i)
-              atomicAdd(dst + c * 4 + i,
-                        make_float4(__uint_as_float(r[4 * i]) * scale,
-                                    __uint_as_float(r[4 * i + 1]) * scale,
-                                    __uint_as_float(r[4 * i + 2]) * scale,
-                                    __uint_as_float(r[4 * i + 3]) * scale));
+            for (int q = 0; q < 4; ++q)
+#pragma unroll
+              for (int i = 0; i < 4; ++i)
+                atomicAdd(dst + h * 16 + q * 4 + i,
+                          make_float4(__uint_as_float(r[q][4 * i]) * scale,
+                                      __uint_as_float(r[q][4 * i + 1]) * scale,
+                                      __uint_as_float(r[q][4 * i + 2]) * scale,
+                                      __uint_as_float(r[q][4 * i + 3]) * scale));
           }
         }
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&tempty[acc]);
     }
   }
 

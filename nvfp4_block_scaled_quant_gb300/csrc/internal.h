@@ -65,6 +65,9 @@ struct GemmArgs {
   const int *offsets;       // [G+1] unpadded (sorted order)
   const int *pad_offsets;   // [G+1]
   const int *tile_offsets;  // [G+1]
+  const int4 *tile_table;   // per m tile in tile order: group, m tile in group, live rows,
+                            // first A row (written by the routing kernel); null: every group
+                            // has dense_M rows
   int shared_group;         // group using the *_shared weights, or -1
   // scale factors
   const uint8_t *a_sf;      // swizzled, 128-row blocks aligned with the A rows
@@ -136,6 +139,7 @@ cudaError_t launch_prepare(const uint8_t *w, const uint8_t *sf, int64_t G, int64
 
 struct RouteBufs {
   int *counts, *offsets, *pad_offsets, *tile_offsets, *sorted_idx, *inv_idx, *dest_rows;
+  int4 *tile_table;  // per 128-row tile: group, tile in group, live rows, first row (or null)
 };
 cudaError_t launch_route_amax(const int32_t *ids, int T, int topk, int E, int has_shared,
                               RouteBufs rb, const void *x, int64_t H, uint32_t *partials,

@@ -9,7 +9,16 @@ namespace {
 
 constexpr int kRouteThreads = 512;
 constexpr int kDispatchThreads = 256;
-constexpr int kRouteChunk = 2048;  // ids staged in shared memory per ranking pass
+constexpr int kRankWarps = kRouteThreads / 32;
+constexpr int kRankPerWarp = 128;                      // entries per warp and chunk
+constexpr int kRankChunk = kRankWarps * kRankPerWarp;  // entries ranked per pass
+constexpr int kSmallRank = 256;                        // up to this many entries one warp ranks
+
+// dynamic shared memory of the routing block (counts, cursors, deltas, scan scratch,
+// per-warp counts)
+size_t route_smem_bytes(int E) {
+  return sizeof(int) * (static_cast<size_t>(E) * (3 + kRankWarps) + 1 + 96);
+}
 
 // Block-wide exclusive scan of three int sequences of length n (n <= 4 * blockDim).
 // Writes out_x[0..n] (n+1 entries, the last one the total; n >= 1); out_pad and
@@ -90,6 +99,14 @@ __device__ void block_scan3(const int *in_count, int n, int *out_off, int *out_p
 
 // Block 0 routes; blocks 1.. compute amax partials of x (when partials != nullptr)
 // and zero the fp32 accumulator y_acc (T*H floats).
+//
+// Routing keeps flat order within each expert (a stable counting sort of the
+// T*k entries).  Up to kSmallRank entries one warp walks them 32 at a time.
+// Beyond that the entries go in chunks of kRankChunk: warp w owns the
+// contiguous slice [w*kRankPerWarp, (w+1)*kRankPerWarp) of the chunk, counts
+// its entries per expert, a scan over the warps (per expert, in warp order)
+// turns the counts into starting positions, and a second walk hands out
+// consecutive positions to equal experts in flat order.
 __global__ void __launch_bounds__(kRouteThreads) route_amax_kernel(
     const int32_t *__restrict__ ids, int T, int topk, int E, int has_shared, RouteBufs rb,
     const uint16_t *__restrict__ x, int64_t H, uint32_t *__restrict__ partials, int nparts,
@@ -97,21 +114,30 @@ __global__ void __launch_bounds__(kRouteThreads) route_amax_kernel(
   pdl_wait();
   pdl_trigger();
   if (blockIdx.x == 0) {
-    __shared__ int s_cnt[kMaxExperts + 1];
-    __shared__ int s_cursor[kMaxExperts];
-    __shared__ int s_delta[kMaxExperts];  // padded row - sorted position, per expert
-    __shared__ int s_tmp[96];
-    __shared__ int s_ids[kRouteChunk];
+    extern __shared__ int route_smem[];
+    int *s_cnt = route_smem;        // G = E (+1 shared) counts
+    int *s_cursor = s_cnt + E + 1;  // next free sorted position per expert
+    int *s_delta = s_cursor + E;    // padded row - sorted position, per expert
+    int *s_tmp = s_delta + E;       // scan scratch (96)
+    int *s_wcnt = s_tmp + 96;       // kRankWarps x E per-warp counts, then positions
     const int G = E + (has_shared ? 1 : 0);
     const int Tk = T * topk;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     for (int g = threadIdx.x; g < G; g += blockDim.x) s_cnt[g] = 0;
     __syncthreads();
-    for (int f = threadIdx.x; f < Tk; f += blockDim.x) {
-      const int e = ids[f];
-      if (e >= 0 && e < E)
-        atomicAdd(&s_cnt[e], 1);
-      else
-        raise_device_error(err, NVFP4_DEVERR_BAD_EXPERT_ID);
+    // histogram: one shared-memory atomic per distinct expert of each 32 entries
+    for (int f0 = warp * 32; f0 < Tk; f0 += blockDim.x) {
+      const int f = f0 + lane;
+      int e = -1;
+      if (f < Tk) {
+        e = __ldg(ids + f);
+        if (e < 0 || e >= E) {
+          raise_device_error(err, NVFP4_DEVERR_BAD_EXPERT_ID);
+          e = -1;
+        }
+      }
+      const unsigned peers = __match_any_sync(0xffffffffu, e);
+      if (e >= 0 && lane == __ffs(peers) - 1) atomicAdd(&s_cnt[e], __popc(peers));
     }
     if (has_shared && threadIdx.x == 0) s_cnt[E] = T;
     __syncthreads();
@@ -122,43 +148,76 @@ __global__ void __launch_bounds__(kRouteThreads) route_amax_kernel(
       s_cursor[e] = rb.offsets[e];
       s_delta[e] = rb.pad_offsets ? rb.pad_offsets[e] - rb.offsets[e] : 0;
     }
+    // the GEMMs' tile schedule: one entry per 128-row tile of the permuted buffers
+    if (rb.tile_table)
+      for (int g = threadIdx.x; g < G; g += blockDim.x) {
+        const int c = s_cnt[g], t0 = rb.tile_offsets[g], p0 = rb.pad_offsets[g];
+        for (int mt = 0; mt * kBlockM < c; ++mt)
+          rb.tile_table[t0 + mt] = make_int4(g, mt, min(kBlockM, c - mt * kBlockM), p0 + mt * kBlockM);
+      }
     __syncthreads();
-    // Stable ranking: the ids are staged in shared memory chunk by chunk; one warp
-    // walks each chunk in order, 32 entries at a time, and lanes holding the same
-    // expert get consecutive positions in flat order.
-    for (int base = 0; base < Tk; base += kRouteChunk) {
-      const int n = min(kRouteChunk, Tk - base);
-      for (int i = threadIdx.x; i < n; i += blockDim.x) s_ids[i] = ids[base + i];
-      __syncthreads();
-      if (threadIdx.x < 32) {
-        const int lane = threadIdx.x;
-        for (int b = 0; b < n; b += 32) {
-          const int fl = b + lane;
-          int e = fl < n ? s_ids[fl] : -1;
-          if (e < 0 || e >= E) e = -1;
-          const unsigned peers = __match_any_sync(0xffffffffu, e);
-          const int leader = __ffs(peers) - 1;
-          const int rank = __popc(peers & ((1u << lane) - 1u));
-          int start = 0;
-          if (lane == leader && e >= 0) {
-            start = s_cursor[e];
-            s_cursor[e] = start + __popc(peers);
-          }
-          start = __shfl_sync(0xffffffffu, start, leader);
-          if (fl < n) {
-            const int f = base + fl;
-            if (e >= 0) {
-              const int pos = start + rank;
-              rb.sorted_idx[pos] = f;
-              rb.inv_idx[f] = pos;
-              if (rb.dest_rows) rb.dest_rows[f] = s_delta[e] + pos;
-            } else {
-              rb.inv_idx[f] = -1;
-              if (rb.dest_rows) rb.dest_rows[f] = -1;
-            }
-          }
+    // Hand out positions to the 32 entries starting at f0 (warp-uniform), taking
+    // each expert's next position from slot[e] and advancing it.
+    auto place32 = [&](int f0, int e, int *slot) {
+      const int f = f0 + lane;
+      const unsigned peers = __match_any_sync(0xffffffffu, e);
+      const int leader = __ffs(peers) - 1;
+      const int rank = __popc(peers & ((1u << lane) - 1u));
+      int start = 0;
+      if (lane == leader && e >= 0) {
+        start = slot[e];
+        slot[e] = start + __popc(peers);
+      }
+      start = __shfl_sync(0xffffffffu, start, leader);
+      if (f < Tk) {
+        if (e >= 0) {
+          const int pos = start + rank;
+          rb.sorted_idx[pos] = f;
+          rb.inv_idx[f] = pos;
+          if (rb.dest_rows) rb.dest_rows[f] = s_delta[e] + pos;
+        } else {
+          rb.inv_idx[f] = -1;
+          if (rb.dest_rows) rb.dest_rows[f] = -1;
         }
       }
+      __syncwarp();
+    };
+    auto load_id = [&](int f) {
+      int e = f < Tk ? __ldg(ids + f) : -1;
+      return (e < 0 || e >= E) ? -1 : e;
+    };
+    if (Tk <= kSmallRank) {
+      if (warp == 0)
+        for (int f0 = 0; f0 < Tk; f0 += 32) place32(f0, load_id(f0 + lane), s_cursor);
+      return;
+    }
+    for (int base = 0; base < Tk; base += kRankChunk) {
+      for (int i = threadIdx.x; i < kRankWarps * E; i += blockDim.x) s_wcnt[i] = 0;
+      __syncthreads();
+      int *my_cnt = s_wcnt + warp * E;
+      const int w0 = base + warp * kRankPerWarp;
+      int my_e[kRankPerWarp / 32];
+#pragma unroll
+      for (int j = 0; j < kRankPerWarp / 32; ++j) {
+        const int e = load_id(w0 + 32 * j + lane);
+        my_e[j] = e;
+        const unsigned peers = __match_any_sync(0xffffffffu, e);
+        if (e >= 0 && lane == __ffs(peers) - 1) my_cnt[e] += __popc(peers);
+        __syncwarp();
+      }
+      __syncthreads();
+      for (int e = threadIdx.x; e < E; e += blockDim.x) {
+        int run = s_cursor[e];
+        for (int w = 0; w < kRankWarps; ++w) {
+          const int c = s_wcnt[w * E + e];
+          s_wcnt[w * E + e] = run;
+          run += c;
+        }
+        s_cursor[e] = run;
+      }
+      __syncthreads();
+#pragma unroll
+      for (int j = 0; j < kRankPerWarp / 32; ++j) place32(w0 + 32 * j, my_e[j], my_cnt);
       __syncthreads();
     }
     return;
@@ -280,7 +339,13 @@ cudaError_t launch_route_amax(const int32_t *ids, int T, int topk, int E, int ha
   if (partials && helpers < nparts) helpers = nparts;
   if (helpers < 1) helpers = 1;
   if (helpers > 1024) helpers = 1024;
-  return launch_pdl(route_amax_kernel, dim3(1 + helpers), dim3(kRouteThreads), 0, s, ids, T, topk, E,
+  const size_t smem = route_smem_bytes(E);
+  if (smem > 48 * 1024) {
+    const cudaError_t e = cudaFuncSetAttribute(route_amax_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                               static_cast<int>(route_smem_bytes(kMaxExperts)));
+    if (e != cudaSuccess) return e;
+  }
+  return launch_pdl(route_amax_kernel, dim3(1 + helpers), dim3(kRouteThreads), smem, s, ids, T, topk, E,
                     has_shared, rb, static_cast<const uint16_t *>(x), H, partials, nparts, y_acc, err);
 }
 

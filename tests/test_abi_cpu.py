@@ -22,7 +22,7 @@ def test_exports_every_declared_symbol(L):
     for n in names:
         assert hasattr(L, n), n
     assert set(names) == set(_lib._SIGNATURES), "binding signatures and header disagree"
-    assert L.nvfp4_abi_version() == 1
+    assert L.nvfp4_abi_version() == _lib.ABI_VERSION
 
 
 def test_sf_bytes_matches_layout_definition(L):
@@ -95,7 +95,8 @@ def test_valid_call_without_a_gpu_fails_cleanly(L):
 def test_moe_workspace_layout(L, T, H, I, E, k, sh):
     lay = _lib.MoeWsLayout()
     assert L.nvfp4_moe_workspace_layout(T, H, I, E, k, sh, ctypes.byref(lay)) == 0
-    fields = ["counts", "offsets", "pad_offsets", "tile_offsets", "sorted_idx", "inv_idx", "dest_rows", "amax_partials", "xq",
+    fields = ["counts", "offsets", "pad_offsets", "tile_offsets", "sorted_idx", "inv_idx", "dest_rows", "tile_table",
+              "amax_partials", "xq",
               "xsf", "hq", "hsf", "y_acc", "total"]
     offs = [getattr(lay, f) for f in fields]
     assert offs == sorted(offs) and all(o % 256 == 0 for o in offs)
@@ -104,6 +105,7 @@ def test_moe_workspace_layout(L, T, H, I, E, k, sh):
     assert rc % 128 == 0
     # the padded segments always fit: sum_e roundup(c_e, 128) <= T*k + 127 * min(E, T*k), plus the shared rows
     assert rc >= T * k + (127 * min(E, T * k)) // 128 * 128 + (((T + 127) // 128) * 128 if sh else 0)
+    assert lay.amax_partials - lay.tile_table >= rc // 128 * 16   # one int32x4 entry per 128-row tile
     assert lay.xsf - lay.xq >= rc * H // 2 and lay.hq - lay.xsf >= O.sf_bytes(rc, H)
     assert lay.hsf - lay.hq >= rc * I // 2 and lay.y_acc - lay.hsf >= O.sf_bytes(rc, I)
     assert lay.total - lay.y_acc >= T * H * 4
