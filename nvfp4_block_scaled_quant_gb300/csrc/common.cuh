@@ -237,6 +237,13 @@ __device__ __forceinline__ void tmem_st_wait() {
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
+// One 32-byte global store (256-bit vector); the address must be 32-byte aligned.
+__device__ __forceinline__ void st_global_v8(void *p, const uint32_t (&w)[8]) {
+  asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(w[0]), "r"(w[1]),
+               "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7])
+               : "memory");
+}
+
 // ---------------------------------------------------------------- NVFP4 block encoder
 
 // Unsigned E4M3 byte -> fp32 (exact): bias 7, subnormal m * 2^-9 at exponent 0.

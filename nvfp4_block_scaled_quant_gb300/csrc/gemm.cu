@@ -393,6 +393,7 @@ __global__ void __launch_bounds__(kGemmThreads, kCtasPerSm)
         release();
       } else if constexpr (kEpi == static_cast<int>(Epi::kLinear)) {
         const float alpha = gs_scalar * ws2;
+        const bool out32 = (reinterpret_cast<uintptr_t>(args.out) & 31u) == 0;
         const int64_t row = t.a_row0 + m;
         __nv_bfloat16 *y = static_cast<__nv_bfloat16 *>(args.out) +
                            row * static_cast<int64_t>(args.out_ld) +
@@ -411,9 +412,15 @@ __global__ void __launch_bounds__(kGemmThreads, kCtasPerSm)
                   __uint_as_float(r[2 * i]) * alpha, __uint_as_float(r[2 * i + 1]) * alpha);
               packed[i] = *reinterpret_cast<const uint32_t *>(&v);
             }
-            uint4 *dst = reinterpret_cast<uint4 *>(y + c * 16);
-            dst[0] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
-            dst[1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
+            // 32 bytes per row and chunk: one 256-bit store when the output is 32-byte
+            // aligned (row strides and column offsets are multiples of 256 bytes)
+            if (out32) {
+              st_global_v8(y + c * 16, packed);
+            } else {
+              uint4 *dst = reinterpret_cast<uint4 *>(y + c * 16);
+              dst[0] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+              dst[1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
+            }
           }
         }
       } else if constexpr (kEpi == static_cast<int>(Epi::kW13)) {
@@ -448,10 +455,9 @@ __global__ void __launch_bounds__(kGemmThreads, kCtasPerSm)
         }
         release();
         if (row_ok) {
-          uint4 *dst = reinterpret_cast<uint4 *>(static_cast<uint8_t *>(args.out) +
-                                                 p * args.out_ld + t.nt * 32);
-          dst[0] = make_uint4(codes[0], codes[1], codes[2], codes[3]);
-          dst[1] = make_uint4(codes[4], codes[5], codes[6], codes[7]);
+          // 32 code bytes of this row and tile; the workspace is 256-byte aligned and
+          // rows are I/2 (a multiple of 32) bytes apart
+          st_global_v8(static_cast<uint8_t *>(args.out) + p * args.out_ld + t.nt * 32, codes);
           *reinterpret_cast<uint32_t *>(args.out_sf + sf_word_offset(p, t.nt, I / 64)) = sfw;
         }
       } else {  // kW2
