@@ -67,6 +67,19 @@ __global__ void __launch_bounds__(kQuantThreads) quantize_kernel(
   __shared__ uint32_t scratch[32];
   pdl_wait();
   pdl_trigger();
+  const int64_t kb = K / 16;
+  const int64_t gb = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const bool valid = gb < rows_total * kb;
+  const int64_t r = valid ? gb / kb : 0;
+  const int64_t c = valid ? gb - r * kb : 0;
+  const bool live = valid && r < M;
+  // the block's 16 elements are loaded first: their latency overlaps the gs reduction
+  uint4 a = make_uint4(0u, 0u, 0u, 0u), b = a;
+  if (live) {
+    const uint4 *src = reinterpret_cast<const uint4 *>(x + r * ldx + c * 16);
+    a = __ldg(src);
+    b = __ldg(src + 1);
+  }
   float gs;
   if (partials) {
     gs = gs_from_partials(partials, nparts, scratch);
@@ -75,16 +88,8 @@ __global__ void __launch_bounds__(kQuantThreads) quantize_kernel(
     gs = *gs_static;
   }
   const float six_gs = __fmul_rn(6.0f, gs);
-  const int64_t kb = K / 16;
-  const int64_t gb = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-  const bool valid = gb < rows_total * kb;
-  const int64_t r = valid ? gb / kb : 0;
-  const int64_t c = valid ? gb - r * kb : 0;
-  const bool live = valid && r < M;
   uint32_t sfb = 0;
   if (live) {
-    const uint4 *src = reinterpret_cast<const uint4 *>(x + r * ldx + c * 16);
-    const uint4 a = __ldg(src), b = __ldg(src + 1);
     const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
     float v[16];
 #pragma unroll

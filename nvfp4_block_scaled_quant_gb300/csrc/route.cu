@@ -9,6 +9,7 @@ namespace {
 
 constexpr int kRouteThreads = 512;
 constexpr int kDispatchThreads = 256;
+constexpr int kDestRegs = 8;  // destination rows held in registers (top-k up to 8)
 constexpr int kRankWarps = kRouteThreads / 32;
 constexpr int kRankPerWarp = 128;                      // entries per warp and chunk
 constexpr int kRankChunk = kRankWarps * kRankPerWarp;  // entries ranked per pass
@@ -17,7 +18,7 @@ constexpr int kSmallRank = 256;                        // up to this many entrie
 // dynamic shared memory of the routing block (counts, cursors, deltas, scan scratch,
 // per-warp counts)
 size_t route_smem_bytes(int E) {
-  return sizeof(int) * (static_cast<size_t>(E) * (3 + kRankWarps) + 1 + 96);
+  return sizeof(int) * (static_cast<size_t>(E) * (6 + kRankWarps) + 1 + 96 + 6);
 }
 
 // Block-wide exclusive scan of three int sequences of length n (n <= 4 * blockDim).
@@ -119,7 +120,10 @@ __global__ void __launch_bounds__(kRouteThreads) route_amax_kernel(
     int *s_cursor = s_cnt + E + 1;  // next free sorted position per expert
     int *s_delta = s_cursor + E;    // padded row - sorted position, per expert
     int *s_tmp = s_delta + E;       // scan scratch (96)
-    int *s_wcnt = s_tmp + 96;       // kRankWarps x E per-warp counts, then positions
+    int *s_off = s_tmp + 96;        // G + 1 exclusive scans: rows, padded rows, tiles
+    int *s_pad = s_off + E + 2;
+    int *s_tiles = s_pad + E + 2;
+    int *s_wcnt = s_tiles + E + 2;  // kRankWarps x E per-warp counts, then positions
     const int G = E + (has_shared ? 1 : 0);
     const int Tk = T * topk;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -141,17 +145,22 @@ __global__ void __launch_bounds__(kRouteThreads) route_amax_kernel(
     }
     if (has_shared && threadIdx.x == 0) s_cnt[E] = T;
     __syncthreads();
-    for (int g = threadIdx.x; g < G; g += blockDim.x) rb.counts[g] = s_cnt[g];
-    block_scan3(s_cnt, G, rb.offsets, rb.pad_offsets, rb.tile_offsets, s_tmp);
+    block_scan3(s_cnt, G, s_off, s_pad, s_tiles, s_tmp);
     __syncthreads();
+    for (int g = threadIdx.x; g <= G; g += blockDim.x) {
+      if (g < G) rb.counts[g] = s_cnt[g];
+      rb.offsets[g] = s_off[g];
+      if (rb.pad_offsets) rb.pad_offsets[g] = s_pad[g];
+      if (rb.tile_offsets) rb.tile_offsets[g] = s_tiles[g];
+    }
     for (int e = threadIdx.x; e < E; e += blockDim.x) {
-      s_cursor[e] = rb.offsets[e];
-      s_delta[e] = rb.pad_offsets ? rb.pad_offsets[e] - rb.offsets[e] : 0;
+      s_cursor[e] = s_off[e];
+      s_delta[e] = s_pad[e] - s_off[e];
     }
     // the GEMMs' tile schedule: one entry per 128-row tile of the permuted buffers
     if (rb.tile_table)
       for (int g = threadIdx.x; g < G; g += blockDim.x) {
-        const int c = s_cnt[g], t0 = rb.tile_offsets[g], p0 = rb.pad_offsets[g];
+        const int c = s_cnt[g], t0 = s_tiles[g], p0 = s_pad[g];
         for (int mt = 0; mt * kBlockM < c; ++mt)
           rb.tile_table[t0 + mt] = make_int4(g, mt, min(kBlockM, c - mt * kBlockM), p0 + mt * kBlockM);
       }
@@ -257,7 +266,7 @@ __global__ void __launch_bounds__(kRouteThreads) route_amax_kernel(
 // One thread per 16-element block of x (T, H).  Every token is quantised once
 // and its codes and scales are written to its row in each routed expert's
 // segment (and the shared expert's segment).
-__global__ void __launch_bounds__(kDispatchThreads) dispatch_quant_kernel(
+__global__ void __launch_bounds__(kDispatchThreads, 1) dispatch_quant_kernel(
     const uint16_t *__restrict__ x, int T, int64_t H, int topk, int E, int has_shared,
     const int32_t *__restrict__ ids, RouteBufs rb, const uint32_t *__restrict__ partials,
     int nparts, const float *__restrict__ gs_static, float *__restrict__ gs_out,
@@ -265,6 +274,23 @@ __global__ void __launch_bounds__(kDispatchThreads) dispatch_quant_kernel(
   __shared__ uint32_t scratch[32];
   pdl_wait();
   pdl_trigger();
+  const int64_t kb = H / 16;
+  const int64_t gb = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const bool valid = gb < static_cast<int64_t>(T) * kb;
+  const int64_t t = valid ? gb / kb : 0;
+  const int64_t c = valid ? gb - t * kb : 0;
+  // The block's 16 elements and the token's destination rows are loaded first, so
+  // their latency overlaps the gs reduction.
+  uint4 a = make_uint4(0u, 0u, 0u, 0u), b = a;
+  int dest[kDestRegs];
+  const int *dest_src = rb.dest_rows + t * topk;
+  if (valid) {
+    const uint4 *src = reinterpret_cast<const uint4 *>(x + t * H + c * 16);
+    a = __ldg(src);
+    b = __ldg(src + 1);
+  }
+#pragma unroll
+  for (int j = 0; j < kDestRegs; ++j) dest[j] = (valid && j < topk && topk <= kDestRegs) ? __ldg(dest_src + j) : -1;
   float gs;
   if (partials) {
     gs = gs_from_partials(partials, nparts, scratch);
@@ -273,15 +299,8 @@ __global__ void __launch_bounds__(kDispatchThreads) dispatch_quant_kernel(
     gs = *gs_static;
   }
   const float six_gs = __fmul_rn(6.0f, gs);
-  const int64_t kb = H / 16;
-  const int64_t gb = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-  const bool valid = gb < static_cast<int64_t>(T) * kb;
-  const int64_t t = valid ? gb / kb : 0;
-  const int64_t c = valid ? gb - t * kb : 0;
   uint32_t codes[2] = {0u, 0u}, sfb = 0;
   if (valid) {
-    const uint4 *src = reinterpret_cast<const uint4 *>(x + t * H + c * 16);
-    const uint4 a = __ldg(src), b = __ldg(src + 1);
     const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
     float v[16];
 #pragma unroll
@@ -298,21 +317,23 @@ __global__ void __launch_bounds__(kDispatchThreads) dispatch_quant_kernel(
   if (!valid) return;
   const uint2 cv = make_uint2(codes[0], codes[1]);
   const bool sf_writer = (lane & 3) == 0;
-  // destination rows: routed entries from the routing kernel, then the shared segment
-  const int *dest = rb.dest_rows + t * topk;
-#pragma unroll 4
-  for (int j = 0; j <= topk; ++j) {
-    int64_t p;
-    if (j < topk) {
-      p = __ldg(dest + j);
-      if (p < 0) continue;
-    } else {
-      if (!has_shared) break;
-      p = static_cast<int64_t>(__ldg(rb.pad_offsets + E)) + t;
-    }
+  auto put = [&](int64_t p) {
     *reinterpret_cast<uint2 *>(xq + p * (H / 2) + c * 8) = cv;
     if (sf_writer) *reinterpret_cast<uint32_t *>(xsf + sf_word_offset(p, c >> 2, kb >> 2)) = word;
+  };
+  // destination rows: routed entries from the routing kernel (dropped entries are -1),
+  // then the shared segment
+  if (topk <= kDestRegs) {
+#pragma unroll
+    for (int j = 0; j < kDestRegs; ++j)
+      if (dest[j] >= 0) put(dest[j]);
+  } else {
+    for (int j = 0; j < topk; ++j) {
+      const int p = __ldg(dest_src + j);
+      if (p >= 0) put(p);
+    }
   }
+  if (has_shared) put(static_cast<int64_t>(__ldg(rb.pad_offsets + E)) + t);
 }
 
 __global__ void finalize_kernel(const float4 *__restrict__ acc, int64_t n4, uint2 *__restrict__ y) {
