@@ -151,7 +151,7 @@ def run_native(args, rank: int, world: int, local_rank: int):
 
     from nvfp4_block_scaled_quant_gb300 import build as B
     B.build()
-    from nvfp4_block_scaled_quant_gb300 import model, ops, workloads
+    from nvfp4_block_scaled_quant_gb300 import model, ops, replicas, workloads
 
     dev = torch.device("cuda", local_rank)
     torch.cuda.set_device(dev)
@@ -231,16 +231,13 @@ def run_native(args, rank: int, world: int, local_rank: int):
     clk = clocks.stop()
     t_w13 = sum(ev[s][c][0].elapsed_time(ev[s][c][1]) for s in range(args.steps) for c in range(C)) / args.steps
     t_w2 = sum(ev[s][c][2].elapsed_time(ev[s][c][3]) for s in range(args.steps) for c in range(C)) / args.steps
-    if dist:
-        tt = torch.tensor([elapsed_ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        elapsed_ms = float(tt.item())
     st, flags = ops.device_error()
     if st != 0:
         raise RuntimeError(f"device fault flags {flags:#x} in the timed region")
 
+    # independent replicas: all ranks' tokens over the slowest rank's time
     tokens_per_step = T * C
-    value = world * tokens_per_step * args.steps / (elapsed_ms / 1e3)
+    value, elapsed_ms, _ = replicas.replica_throughput(elapsed_ms, tokens_per_step * args.steps, device=dev)
     ms_per_step = elapsed_ms / args.steps
     hbm, bf16, bf16_sus, peak_kind = peaks()
     fp4_peak = bf16 * FP4_OVER_BF16
