@@ -91,6 +91,7 @@ typedef enum nvfp4_status {
 /* device fault flags returned by nvfp4_get_device_error */
 #define NVFP4_DEVERR_BAD_EXPERT_ID 1  /* a top-k id outside [0, E); the entry was dropped  */
 #define NVFP4_DEVERR_PIPELINE_TIMEOUT 2 /* a GEMM pipeline wait exceeded its limit        */
+#define NVFP4_DEVERR_INTERNAL 4         /* a kernel invariant failed (a library bug)      */
 
 NVFP4_API int nvfp4_abi_version(void);
 NVFP4_API const char *nvfp4_status_string(nvfp4_status s);

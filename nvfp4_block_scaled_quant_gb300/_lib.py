@@ -33,6 +33,7 @@ PREP_PLAIN = 0
 PREP_W13_INTERLEAVE = 1
 DEVERR_BAD_EXPERT_ID = 1
 DEVERR_PIPELINE_TIMEOUT = 2
+DEVERR_INTERNAL = 4
 LINEAR_NOALLOC_MAX_BYTES = 4 << 20
 
 

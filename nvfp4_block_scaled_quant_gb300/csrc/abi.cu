@@ -298,7 +298,10 @@ nvfp4_status moe_gemm_impl(const char *fn, DeviceInfo *d, Epi epi, int64_t T, in
     a.topk_w = topk_w;
     a.topk = topk;
   }
-  NV_CUDA(launch_gemm(epi, ta, tb, tbs, a, d->sms * kCtasPerSm, false, s), "grouped GEMM launch");
+  // A routed group holds at most T*topk rows (duplicate ids included) and the shared one T:
+  // when both stay within one 32-row box, the ring with 4 small stages applies.
+  const bool small_a = T * topk <= kABoxRows && T <= kABoxRows;
+  NV_CUDA(launch_gemm(epi, ta, tb, tbs, a, d->sms * kCtasPerSm, false, small_a, s), "grouped GEMM launch");
   return NVFP4_OK;
 }
 
@@ -504,7 +507,8 @@ static nvfp4_status gemm_dense(const char *fn, DeviceInfo *d, const uint8_t *xq,
   a.early_b = early_b;
   const int64_t tiles = G * ((M + kBlockM - 1) / kBlockM) * (N / kBlockN);
   const int grid = static_cast<int>(tiles < d->sms * kCtasPerSm ? tiles : d->sms * kCtasPerSm);
-  NV_CUDA(launch_gemm(Epi::kLinear, ta, tb, tb, a, grid, grid <= d->sms, s), "GEMM launch");
+  // M <= 32: every tile has at most one 32-row A box, so the ring with 4 small stages applies
+  NV_CUDA(launch_gemm(Epi::kLinear, ta, tb, tb, a, grid, grid <= d->sms, M <= kABoxRows, s), "GEMM launch");
   return NVFP4_OK;
 }
 

@@ -72,31 +72,33 @@ __device__ __forceinline__ float silu_mul(float g, float u) {
   return __fdividef(g, 1.0f + __expf(-g)) * u;
 }
 
-template <int kEpi>
+template <int kEpi, bool kSmallA>
 __global__ void __launch_bounds__(kGemmThreads, kCtasPerSm)
     nvfp4_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                       const __grid_constant__ CUtensorMap tmB,
                       const __grid_constant__ CUtensorMap tmBs, const GemmArgs args) {
+  constexpr int S = Ring<kSmallA>::kStagesR;    // stages in the ring
+  constexpr int kAB = Ring<kSmallA>::kABytes;    // A slot per stage
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   uint8_t *sA = smem;
-  uint8_t *sB = sA + kStages * kTileBytesA;
-  uint8_t *sSFA = sB + kStages * kTileBytesB;
-  uint8_t *sSFB = sSFA + kStages * kSfBytesStage;
-  uint64_t *full = reinterpret_cast<uint64_t *>(sSFB + kStages * kSfBytesStage);
-  uint64_t *empty = full + kStages;
-  uint64_t *tfull = empty + kStages;
+  uint8_t *sB = sA + S * kAB;
+  uint8_t *sSFA = sB + S * kTileBytesB;
+  uint8_t *sSFB = sSFA + S * kSfBytesStage;
+  uint64_t *full = reinterpret_cast<uint64_t *>(sSFB + S * kSfBytesStage);
+  uint64_t *empty = full + S;
+  uint64_t *tfull = empty + S;
   uint64_t *tempty = tfull + 2;
   uint64_t *sf_ready = tempty + 2;
-  uint64_t *drain = sf_ready + kStages;
+  uint64_t *drain = sf_ready + S;
   uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(drain + 1);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_holder + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kStages; ++s) {
+    for (int s = 0; s < S; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
       mbar_init(&sf_ready[s], 4);
@@ -162,7 +164,7 @@ __global__ void __launch_bounds__(kGemmThreads, kCtasPerSm)
           const uint8_t *sfb;
           b_src(t, mb, b_row0, sfb);
           const uint64_t pol_w = (t.mt > 0 || t.rows == kBlockM) ? pol_reuse : pol_stream;
-          early = min(kStages, k_stages);
+          early = min(S, k_stages);
           for (int s = 0; s < early; ++s) {
             const int kv = min(4, k_steps - 4 * s);
             mbar_expect_tx(&full[s], kTileBytesB + kv * kSfBytesPerKStep);
@@ -195,7 +197,11 @@ __global__ void __launch_bounds__(kGemmThreads, kCtasPerSm)
             args.a_sf + (static_cast<size_t>(t.a_row0 / kBlockM) * args.a_kc_total +
                          static_cast<size_t>(t.g) * args.a_group_koff) * kSfBytesPerKStep;
         const int a_x0 = t.g * args.a_group_koff * (kUmmaK / 2);  // A byte column of this group
-        const int nbox = (t.rows + kABoxRows - 1) / kABoxRows;
+        int nbox = (t.rows + kABoxRows - 1) / kABoxRows;
+        if (kSmallA && nbox > 1) {  // the launch promised at most one box per tile
+          raise_device_error(args.err, NVFP4_DEVERR_INTERNAL);
+          nbox = 1;
+        }
         for (int ks = 0; ks < k_stages; ++ks) {
           const int kv = min(4, k_steps - 4 * ks);
           if (!mbar_wait_bounded(&empty[stage], phase ^ 1, abort_flag, args.err,
@@ -207,7 +213,7 @@ __global__ void __launch_bounds__(kGemmThreads, kCtasPerSm)
           mbar_arrive_expect_tx(&full[stage],
                                 nbox * (kABoxRows * kStageK / 2) + kv * kSfBytesPerKStep +
                                     (b_done ? 0 : kTileBytesB + kv * kSfBytesPerKStep));
-          uint8_t *a_dst = sA + stage * kTileBytesA;
+          uint8_t *a_dst = sA + stage * kAB;
           for (int b = 0; b < nbox; ++b)
             tma_load_2d(a_dst + b * (kABoxRows * kStageK / 2), &tmA, a_x0 + ks * (kStageK / 2),
                         t.a_row0 + b * kABoxRows, &full[stage], pol_a);
@@ -221,7 +227,7 @@ __global__ void __launch_bounds__(kGemmThreads, kCtasPerSm)
           }
           ++n_issued;
           issued = (issued & ~(0x101u << stage)) | (1u << stage) | (phase << (stage + 8));
-          if (++stage == kStages) {
+          if (++stage == S) {
             stage = 0;
             phase ^= 1;
           }
@@ -231,7 +237,7 @@ __global__ void __launch_bounds__(kGemmThreads, kCtasPerSm)
         // let the copies already in flight land before the CTA leaves (this wait
         // ignores the abort flag; it is bounded by its own 100 ms limit)
         volatile int never = 0;
-        for (int s = 0; s < kStages; ++s)
+        for (int s = 0; s < S; ++s)
           if (issued & (1u << s))
             mbar_wait_bounded(&full[s], (issued >> (s + 8)) & 1u, &never, nullptr, 100000000ull);
       }
@@ -269,7 +275,7 @@ __global__ void __launch_bounds__(kGemmThreads, kCtasPerSm)
           }
           tc_fence_after();
           const uint32_t sf_col = tmem_base + kTmemAccCols + stage * kTmemSfCols;
-          const uint64_t adesc = smem_desc(sA0 + stage * kTileBytesA, 16, 1024, 2);
+          const uint64_t adesc = smem_desc(sA0 + stage * kAB, 16, 1024, 2);
           const uint64_t bdesc = smem_desc(sB0 + stage * kTileBytesB, 16, 1024, 2);
           for (int j = 0; j < kv; ++j) {
             // +32 bytes of K per step inside the 128-byte swizzle row (descriptor units of 16 B)
@@ -277,7 +283,7 @@ __global__ void __launch_bounds__(kGemmThreads, kCtasPerSm)
                         sf_col + 16 + j * 4, (ks | j) != 0);
           }
           tc_commit(&empty[stage]);
-          if (++stage == kStages) {
+          if (++stage == S) {
             stage = 0;
             phase ^= 1;
           }
@@ -349,7 +355,7 @@ __global__ void __launch_bounds__(kGemmThreads, kCtasPerSm)
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&sf_ready[sstage]);
-        if (++sstage == kStages) {
+        if (++sstage == S) {
           sstage = 0;
           sphase ^= 1;
         }
@@ -492,6 +498,7 @@ __global__ void __launch_bounds__(kGemmThreads, kCtasPerSm)
   __syncthreads();
   tc_fence_after();
   if (warp == 1) tmem_dealloc(tmem_base, kTmemCols);
+
 }
 
 // Bounded-wait probe: one thread waits on a barrier that never completes.
@@ -512,37 +519,45 @@ __global__ void wait_timeout_probe_kernel(uint64_t timeout_ns, uint32_t *err) {
   }
 }
 
-template <int kEpi>
+template <int kEpi, bool kSmallA>
 cudaError_t launch_gemm_t(const CUtensorMap &ta, const CUtensorMap &tb, const CUtensorMap &tbs,
                           const GemmArgs &args, int grid, bool one_per_sm, cudaStream_t s) {
+  using R = Ring<kSmallA>;
   static bool attr_done[64] = {false};
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 64 && !attr_done[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(nvfp4_gemm_kernel<kEpi>,
+    cudaError_t e = cudaFuncSetAttribute(nvfp4_gemm_kernel<kEpi, kSmallA>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(kGemmSmemBytesSolo));
+                                         static_cast<int>(R::kSmemSolo));
     if (e != cudaSuccess) return e;
     attr_done[dev] = true;
   }
   // A grid no larger than the SM count asks for enough shared memory to keep one CTA per
   // SM, so its tiles spread over as many SMs as there are tiles.
-  return launch_pdl(nvfp4_gemm_kernel<kEpi>, dim3(grid), dim3(kGemmThreads),
-                    one_per_sm ? kGemmSmemBytesSolo : kGemmSmemBytes, s, ta, tb, tbs, args);
+  return launch_pdl(nvfp4_gemm_kernel<kEpi, kSmallA>, dim3(grid), dim3(kGemmThreads),
+                    one_per_sm ? R::kSmemSolo : R::kSmem, s, ta, tb, tbs, args);
+}
+
+template <int kEpi>
+cudaError_t launch_gemm_e(const CUtensorMap &ta, const CUtensorMap &tb, const CUtensorMap &tbs,
+                          const GemmArgs &args, int grid, bool one_per_sm, bool small_a, cudaStream_t s) {
+  return small_a ? launch_gemm_t<kEpi, true>(ta, tb, tbs, args, grid, one_per_sm, s)
+                 : launch_gemm_t<kEpi, false>(ta, tb, tbs, args, grid, one_per_sm, s);
 }
 
 }  // namespace
 
 cudaError_t launch_gemm(Epi epi, const CUtensorMap &ta, const CUtensorMap &tb,
                         const CUtensorMap &tbs, const GemmArgs &args, int grid, bool one_per_sm,
-                        cudaStream_t s) {
+                        bool small_a, cudaStream_t s) {
   switch (epi) {
     case Epi::kLinear:
-      return launch_gemm_t<static_cast<int>(Epi::kLinear)>(ta, tb, tbs, args, grid, one_per_sm, s);
+      return launch_gemm_e<static_cast<int>(Epi::kLinear)>(ta, tb, tbs, args, grid, one_per_sm, small_a, s);
     case Epi::kW13:
-      return launch_gemm_t<static_cast<int>(Epi::kW13)>(ta, tb, tbs, args, grid, one_per_sm, s);
+      return launch_gemm_e<static_cast<int>(Epi::kW13)>(ta, tb, tbs, args, grid, one_per_sm, small_a, s);
     case Epi::kW2:
-      return launch_gemm_t<static_cast<int>(Epi::kW2)>(ta, tb, tbs, args, grid, one_per_sm, s);
+      return launch_gemm_e<static_cast<int>(Epi::kW2)>(ta, tb, tbs, args, grid, one_per_sm, small_a, s);
   }
   return cudaErrorInvalidValue;
 }

@@ -38,19 +38,31 @@ constexpr int kGemmThreads = 192;       // warp 0 TMA, warp 1 MMA, warps 2..5 ep
 constexpr uint32_t kTmemAccCols = kAccBufs * kBlockN;
 constexpr uint32_t kTmemSfCols = 32;                 // per stage: 16 SFA + 16 SFB columns
 constexpr uint32_t kTmemCols = 256;                  // per CTA: 128 accumulator + 96 scale columns
-static_assert(kTmemAccCols + kStages * kTmemSfCols <= kTmemCols, "TMEM budget");
 static_assert(kCtasPerSm * kTmemCols <= 512, "two CTAs share the SM's 512 TMEM columns");
 
 // full, empty, sf_ready per stage; two tfull/tempty; drain; TMEM address; abort flag
 constexpr size_t kGemmBarrierBytes = 256;
-static_assert((3 * kStages + 5) * 8 + 8 <= kGemmBarrierBytes, "barrier region");
-constexpr size_t kGemmSmemBytes =
-    1024 /* alignment slack */ +
-    static_cast<size_t>(kStages) * (kTileBytesA + kTileBytesB + 2 * kSfBytesStage) +
-    kGemmBarrierBytes;
-// Requested (not used) by launches that want one CTA per SM: two of these do not fit.
-constexpr size_t kGemmSmemBytesSolo = 2 * kGemmSmemBytes;
-static_assert(kGemmSmemBytesSolo <= 232448, "per-block shared memory limit");
+
+// The stage ring in shared memory.  The regular ring holds kStages stages with a
+// 128-row A slot.  When no tile can have more than 32 live rows (decode-sized MoE
+// calls, M <= 32), the A slot shrinks to one 32-row box and 4 stages fit in less
+// shared memory: a third more weight bytes in flight per CTA.
+template <bool kSmallA>
+struct Ring {
+  static constexpr int kStagesR = kSmallA ? 4 : kStages;
+  static constexpr int kABytes = kSmallA ? kABoxRows * kStageK / 2 : kTileBytesA;
+  static constexpr size_t kSmem = 1024 /* alignment slack */ +
+                                  static_cast<size_t>(kStagesR) *
+                                      (kABytes + kTileBytesB + 2 * kSfBytesStage) +
+                                  kGemmBarrierBytes;
+  // Requested (not used) by launches that want one CTA per SM: two of these do not fit.
+  static constexpr size_t kSmemSolo = 2 * kSmem;
+  static_assert(kTmemAccCols + kStagesR * kTmemSfCols <= kTmemCols, "TMEM budget");
+  static_assert((3 * kStagesR + 5) * 8 + 8 <= kGemmBarrierBytes, "barrier region");
+  static_assert(kSmemSolo <= 232448, "per-block shared memory limit");
+  static_assert(2 * (kSmem + 1024) <= 233472, "two CTAs per SM");
+  static_assert(kABytes % 1024 == 0, "128-byte swizzle atoms stay 1024-byte aligned");
+};
 
 enum class Epi : int { kLinear = 0, kW13 = 1, kW2 = 2 };
 
@@ -149,9 +161,11 @@ cudaError_t launch_dispatch_quant(const void *x, int T, int64_t H, int topk, int
                                   const uint32_t *partials, int nparts, const float *gs_static,
                                   float *gs_out, uint8_t *xq, uint8_t *xsf, cudaStream_t s);
 cudaError_t launch_finalize(const float *y_acc, int64_t n, void *y, cudaStream_t s);
+// small_a: every tile has at most kABoxRows live rows (the caller guarantees it; the
+// kernel raises NVFP4_DEVERR_INTERNAL otherwise).
 cudaError_t launch_gemm(Epi epi, const CUtensorMap &ta, const CUtensorMap &tb,
                         const CUtensorMap &tbs, const GemmArgs &args, int grid, bool one_per_sm,
-                        cudaStream_t s);
+                        bool small_a, cudaStream_t s);
 cudaError_t launch_wait_timeout_probe(uint32_t timeout_us, uint32_t *err, cudaStream_t s);
 
 }  // namespace nvfp4

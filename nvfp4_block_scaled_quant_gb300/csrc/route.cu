@@ -108,13 +108,9 @@ __device__ void block_scan3(const int *in_count, int n, int *out_off, int *out_p
 // its entries per expert, a scan over the warps (per expert, in warp order)
 // turns the counts into starting positions, and a second walk hands out
 // consecutive positions to equal experts in flat order.
-__global__ void __launch_bounds__(kRouteThreads) route_amax_kernel(
-    const int32_t *__restrict__ ids, int T, int topk, int E, int has_shared, RouteBufs rb,
-    const uint16_t *__restrict__ x, int64_t H, uint32_t *__restrict__ partials, int nparts,
-    float *__restrict__ y_acc, uint32_t *err) {
-  pdl_wait();
-  pdl_trigger();
-  if (blockIdx.x == 0) {
+__device__ void route_block(const int32_t *__restrict__ ids, int T, int topk, int E, int has_shared,
+                            RouteBufs rb, uint32_t *err) {
+  {
     extern __shared__ int route_smem[];
     int *s_cnt = route_smem;        // G = E (+1 shared) counts
     int *s_cursor = s_cnt + E + 1;  // next free sorted position per expert
@@ -229,6 +225,17 @@ __global__ void __launch_bounds__(kRouteThreads) route_amax_kernel(
       for (int j = 0; j < kRankPerWarp / 32; ++j) place32(w0 + 32 * j, my_e[j], my_cnt);
       __syncthreads();
     }
+  }
+}
+
+__global__ void __launch_bounds__(kRouteThreads) route_amax_kernel(
+    const int32_t *__restrict__ ids, int T, int topk, int E, int has_shared, RouteBufs rb,
+    const uint16_t *__restrict__ x, int64_t H, uint32_t *__restrict__ partials, int nparts,
+    float *__restrict__ y_acc, uint32_t *err) {
+  pdl_wait();
+  pdl_trigger();
+  if (blockIdx.x == 0) {
+    route_block(ids, T, topk, E, has_shared, rb, err);
     return;
   }
   // amax partials + zeroing
@@ -263,45 +270,39 @@ __global__ void __launch_bounds__(kRouteThreads) route_amax_kernel(
     y4[i] = make_float4(0.f, 0.f, 0.f, 0.f);
 }
 
-// One thread per 16-element block of x (T, H).  Every token is quantised once
-// and its codes and scales are written to its row in each routed expert's
-// segment (and the shared expert's segment).
-__global__ void __launch_bounds__(kDispatchThreads, 1) dispatch_quant_kernel(
-    const uint16_t *__restrict__ x, int T, int64_t H, int topk, int E, int has_shared,
-    const int32_t *__restrict__ ids, RouteBufs rb, const uint32_t *__restrict__ partials,
-    int nparts, const float *__restrict__ gs_static, float *__restrict__ gs_out,
-    uint8_t *__restrict__ xq, uint8_t *__restrict__ xsf) {
-  __shared__ uint32_t scratch[32];
-  pdl_wait();
-  pdl_trigger();
-  const int64_t kb = H / 16;
-  const int64_t gb = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-  const bool valid = gb < static_cast<int64_t>(T) * kb;
-  const int64_t t = valid ? gb / kb : 0;
-  const int64_t c = valid ? gb - t * kb : 0;
-  // The block's 16 elements and the token's destination rows are loaded first, so
-  // their latency overlaps the gs reduction.
-  uint4 a = make_uint4(0u, 0u, 0u, 0u), b = a;
+// One thread's share of the dispatch: the 16-element block c of token t, and the
+// token's destination rows (routed entries, -1 when dropped).
+struct DispatchIn {
+  uint4 a, b;
   int dest[kDestRegs];
-  const int *dest_src = rb.dest_rows + t * topk;
+};
+
+__device__ __forceinline__ void dispatch_load(const uint16_t *__restrict__ x, bool valid, int64_t t, int64_t c,
+                                              int64_t H, int topk, const RouteBufs &rb, DispatchIn &in) {
+  in.a = make_uint4(0u, 0u, 0u, 0u);
+  in.b = in.a;
   if (valid) {
     const uint4 *src = reinterpret_cast<const uint4 *>(x + t * H + c * 16);
-    a = __ldg(src);
-    b = __ldg(src + 1);
+    in.a = __ldg(src);
+    in.b = __ldg(src + 1);
   }
+  const int *dest_src = rb.dest_rows + t * topk;
 #pragma unroll
-  for (int j = 0; j < kDestRegs; ++j) dest[j] = (valid && j < topk && topk <= kDestRegs) ? __ldg(dest_src + j) : -1;
-  float gs;
-  if (partials) {
-    gs = gs_from_partials(partials, nparts, scratch);
-    if (blockIdx.x == 0 && threadIdx.x == 0) *gs_out = gs;
-  } else {
-    gs = *gs_static;
-  }
+  for (int j = 0; j < kDestRegs; ++j)
+    in.dest[j] = (valid && j < topk && topk <= kDestRegs) ? __ldg(dest_src + j) : -1;
+}
+
+// Encode the block with gs and write its codes and scale word into every destination
+// row (the routed rows, then the shared segment).  Every lane of the warp calls this:
+// the four scale bytes of a 64-element group are gathered with shuffles.
+__device__ __forceinline__ void dispatch_store(const DispatchIn &in, bool valid, int64_t t, int64_t c, int64_t H,
+                                               int topk, int E, int has_shared, const RouteBufs &rb, float gs,
+                                               uint8_t *__restrict__ xq, uint8_t *__restrict__ xsf) {
+  const int64_t kb = H / 16;
   const float six_gs = __fmul_rn(6.0f, gs);
   uint32_t codes[2] = {0u, 0u}, sfb = 0;
   if (valid) {
-    const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+    const uint32_t w[8] = {in.a.x, in.a.y, in.a.z, in.a.w, in.b.x, in.b.y, in.b.z, in.b.w};
     float v[16];
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
@@ -321,19 +322,48 @@ __global__ void __launch_bounds__(kDispatchThreads, 1) dispatch_quant_kernel(
     *reinterpret_cast<uint2 *>(xq + p * (H / 2) + c * 8) = cv;
     if (sf_writer) *reinterpret_cast<uint32_t *>(xsf + sf_word_offset(p, c >> 2, kb >> 2)) = word;
   };
-  // destination rows: routed entries from the routing kernel (dropped entries are -1),
-  // then the shared segment
   if (topk <= kDestRegs) {
 #pragma unroll
     for (int j = 0; j < kDestRegs; ++j)
-      if (dest[j] >= 0) put(dest[j]);
+      if (in.dest[j] >= 0) put(in.dest[j]);
   } else {
+    const int *dest_src = rb.dest_rows + t * topk;
     for (int j = 0; j < topk; ++j) {
       const int p = __ldg(dest_src + j);
       if (p >= 0) put(p);
     }
   }
   if (has_shared) put(static_cast<int64_t>(__ldg(rb.pad_offsets + E)) + t);
+}
+
+// One thread per 16-element block of x (T, H).  Every token is quantised once
+// and its codes and scales are written to its row in each routed expert's
+// segment (and the shared expert's segment).
+__global__ void __launch_bounds__(kDispatchThreads, 1) dispatch_quant_kernel(
+    const uint16_t *__restrict__ x, int T, int64_t H, int topk, int E, int has_shared,
+    const int32_t *__restrict__ ids, RouteBufs rb, const uint32_t *__restrict__ partials,
+    int nparts, const float *__restrict__ gs_static, float *__restrict__ gs_out,
+    uint8_t *__restrict__ xq, uint8_t *__restrict__ xsf) {
+  __shared__ uint32_t scratch[32];
+  pdl_wait();
+  pdl_trigger();
+  const int64_t kb = H / 16;
+  const int64_t gb = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const bool valid = gb < static_cast<int64_t>(T) * kb;
+  const int64_t t = valid ? gb / kb : 0;
+  const int64_t c = valid ? gb - t * kb : 0;
+  // The block's 16 elements and the token's destination rows are loaded first, so
+  // their latency overlaps the gs reduction.
+  DispatchIn in;
+  dispatch_load(x, valid, t, c, H, topk, rb, in);
+  float gs;
+  if (partials) {
+    gs = gs_from_partials(partials, nparts, scratch);
+    if (blockIdx.x == 0 && threadIdx.x == 0) *gs_out = gs;
+  } else {
+    gs = *gs_static;
+  }
+  dispatch_store(in, valid, t, c, H, topk, E, has_shared, rb, gs, xq, xsf);
 }
 
 __global__ void finalize_kernel(const float4 *__restrict__ acc, int64_t n4, uint2 *__restrict__ y) {

@@ -171,6 +171,45 @@ def test_moe_tiny_duplicates_and_skew():
     run_moe_check(x, ids, w, W, oe, list(range(0, T, 7)), True)
 
 
+@pytest.mark.parametrize("T", [1, 2, 3, 4, 5])
+def test_moe_small_batches_all_tokens(T):
+    """Decode-sized calls, all tokens: T*k <= 32 takes the GEMM ring with 4 small A stages (one
+    32-row box per tile); T = 5 (T*k = 40) the regular one."""
+    cfg = workloads.MoEConfig("small", T, 256, 128, 16, 8, True, "softmax", False)
+    base = 109
+    W = model.make_moe_weights(cfg.E, cfg.H, cfg.I, base, DEV, shared=True)
+    oe = oracle_expert_fn(base, cfg.H, cfg.I, DEV)
+    x = workloads.activations(T, cfg.H, seed=110 + T, device="cpu")
+    ids, w = workloads.routing(cfg, seed=120 + T, device="cpu")
+    run_moe_check(x, ids, w, W, oe, list(range(T)), True)
+
+
+@pytest.mark.parametrize("T", [2, 9])
+def test_moe_dispatch_static_gs(T):
+    """Static a1 scale: every routed and shared row holds the oracle's codes."""
+    H, I, E, k = 256, 128, 8, 2
+    W = model.make_moe_weights(E, H, I, 111, DEV, shared=True)
+    x = workloads.activations(T, H, seed=112, device="cpu")
+    ids = torch.from_numpy(np.random.default_rng(T).integers(0, E, (T, k)).astype(np.int32))
+    L = ops.moe_workspace_layout(T, H, I, E, k, True)
+    ws = torch.empty(L.total, dtype=torch.uint8, device=DEV)
+    gs = 0.003
+    ops.moe_dispatch(x.to(DEV), ids.to(DEV), W, torch.tensor([gs], dtype=torch.float32, device=DEV), False, ws)
+    torch.cuda.synchronize()
+    assert ops.device_error() == (0, 0)
+    ref = O.quantize(x.float().numpy(), gs=F32(gs))
+    rc = L.rows_capacity
+    xq = O.unpack_codes(_region(ws, L.xq, rc * H // 2, torch.uint8).view(rc, H // 2).cpu().numpy())
+    xsf = _region(ws, L.xsf, O.sf_bytes(rc, H), torch.uint8).cpu().numpy()
+    off = O.sf_swizzle_offsets(rc, H)
+    dest = _region(ws, L.dest_rows, T * k, torch.int32).cpu().numpy().reshape(T, k)
+    pad = _region(ws, L.pad_offsets, E + 2, torch.int32).cpu().numpy()
+    for t in range(T):
+        for p in list(dest[t]) + [pad[E] + t]:
+            np.testing.assert_array_equal(xq[p], ref.codes[t])
+            np.testing.assert_array_equal(xsf[off[p, : H // 16]], ref.sf[t])
+
+
 def test_moe_empty_batch():
     W = model.make_moe_weights(4, 256, 128, 106, DEV, shared=True)
     y, g = ops.moe_forward(torch.empty(0, 256, dtype=torch.bfloat16, device=DEV),
