@@ -483,11 +483,9 @@ __global__ void __launch_bounds__(kGemmThreads, kCtasPerSm)
             for (int q = 0; q < 4; ++q)
 #pragma unroll
               for (int i = 0; i < 4; ++i)
-                atomicAdd(dst + h * 16 + q * 4 + i,
-                          make_float4(__uint_as_float(r[q][4 * i]) * scale,
-                                      __uint_as_float(r[q][4 * i + 1]) * scale,
-                                      __uint_as_float(r[q][4 * i + 2]) * scale,
-                                      __uint_as_float(r[q][4 * i + 3]) * scale));
+                red_add_v4(dst + h * 16 + q * 4 + i, __uint_as_float(r[q][4 * i]) * scale,
+                           __uint_as_float(r[q][4 * i + 1]) * scale, __uint_as_float(r[q][4 * i + 2]) * scale,
+                           __uint_as_float(r[q][4 * i + 3]) * scale);
           }
         }
       }
