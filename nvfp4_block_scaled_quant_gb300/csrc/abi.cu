@@ -382,10 +382,8 @@ nvfp4_status nvfp4_quantize_act(const void *x, int64_t M, int64_t K, int64_t ldx
   nvfp4_status st = device_info(__func__, &d);
   if (st != NVFP4_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  const int nparts = amax_partial_count(M, K);
   uint32_t *partials = dyn ? static_cast<uint32_t *>(ws) : nullptr;
-  if (dyn) NV_CUDA(launch_amax_partials(x, M, K, ldx, partials, nparts, s), "amax kernel launch");
-  NV_CUDA(launch_quantize(x, M, K, ldx, partials, nparts, gs, gs, q, sf, sf_layout, s), "quantize kernel launch");
+  NV_CUDA(launch_act_quant(x, M, K, ldx, dyn, partials, gs, gs, q, sf, sf_layout, s), "quantize kernel launch");
   return NVFP4_OK;
 }
 
@@ -550,11 +548,8 @@ nvfp4_status nvfp4_linear(const void *x, int64_t M, int64_t K, int64_t N, const 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   uint8_t *xq = at<uint8_t>(ws, L.xq), *xsf = at<uint8_t>(ws, L.xsf);
   const bool dyn = gs_mode == NVFP4_GS_DYNAMIC;
-  const int nparts = amax_partial_count(M, K);
   uint32_t *partials = dyn ? at<uint32_t>(ws, L.partials) : nullptr;
-  if (dyn) NV_CUDA(launch_amax_partials(x, M, K, K, partials, nparts, s), "amax kernel launch");
-  NV_CUDA(launch_quantize(x, M, K, K, partials, nparts, gs, gs, xq, xsf, NVFP4_SF_SWIZZLED, s),
-          "quantize kernel launch");
+  NV_CUDA(launch_act_quant(x, M, K, K, dyn, partials, gs, gs, xq, xsf, NVFP4_SF_SWIZZLED, s), "quantize kernel launch");
   // the quantise launch just before this GEMM runs after everything that wrote W
   return gemm_dense(__func__, d, xq, xsf, gs, M, K, N, w, w_sf, ws2, y, s, 1);
 }
@@ -608,11 +603,8 @@ nvfp4_status nvfp4_linear_noalloc(const void *x, int64_t M, int64_t K, int64_t N
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   uint8_t *xq = at<uint8_t>(scratch, L.xq), *xsf = at<uint8_t>(scratch, L.xsf);
   const bool dyn = gs_mode == NVFP4_GS_DYNAMIC;
-  const int nparts = amax_partial_count(M, K);
   uint32_t *partials = dyn ? at<uint32_t>(scratch, L.partials) : nullptr;
-  if (dyn) NV_CUDA(launch_amax_partials(x, M, K, K, partials, nparts, s), "amax kernel launch");
-  NV_CUDA(launch_quantize(x, M, K, K, partials, nparts, gs, gs, xq, xsf, NVFP4_SF_SWIZZLED, s),
-          "quantize kernel launch");
+  NV_CUDA(launch_act_quant(x, M, K, K, dyn, partials, gs, gs, xq, xsf, NVFP4_SF_SWIZZLED, s), "quantize kernel launch");
   // the quantise launch just before this GEMM runs after everything that wrote W
   return gemm_dense(__func__, d, xq, xsf, gs, M, K, N, w, w_sf, ws2, y, s, 1);
 }
@@ -642,10 +634,8 @@ nvfp4_status nvfp4_grouped_linear(const void *x, int64_t M, int64_t G, int64_t K
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   uint8_t *xq = at<uint8_t>(ws, L.xq), *xsf = at<uint8_t>(ws, L.xsf);
   const bool dyn = gs_mode == NVFP4_GS_DYNAMIC;
-  const int nparts = amax_partial_count(M, G * K);
   uint32_t *partials = dyn ? at<uint32_t>(ws, L.partials) : nullptr;
-  if (dyn) NV_CUDA(launch_amax_partials(x, M, G * K, G * K, partials, nparts, s), "amax kernel launch");
-  NV_CUDA(launch_quantize(x, M, G * K, G * K, partials, nparts, gs, gs, xq, xsf, NVFP4_SF_SWIZZLED, s),
+  NV_CUDA(launch_act_quant(x, M, G * K, G * K, dyn, partials, gs, gs, xq, xsf, NVFP4_SF_SWIZZLED, s),
           "quantize kernel launch");
   return gemm_dense(__func__, d, xq, xsf, gs, M, K, N, w, w_sf, ws2, y, s, 1, G);
 }

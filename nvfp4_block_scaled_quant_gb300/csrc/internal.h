@@ -135,6 +135,13 @@ cudaError_t launch_quantize(const void *x, int64_t M, int64_t K, int64_t ldx,
                             const uint32_t *partials, int nparts, const float *gs_static,
                             float *gs_out, uint8_t *q, uint8_t *sf, int sf_layout,
                             cudaStream_t s);
+// Activation quantisation with a dynamic (amax/2688) or static gs.  Dynamic inputs of at most
+// kInlineAmaxElems elements take one launch (each quantise block reduces x itself); larger ones
+// an amax-partials launch first (partials: amax_partial_count(M, K) words of workspace).
+constexpr int64_t kInlineAmaxElems = 32768;
+cudaError_t launch_act_quant(const void *x, int64_t M, int64_t K, int64_t ldx, bool dynamic, uint32_t *partials,
+                             const float *gs_static, float *gs_out, uint8_t *q, uint8_t *sf, int sf_layout,
+                             cudaStream_t s);
 cudaError_t launch_rmsnorm_stats(const void *x, int64_t M, int64_t K, int64_t ldx, const void *gamma, float eps,
                                  float *inv_rms, uint32_t *partials, int nparts, void *y, cudaStream_t s);
 cudaError_t launch_rmsnorm_quantize(const void *x, int64_t M, int64_t K, int64_t ldx, const void *gamma,

@@ -80,8 +80,26 @@ __global__ void __launch_bounds__(kQuantThreads) quantize_kernel(
     a = __ldg(src);
     b = __ldg(src + 1);
   }
-  float gs;
-  if (partials) {
+  float gs = 0.f;
+  if (nparts == 0) {
+    // Small input: every block with live rows reduces the whole of x itself (one launch
+    // fewer); blocks of padding rows only write zero scales and need no gs.  Block 0
+    // always reduces, so gs_out is written (0 when M == 0).  The condition is uniform
+    // over the block, so the reduction's barriers are safe.
+    if (blockIdx.x == 0 || static_cast<int64_t>(blockIdx.x) * blockDim.x / kb < M) {
+      uint32_t m = 0;
+      const int64_t chunks = K / 8;
+      for (int64_t i = threadIdx.x; i < M * chunks; i += blockDim.x) {
+        const int64_t rr = i / chunks;
+        const uint4 v = __ldg(reinterpret_cast<const uint4 *>(x + rr * ldx) + (i - rr * chunks));
+        m = max(m, max(max(max_abs_bf16x2(v.x), max_abs_bf16x2(v.y)),
+                       max(max_abs_bf16x2(v.z), max_abs_bf16x2(v.w))));
+      }
+      m = block_reduce_max(m, scratch);
+      gs = __fdiv_rn(__uint_as_float(m << 16), 2688.0f);
+      if (blockIdx.x == 0 && threadIdx.x == 0) *gs_out = gs;
+    }
+  } else if (partials) {
     gs = gs_from_partials(partials, nparts, scratch);
     if (blockIdx.x == 0 && threadIdx.x == 0) *gs_out = gs;
   } else {
@@ -178,6 +196,18 @@ cudaError_t launch_quantize(const void *x, int64_t M, int64_t K, int64_t ldx,
   return launch_pdl(quantize_kernel, dim3(static_cast<unsigned>(blocks)), dim3(kQuantThreads), 0, s,
                     static_cast<const uint16_t *>(x), M, K, ldx, partials, nparts, gs_static, gs_out, q, sf,
                     sf_layout, rows_total);
+}
+
+cudaError_t launch_act_quant(const void *x, int64_t M, int64_t K, int64_t ldx, bool dynamic, uint32_t *partials,
+                             const float *gs_static, float *gs_out, uint8_t *q, uint8_t *sf, int sf_layout,
+                             cudaStream_t s) {
+  if (!dynamic) return launch_quantize(x, M, K, ldx, nullptr, 1, gs_static, gs_out, q, sf, sf_layout, s);
+  if (M * K <= kInlineAmaxElems)  // nparts = 0: the quantise blocks reduce x themselves
+    return launch_quantize(x, M, K, ldx, nullptr, 0, gs_static, gs_out, q, sf, sf_layout, s);
+  const int nparts = amax_partial_count(M, K);
+  const cudaError_t e = launch_amax_partials(x, M, K, ldx, partials, nparts, s);
+  if (e != cudaSuccess) return e;
+  return launch_quantize(x, M, K, ldx, partials, nparts, gs_static, gs_out, q, sf, sf_layout, s);
 }
 
 cudaError_t launch_prepare(const uint8_t *w, const uint8_t *sf, int64_t G, int64_t N, int64_t K,
