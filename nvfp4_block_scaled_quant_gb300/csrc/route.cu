@@ -11,9 +11,10 @@ constexpr int kRouteThreads = 512;
 constexpr int kDispatchThreads = 256;
 constexpr int kDestRegs = 8;  // destination rows held in registers (top-k up to 8)
 constexpr int kRankWarps = kRouteThreads / 32;
-constexpr int kRankPerWarp = 128;                      // entries per warp and chunk
+constexpr int kRankPerWarp = 256;                      // entries per warp and chunk
 constexpr int kRankChunk = kRankWarps * kRankPerWarp;  // entries ranked per pass
 constexpr int kSmallRank = 256;                        // up to this many entries one warp ranks
+constexpr int kHistUnroll = 8;                         // id loads in flight per histogram step
 
 // dynamic shared memory of the routing block (counts, cursors, deltas, scan scratch,
 // per-warp counts)
@@ -125,19 +126,26 @@ __device__ void route_block(const int32_t *__restrict__ ids, int T, int topk, in
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     for (int g = threadIdx.x; g < G; g += blockDim.x) s_cnt[g] = 0;
     __syncthreads();
-    // histogram: one shared-memory atomic per distinct expert of each 32 entries
-    for (int f0 = warp * 32; f0 < Tk; f0 += blockDim.x) {
-      const int f = f0 + lane;
-      int e = -1;
-      if (f < Tk) {
-        e = __ldg(ids + f);
-        if (e < 0 || e >= E) {
+    // histogram: one shared-memory atomic per distinct expert of each 32 entries; each
+    // warp has kHistUnroll loads in flight before it uses the first
+    for (int f0 = warp * 32; f0 < Tk; f0 += blockDim.x * kHistUnroll) {
+      int ev[kHistUnroll];
+#pragma unroll
+      for (int u = 0; u < kHistUnroll; ++u) {
+        const int f = f0 + u * blockDim.x + lane;
+        ev[u] = f < Tk ? __ldg(ids + f) : -1;
+      }
+#pragma unroll
+      for (int u = 0; u < kHistUnroll; ++u) {
+        const int f = f0 + u * blockDim.x + lane;
+        int e = ev[u];
+        if (f < Tk && (e < 0 || e >= E)) {
           raise_device_error(err, NVFP4_DEVERR_BAD_EXPERT_ID);
           e = -1;
         }
+        const unsigned peers = __match_any_sync(0xffffffffu, e);
+        if (e >= 0 && lane == __ffs(peers) - 1) atomicAdd(&s_cnt[e], __popc(peers));
       }
-      const unsigned peers = __match_any_sync(0xffffffffu, e);
-      if (e >= 0 && lane == __ffs(peers) - 1) atomicAdd(&s_cnt[e], __popc(peers));
     }
     if (has_shared && threadIdx.x == 0) s_cnt[E] = T;
     __syncthreads();
