@@ -346,6 +346,33 @@ def run_secondary(state, args):
         e.synchronize()
         return s.elapsed_time(e) / iters
 
+    cap = torch.cuda.Stream(dev)
+
+    def graph_time_fn(body, calls, reps):
+        """Device time per call from CUDA-graph replay: body(stream) enqueues `calls` calls;
+        the graph of one body is replayed `reps` times between two events."""
+        cap.wait_stream(stream)
+        with torch.cuda.stream(cap):
+            body(cap)  # warm-up outside the capture (per-device set-up, kernel attributes)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=cap):
+            body(cap)
+        with torch.cuda.stream(cap):
+            for _ in range(2):
+                g.replay()
+        torch.cuda.synchronize()
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(cap):  # replay() launches on the current stream
+            s.record(cap)
+            for _ in range(reps):
+                g.replay()
+            e.record(cap)
+        e.synchronize()
+        stream.wait_stream(cap)
+        del g
+        return s.elapsed_time(e) / (reps * calls)
+
     for T in (1, 8, 64):
         cfg = workloads.DECODE[T]
         steps = [workloads.decode_step(T, step=i, device="cpu") for i in range(16)]
@@ -360,12 +387,18 @@ def run_secondary(state, args):
             it[0] += 1
             ops.moe_forward(x, i, w, W, a2, workspace=ws, out=y)
 
-        ms = time_fn(fwd, 64)
+        def fwd16(st):
+            for x, i, w in dev_steps:
+                ops.moe_forward(x, i, w, W, a2, workspace=ws, out=y, stream=st)
+
+        eager_ms = time_fn(fwd, 64)
+        ms = graph_time_fn(fwd16, 16, 8)
         b = sum(a["step_bytes"] for a in acct) / 16
         out.append({"workload": cfg.name, "tokens_per_s": T / (ms / 1e3), "ms_per_step": ms,
                     "hbm_gbs": b / (ms / 1e3) / 1e9, "hbm_frac": b / (ms / 1e3) / 1e9 / hbm,
-                    "groups_mean": sum(a["groups"] for a in acct) / 16,
-                    "note": "16 seeded routings cycled; weights streamed from HBM (> L2)"})
+                    "eager_ms_per_step": eager_ms, "groups_mean": sum(a["groups"] for a in acct) / 16,
+                    "note": "16 seeded routings cycled, replayed as one CUDA graph (eager_ms_per_step: plain calls); "
+                            "weights streamed from HBM (> L2)"})
     # whole prefill in one call: the 32 chunks' 4096 tokens at once (hot experts span many m tiles)
     cfg = workloads.PREFILL_WHOLE
     x, ids, w = workloads.prefill_whole(device="cpu")
@@ -391,18 +424,25 @@ def run_secondary(state, args):
         gs = torch.empty(1, dtype=torch.float32, device=dev)
         it = [0]
 
-        def lin():
-            d = dws[it[0] % 16]
-            it[0] += 1
+        def lin(st=stream, d=None):
+            if d is None:
+                d = dws[it[0] % 16]
+                it[0] += 1
             ops.call("nvfp4_linear", x.data_ptr(), M, K, N, d.w.data_ptr(), d.sf.data_ptr(), d.ws2.data_ptr(), 0,
-                     gs.data_ptr(), y.data_ptr(), wsl.data_ptr(), wsl.numel(), stream.cuda_stream)
+                     gs.data_ptr(), y.data_ptr(), wsl.data_ptr(), wsl.numel(), st.cuda_stream)
 
-        ms = time_fn(lin, 160)
+        def lin16(st):
+            for d in dws:
+                lin(st, d)
+
+        eager_ms = time_fn(lin, 160)
+        ms = graph_time_fn(lin16, 16, 10)
         b = N * K * (0.5 + 1 / 16) + M * K * 2 + M * N * 2
         out.append({"workload": f"dense_linear_M{M}_K{K}_N{N}", "us_per_call": ms * 1e3,
                     "hbm_gbs": b / (ms / 1e3) / 1e9, "hbm_frac": b / (ms / 1e3) / 1e9 / hbm,
-                    "tflops": 2 * M * N * K / (ms / 1e3) / 1e12,
-                    "note": "quantise + GEMM; 16 weight copies rotated (230 MB > L2)"})
+                    "tflops": 2 * M * N * K / (ms / 1e3) / 1e12, "eager_us_per_call": eager_ms * 1e3,
+                    "note": "quantise + GEMM; 16 weight copies rotated (230 MB > L2), replayed as one CUDA graph "
+                            "(eager_us_per_call: plain calls, bounded by the host)"})
     del dws
     # fixed-group linear (grouped o-projection): 8 x (4096 -> 1024); 16 weight copies rotated (> L2)
     for M in sorted(workloads.GROUPED_LINEAR):
@@ -414,18 +454,25 @@ def run_secondary(state, args):
         gs = torch.empty(1, dtype=torch.float32, device=dev)
         it = [0]
 
-        def grp():
-            d = gws[it[0] % 16]
-            it[0] += 1
+        def grp(st=stream, d=None):
+            if d is None:
+                d = gws[it[0] % 16]
+                it[0] += 1
             ops.call("nvfp4_grouped_linear", x.data_ptr(), M, G, K, N, d.w.data_ptr(), d.sf.data_ptr(),
-                     d.ws2.data_ptr(), 0, gs.data_ptr(), y.data_ptr(), wsg.data_ptr(), wsg.numel(), stream.cuda_stream)
+                     d.ws2.data_ptr(), 0, gs.data_ptr(), y.data_ptr(), wsg.data_ptr(), wsg.numel(), st.cuda_stream)
 
-        ms = time_fn(grp, 160)
+        def grp16(st):
+            for d in gws:
+                grp(st, d)
+
+        eager_ms = time_fn(grp, 160)
+        ms = graph_time_fn(grp16, 16, 10)
         b = G * N * K * (0.5 + 1 / 16) + M * G * K * 2 + M * G * N * 2
         out.append({"workload": f"grouped_linear_M{M}_G{G}_K{K}_N{N}", "us_per_call": ms * 1e3,
                     "hbm_gbs": b / (ms / 1e3) / 1e9, "hbm_frac": b / (ms / 1e3) / 1e9 / hbm,
-                    "tflops": 2 * M * G * N * K / (ms / 1e3) / 1e12,
-                    "note": "quantise + grouped GEMM; 16 weight copies rotated (300 MB > L2)"})
+                    "tflops": 2 * M * G * N * K / (ms / 1e3) / 1e12, "eager_us_per_call": eager_ms * 1e3,
+                    "note": "quantise + grouped GEMM; 16 weight copies rotated (300 MB > L2), replayed as one CUDA "
+                            "graph (eager_us_per_call: plain calls, bounded by the host)"})
         del gws
     K = N = 7168
     dw = model.make_dense_weight(N, K, seed=70, device=dev)
