@@ -510,6 +510,43 @@ static nvfp4_status gemm_dense(const char *fn, DeviceInfo *d, const uint8_t *xq,
   return NVFP4_OK;
 }
 
+// Dense linear for 1 <= M <= 32 rows, K <= kQuantMaxK and M*K <= kQuantMaxElems in one
+// launch: the GEMM CTAs quantise x themselves (same arithmetic as nvfp4_quantize_act)
+// into resident A boxes.
+static nvfp4_status linear_fused(const char *fn, DeviceInfo *d, const void *x, int64_t M, int64_t K, int64_t N,
+                                 const uint8_t *w, const uint8_t *w_sf, const float *ws2, bool dyn, float *gs,
+                                 void *y, cudaStream_t s) {
+  CUtensorMap tb;
+  nvfp4_status st = make_map(fn, &tb, w, K / 2, N, K / 2, kBlockN);
+  if (st != NVFP4_OK) return st;
+  GemmArgs a;
+  std::memset(&a, 0, sizeof(a));
+  a.G = 1;
+  a.N = static_cast<int>(N);
+  a.K = static_cast<int>(K);
+  a.dense_M = static_cast<int>(M);
+  a.shared_group = -1;
+  a.b_sf = w_sf;
+  a.ws2 = ws2;
+  a.out = y;
+  a.out_ld = static_cast<int>(N);
+  a.out_group_cols = static_cast<int>(N);
+  a.err = d->flags;
+  a.early_b = 0;  // the launch just before this one may have written W
+  a.qa_x = x;
+  a.qa_ld = K;
+  a.qa_gs_static = dyn ? nullptr : gs;
+  a.qa_gs_out = dyn ? gs : nullptr;
+  const int64_t tiles = N / kBlockN;
+  const int grid = static_cast<int>(tiles < d->sms ? tiles : d->sms);
+  NV_CUDA(launch_gemm_quant_a(tb, a, grid, s), "fused linear launch");
+  return NVFP4_OK;
+}
+
+static bool linear_fusable(int64_t M, int64_t K) {
+  return M >= 1 && M <= kABoxRows && K <= kQuantMaxK && M * K <= kQuantMaxElems;
+}
+
 #define NV_CHECK_GEMM_SHAPE(M, K, N)                                                                          \
   NV_REQUIRE((M) >= 0 && (K) > 0 && (N) > 0, NVFP4_ERR_INVALID_ARG, "M=%lld K=%lld N=%lld", (long long)(M),    \
              (long long)(K), (long long)(N));                                                                  \
@@ -546,8 +583,9 @@ nvfp4_status nvfp4_linear(const void *x, int64_t M, int64_t K, int64_t N, const 
   DeviceInfo *d;
   if ((st = device_info(__func__, &d)) != NVFP4_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  uint8_t *xq = at<uint8_t>(ws, L.xq), *xsf = at<uint8_t>(ws, L.xsf);
   const bool dyn = gs_mode == NVFP4_GS_DYNAMIC;
+  if (linear_fusable(M, K)) return linear_fused(__func__, d, x, M, K, N, w, w_sf, ws2, dyn, gs, y, s);
+  uint8_t *xq = at<uint8_t>(ws, L.xq), *xsf = at<uint8_t>(ws, L.xsf);
   uint32_t *partials = dyn ? at<uint32_t>(ws, L.partials) : nullptr;
   NV_CUDA(launch_act_quant(x, M, K, K, dyn, partials, gs, gs, xq, xsf, NVFP4_SF_SWIZZLED, s), "quantize kernel launch");
   // the quantise launch just before this GEMM runs after everything that wrote W
@@ -601,8 +639,9 @@ nvfp4_status nvfp4_linear_noalloc(const void *x, int64_t M, int64_t K, int64_t N
   void *scratch = nullptr;
   if ((st = noalloc_scratch(__func__, &scratch)) != NVFP4_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  uint8_t *xq = at<uint8_t>(scratch, L.xq), *xsf = at<uint8_t>(scratch, L.xsf);
   const bool dyn = gs_mode == NVFP4_GS_DYNAMIC;
+  if (linear_fusable(M, K)) return linear_fused(__func__, d, x, M, K, N, w, w_sf, ws2, dyn, gs, y, s);
+  uint8_t *xq = at<uint8_t>(scratch, L.xq), *xsf = at<uint8_t>(scratch, L.xsf);
   uint32_t *partials = dyn ? at<uint32_t>(scratch, L.partials) : nullptr;
   NV_CUDA(launch_act_quant(x, M, K, K, dyn, partials, gs, gs, xq, xsf, NVFP4_SF_SWIZZLED, s), "quantize kernel launch");
   // the quantise launch just before this GEMM runs after everything that wrote W

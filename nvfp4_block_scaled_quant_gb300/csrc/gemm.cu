@@ -72,20 +72,91 @@ __device__ __forceinline__ float silu_mul(float g, float u) {
   return __fdividef(g, 1.0f + __expf(-g)) * u;
 }
 
-template <int kEpi, bool kSmallA>
-__global__ void __launch_bounds__(kGemmThreads, kCtasPerSm)
+__device__ __forceinline__ void named_barrier_sync(int id, int threads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
+
+// Fused activation quantisation (dense linear, dense_M <= 32 rows): the four epilogue
+// warps (tid 0..127, named barrier 1) take gs = fl32(amax / 2688) over x (or the static
+// scale), then encode every 16-element block with the activation quantiser's arithmetic
+// into the resident A boxes (one 32-row, 128-byte-swizzled 4 KB box per 256-element K
+// stage: 16-byte chunk c of row r sits at chunk c ^ (r & 7)) and their scale blocks
+// (row r's four scales of a 64-element K step at 16 r in that step's 512-byte block).
+// CTA 0 writes gs out; every CTA returns the same gs.
+__device__ float quantize_resident_a(const GemmArgs &a, uint8_t *sA, uint8_t *sSFA, uint32_t *scratch, int tid) {
+  const int64_t M = a.dense_M, K = a.K, ld = a.qa_ld;
+  const uint16_t *x = static_cast<const uint16_t *>(a.qa_x);
+  const int warp = tid >> 5, lane = tid & 31;
+  float gs;
+  if (a.qa_gs_static == nullptr) {
+    uint32_t m = 0;
+    const int64_t chunks = K / 8, n = M * chunks;
+    for (int64_t i0 = tid; i0 < n; i0 += 4 * 128) {  // four 16-byte loads in flight per thread
+      uint4 v[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int64_t i = i0 + u * 128, r = i / chunks;
+        v[u] = i < n ? __ldg(reinterpret_cast<const uint4 *>(x + r * ld) + (i - r * chunks)) : make_uint4(0, 0, 0, 0);
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const uint32_t w[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) m = max(m, max(w[k] & 0x7FFFu, (w[k] >> 16) & 0x7FFFu));
+      }
+    }
+#pragma unroll
+    for (int o = 16; o; o >>= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, o));
+    if (lane == 0) scratch[warp] = m;
+    named_barrier_sync(1, 128);
+    m = max(max(scratch[0], scratch[1]), max(scratch[2], scratch[3]));
+    gs = __fdiv_rn(__uint_as_float(m << 16), 2688.0f);
+  } else {
+    gs = __ldg(a.qa_gs_static);
+  }
+  if (blockIdx.x == 0 && tid == 0 && a.qa_gs_out != nullptr) *a.qa_gs_out = gs;
+  const float six_gs = __fmul_rn(6.0f, gs);
+  const int64_t kb = K / 16;
+#pragma unroll 2
+  for (int64_t i = tid; i < M * kb; i += 128) {
+    const int64_t r = i / kb, c = i - r * kb;  // row, 16-element block
+    const uint4 *src = reinterpret_cast<const uint4 *>(x + r * ld + c * 16);
+    const uint4 p = __ldg(src), q = __ldg(src + 1);
+    const uint32_t w[8] = {p.x, p.y, p.z, p.w, q.x, q.y, q.z, q.w};
+    float v[16];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      v[2 * k] = __uint_as_float(w[k] << 16);
+      v[2 * k + 1] = __uint_as_float(w[k] & 0xFFFF0000u);
+    }
+    uint32_t codes[2];
+    const uint32_t sfb = encode_block16(v, gs, six_gs, codes);
+    const int st = static_cast<int>(c >> 4), j = static_cast<int>(c & 15), rr = static_cast<int>(r);
+    const int chunk = (j >> 1) ^ (rr & 7);
+    *reinterpret_cast<uint2 *>(sA + st * (kABoxRows * kStageK / 2) + rr * 128 + chunk * 16 + (j & 1) * 8) =
+        make_uint2(codes[0], codes[1]);
+    sSFA[st * kSfBytesStage + ((j >> 2) & 3) * kSfBytesPerKStep + rr * 16 + (j & 3)] = static_cast<uint8_t>(sfb);
+  }
+  fence_proxy_async_shared();  // the MMAs read the boxes through the async proxy
+  named_barrier_sync(1, 128);
+  return gs;
+}
+
+template <int kEpi, bool kSmallA, bool kQuantA>
+__global__ void __launch_bounds__(kGemmThreads, kQuantA ? 1 : kCtasPerSm)
     nvfp4_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                       const __grid_constant__ CUtensorMap tmB,
                       const __grid_constant__ CUtensorMap tmBs, const GemmArgs args) {
-  constexpr int S = Ring<kSmallA>::kStagesR;    // stages in the ring
-  constexpr int kAB = Ring<kSmallA>::kABytes;    // A slot per stage
+  using R = Ring<kSmallA, kQuantA>;
+  constexpr int S = R::kStagesR;    // stages in the ring
+  constexpr int kAB = R::kABytes;   // A slot per stage (kQuantA: per K stage, resident)
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   uint8_t *sA = smem;
-  uint8_t *sB = sA + S * kAB;
+  uint8_t *sB = sA + R::kASlots * kAB;
   uint8_t *sSFA = sB + S * kTileBytesB;
-  uint8_t *sSFB = sSFA + S * kSfBytesStage;
+  uint8_t *sSFB = sSFA + R::kASlots * kSfBytesStage;
   uint64_t *full = reinterpret_cast<uint64_t *>(sSFB + S * kSfBytesStage);
   uint64_t *empty = full + S;
   uint64_t *tfull = empty + S;
@@ -94,6 +165,7 @@ __global__ void __launch_bounds__(kGemmThreads, kCtasPerSm)
   uint64_t *drain = sf_ready + S;
   uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(drain + 1);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_holder + 1);
+  uint32_t *q_scratch = reinterpret_cast<uint32_t *>(tmem_holder + 2);  // kQuantA: 5 words
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
@@ -118,7 +190,7 @@ __global__ void __launch_bounds__(kGemmThreads, kCtasPerSm)
     if (args.shared_group >= 0) prefetch_tensormap(&tmBs);
   }
   if (warp == 1) {
-    tmem_alloc(tmem_holder, kTmemCols);
+    tmem_alloc(tmem_holder, R::kTmemColsR);
     tmem_relinquish();
   }
   tc_fence_before();
@@ -210,15 +282,17 @@ __global__ void __launch_bounds__(kGemmThreads, kCtasPerSm)
             break;
           }
           const bool b_done = n_issued < early;
-          mbar_arrive_expect_tx(&full[stage],
-                                nbox * (kABoxRows * kStageK / 2) + kv * kSfBytesPerKStep +
-                                    (b_done ? 0 : kTileBytesB + kv * kSfBytesPerKStep));
-          uint8_t *a_dst = sA + stage * kAB;
-          for (int b = 0; b < nbox; ++b)
-            tma_load_2d(a_dst + b * (kABoxRows * kStageK / 2), &tmA, a_x0 + ks * (kStageK / 2),
-                        t.a_row0 + b * kABoxRows, &full[stage], pol_a);
-          bulk_load(sSFA + stage * kSfBytesStage, sfa + static_cast<size_t>(ks) * kSfBytesStage,
-                    kv * kSfBytesPerKStep, &full[stage], pol_a);
+          // kQuantA: the A boxes and their scales are resident (quantised in this CTA)
+          const uint32_t a_bytes = kQuantA ? 0u : nbox * (kABoxRows * kStageK / 2) + kv * kSfBytesPerKStep;
+          mbar_arrive_expect_tx(&full[stage], a_bytes + (b_done ? 0 : kTileBytesB + kv * kSfBytesPerKStep));
+          if constexpr (!kQuantA) {
+            uint8_t *a_dst = sA + stage * kAB;
+            for (int b = 0; b < nbox; ++b)
+              tma_load_2d(a_dst + b * (kABoxRows * kStageK / 2), &tmA, a_x0 + ks * (kStageK / 2),
+                          t.a_row0 + b * kABoxRows, &full[stage], pol_a);
+            bulk_load(sSFA + stage * kSfBytesStage, sfa + static_cast<size_t>(ks) * kSfBytesStage,
+                      kv * kSfBytesPerKStep, &full[stage], pol_a);
+          }
           if (!b_done) {
             tma_load_2d(sB + stage * kTileBytesB, mb, ks * (kStageK / 2), b_row0, &full[stage],
                         pol_w);
@@ -275,7 +349,7 @@ __global__ void __launch_bounds__(kGemmThreads, kCtasPerSm)
           }
           tc_fence_after();
           const uint32_t sf_col = tmem_base + kTmemAccCols + stage * kTmemSfCols;
-          const uint64_t adesc = smem_desc(sA0 + stage * kAB, 16, 1024, 2);
+          const uint64_t adesc = smem_desc(sA0 + (kQuantA ? ks : stage) * kAB, 16, 1024, 2);
           const uint64_t bdesc = smem_desc(sB0 + stage * kTileBytesB, 16, 1024, 2);
           for (int j = 0; j < kv; ++j) {
             // +32 bytes of K per step inside the 128-byte swizzle row (descriptor units of 16 B)
@@ -300,7 +374,12 @@ __global__ void __launch_bounds__(kGemmThreads, kCtasPerSm)
     // -------------------------------------------------------------- epilogue
     const int quarter = warp & 3;  // TMEM lanes [32*quarter, 32*quarter + 32)
     const int m = quarter * 32 + lane;
-    const float gs_scalar = (kEpi == static_cast<int>(Epi::kW2)) ? 0.f : __ldg(args.gs_a);
+    float gs_scalar = 0.f;
+    if constexpr (kQuantA) {
+      gs_scalar = quantize_resident_a(args, sA, sSFA, q_scratch, threadIdx.x - 2 * 32);
+    } else if constexpr (kEpi != static_cast<int>(Epi::kW2)) {
+      gs_scalar = __ldg(args.gs_a);
+    }
     // Scale staging.  Each K step's 512-byte swizzled block holds, at 16 r + 4 c, the
     // four UE4M3 scales (64 K) of operand row 32 c + r.  Every 32-lane quarter of TMEM
     // receives the same copy of the block: lane 32 q + r, column (scale address + c)
@@ -337,7 +416,7 @@ __global__ void __launch_bounds__(kGemmThreads, kCtasPerSm)
         ok = mbar_wait_bounded(&full[sstage], sphase, abort_flag, args.err, kPipelineTimeoutNs);
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) break;
-        const uint8_t *pa = sSFA + sstage * kSfBytesStage + sf_off;
+        const uint8_t *pa = sSFA + (kQuantA ? ks : sstage) * kSfBytesStage + sf_off;
         const uint8_t *pb = sSFB + sstage * kSfBytesStage + sf_off;
         uint32_t ra[16], rb[16];
 #pragma unroll
@@ -495,7 +574,7 @@ __global__ void __launch_bounds__(kGemmThreads, kCtasPerSm)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (warp == 1) tmem_dealloc(tmem_base, kTmemCols);
+  if (warp == 1) tmem_dealloc(tmem_base, R::kTmemColsR);
 
 }
 
@@ -517,15 +596,15 @@ __global__ void wait_timeout_probe_kernel(uint64_t timeout_ns, uint32_t *err) {
   }
 }
 
-template <int kEpi, bool kSmallA>
+template <int kEpi, bool kSmallA, bool kQuantA = false>
 cudaError_t launch_gemm_t(const CUtensorMap &ta, const CUtensorMap &tb, const CUtensorMap &tbs,
                           const GemmArgs &args, int grid, bool one_per_sm, cudaStream_t s) {
-  using R = Ring<kSmallA>;
+  using R = Ring<kSmallA, kQuantA>;
   static bool attr_done[64] = {false};
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 64 && !attr_done[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(nvfp4_gemm_kernel<kEpi, kSmallA>,
+    cudaError_t e = cudaFuncSetAttribute(nvfp4_gemm_kernel<kEpi, kSmallA, kQuantA>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(R::kSmemSolo));
     if (e != cudaSuccess) return e;
@@ -533,7 +612,7 @@ cudaError_t launch_gemm_t(const CUtensorMap &ta, const CUtensorMap &tb, const CU
   }
   // A grid no larger than the SM count asks for enough shared memory to keep one CTA per
   // SM, so its tiles spread over as many SMs as there are tiles.
-  return launch_pdl(nvfp4_gemm_kernel<kEpi, kSmallA>, dim3(grid), dim3(kGemmThreads),
+  return launch_pdl(nvfp4_gemm_kernel<kEpi, kSmallA, kQuantA>, dim3(grid), dim3(kGemmThreads),
                     one_per_sm ? R::kSmemSolo : R::kSmem, s, ta, tb, tbs, args);
 }
 
@@ -558,6 +637,10 @@ cudaError_t launch_gemm(Epi epi, const CUtensorMap &ta, const CUtensorMap &tb,
       return launch_gemm_e<static_cast<int>(Epi::kW2)>(ta, tb, tbs, args, grid, one_per_sm, small_a, s);
   }
   return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_gemm_quant_a(const CUtensorMap &tb, const GemmArgs &args, int grid, cudaStream_t s) {
+  return launch_gemm_t<static_cast<int>(Epi::kLinear), true, true>(tb, tb, tb, args, grid, true, s);
 }
 
 cudaError_t launch_wait_timeout_probe(uint32_t timeout_us, uint32_t *err, cudaStream_t s) {

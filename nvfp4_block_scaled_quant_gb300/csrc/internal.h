@@ -47,20 +47,32 @@ constexpr size_t kGemmBarrierBytes = 256;
 // 128-row A slot.  When no tile can have more than 32 live rows (decode-sized MoE
 // calls, M <= 32), the A slot shrinks to one 32-row box and 4 stages fit in less
 // shared memory: a third more weight bytes in flight per CTA.
-template <bool kSmallA>
+// With kQuantA (dense linear, M <= 32, K <= kQuantMaxK) the CTA quantises the bf16
+// activations itself: every K stage's A box and scale block stay resident (written once
+// by the epilogue warps), and a ring of kQuantStages stages carries the weights only.
+// One CTA per SM, owning all 512 TMEM columns.
+constexpr int kQuantMaxK = 4096;
+// Every CTA quantises all of x: the fused path pays off while x is small.
+constexpr int64_t kQuantMaxElems = 16384;
+constexpr int kQuantStages = 6;
+
+template <bool kSmallA, bool kQuantA = false>
 struct Ring {
-  static constexpr int kStagesR = kSmallA ? 4 : kStages;
+  static constexpr int kStagesR = kQuantA ? kQuantStages : (kSmallA ? 4 : kStages);
   static constexpr int kABytes = kSmallA ? kABoxRows * kStageK / 2 : kTileBytesA;
+  static constexpr int kASlots = kQuantA ? kQuantMaxK / kStageK : kStagesR;  // A and SFA slots
+  static constexpr uint32_t kTmemColsR = kQuantA ? 512 : kTmemCols;
   static constexpr size_t kSmem = 1024 /* alignment slack */ +
-                                  static_cast<size_t>(kStagesR) *
-                                      (kABytes + kTileBytesB + 2 * kSfBytesStage) +
+                                  static_cast<size_t>(kASlots) * (kABytes + kSfBytesStage) +
+                                  static_cast<size_t>(kStagesR) * (kTileBytesB + kSfBytesStage) +
                                   kGemmBarrierBytes;
   // Requested (not used) by launches that want one CTA per SM: two of these do not fit.
-  static constexpr size_t kSmemSolo = 2 * kSmem;
-  static_assert(kTmemAccCols + kStagesR * kTmemSfCols <= kTmemCols, "TMEM budget");
-  static_assert((3 * kStagesR + 5) * 8 + 8 <= kGemmBarrierBytes, "barrier region");
+  static constexpr size_t kSmemSolo = kQuantA ? kSmem : 2 * kSmem;
+  static_assert(!kQuantA || kSmallA, "the resident A holds one 32-row box per K stage");
+  static_assert(kTmemAccCols + kStagesR * kTmemSfCols <= kTmemColsR, "TMEM budget");
+  static_assert((3 * kStagesR + 5) * 8 + 8 + 24 <= kGemmBarrierBytes, "barrier region and scratch");
   static_assert(kSmemSolo <= 232448, "per-block shared memory limit");
-  static_assert(2 * (kSmem + 1024) <= 233472, "two CTAs per SM");
+  static_assert(kQuantA || 2 * (kSmem + 1024) <= 233472, "two CTAs per SM");
   static_assert(kABytes % 1024 == 0, "128-byte swizzle atoms stay 1024-byte aligned");
 };
 
@@ -105,6 +117,12 @@ struct GemmArgs {
   int early_b;              // 1: B tiles and the tile schedule may be read before the
                             // previous kernel completes (the caller's chain guarantees
                             // they were written two or more launches back)
+  // kQuantA: the bf16 activations (dense_M rows of K, row stride qa_ld elements), the
+  // static scale (null: dynamic amax/2688) and where CTA 0 writes the dynamic scale.
+  const void *qa_x;
+  int64_t qa_ld;
+  const float *qa_gs_static;
+  float *qa_gs_out;
 };
 
 // Launch with programmatic dependent launch allowed: the kernel may start while the
@@ -173,6 +191,9 @@ cudaError_t launch_finalize(const float *y_acc, int64_t n, void *y, cudaStream_t
 cudaError_t launch_gemm(Epi epi, const CUtensorMap &ta, const CUtensorMap &tb,
                         const CUtensorMap &tbs, const GemmArgs &args, int grid, bool one_per_sm,
                         bool small_a, cudaStream_t s);
+// Dense linear with the activation quantisation fused (kQuantA): 1 <= M <= 32, K <= kQuantMaxK,
+// grid <= SM count.
+cudaError_t launch_gemm_quant_a(const CUtensorMap &tb, const GemmArgs &args, int grid, cudaStream_t s);
 cudaError_t launch_wait_timeout_probe(uint32_t timeout_us, uint32_t *err, cudaStream_t s);
 
 }  // namespace nvfp4

@@ -36,6 +36,28 @@ def test_linear_ragged_shapes(M, K, N):
     assert_parity(bf16_to_np(y), O.linear(xq, wq.codes, wq.sf, wq.gs), what=f"linear {M}x{K}x{N}")
 
 
+@pytest.mark.parametrize("M,K,N", [(10, 1536, 256), (11, 1536, 256), (4, 4096, 384), (1, 4096, 128), (1, 4160, 128),
+                                   (2, 64, 1024)])
+def test_linear_fused_quantisation_edges(M, K, N):
+    """Small M: the GEMM CTAs quantise x themselves (up to 16K elements, K <= 4096, every K stage
+    resident); just beyond those limits the separate quantise launch runs.  Both give the same
+    result and the same dynamic gs."""
+    x = workloads.activations(M, K, seed=M * 31 + K, device="cpu", outliers=True)
+    wp, sfp, ws2, wq = _weights(N, K, seed=M + N)
+    y, gs = ops.linear(x.to(DEV), wp, sfp, ws2, N)
+    torch.cuda.synchronize()
+    assert ops.device_error() == (0, 0)
+    xq = O.quantize(x.float().numpy())
+    assert gs.item() == float(xq.gs)
+    assert_parity(bf16_to_np(y), O.linear(xq, wq.codes, wq.sf, wq.gs), what=f"linear {M}x{K}x{N}")
+    gst = torch.tensor([0.0017], dtype=torch.float32, device=DEV)
+    y2, g2 = ops.linear(x.to(DEV), wp, sfp, ws2, N, gs=gst)
+    torch.cuda.synchronize()
+    assert g2.item() == np.float32(0.0017)  # a static scale is read, not rewritten
+    xq2 = O.quantize(x.float().numpy(), gs=np.float32(0.0017))
+    assert_parity(bf16_to_np(y2), O.linear(xq2, wq.codes, wq.sf, wq.gs), what=f"linear static {M}x{K}x{N}")
+
+
 @pytest.mark.parametrize("M", sorted(workloads.DENSE_LINEAR))
 def test_linear_dense_workload_full(M):
     """The dense Nvfp4Linear workload (K=1536, N=16384, outlier activations), every output checked."""
