@@ -510,18 +510,18 @@ static nvfp4_status gemm_dense(const char *fn, DeviceInfo *d, const uint8_t *xq,
   return NVFP4_OK;
 }
 
-// Dense linear for 1 <= M <= 32 rows, K <= kQuantMaxK and M*K <= kQuantMaxElems in one
-// launch: the GEMM CTAs quantise x themselves (same arithmetic as nvfp4_quantize_act)
-// into resident A boxes.
-static nvfp4_status linear_fused(const char *fn, DeviceInfo *d, const void *x, int64_t M, int64_t K, int64_t N,
-                                 const uint8_t *w, const uint8_t *w_sf, const float *ws2, bool dyn, float *gs,
-                                 void *y, cudaStream_t s) {
+// Dense (G = 1) or fixed-group linear for 1 <= M <= 32 rows in one launch: the GEMM CTAs
+// quantise x themselves (same arithmetic as nvfp4_quantize_act) into resident A boxes.
+// Every CTA reduces the amax over all G*K columns and quantises its group's K of them.
+static nvfp4_status linear_fused(const char *fn, DeviceInfo *d, const void *x, int64_t M, int64_t G, int64_t K,
+                                 int64_t N, const uint8_t *w, const uint8_t *w_sf, const float *ws2, bool dyn,
+                                 float *gs, void *y, cudaStream_t s) {
   CUtensorMap tb;
-  nvfp4_status st = make_map(fn, &tb, w, K / 2, N, K / 2, kBlockN);
+  nvfp4_status st = make_map(fn, &tb, w, K / 2, G * N, K / 2, kBlockN);
   if (st != NVFP4_OK) return st;
   GemmArgs a;
   std::memset(&a, 0, sizeof(a));
-  a.G = 1;
+  a.G = static_cast<int>(G);
   a.N = static_cast<int>(N);
   a.K = static_cast<int>(K);
   a.dense_M = static_cast<int>(M);
@@ -529,22 +529,24 @@ static nvfp4_status linear_fused(const char *fn, DeviceInfo *d, const void *x, i
   a.b_sf = w_sf;
   a.ws2 = ws2;
   a.out = y;
-  a.out_ld = static_cast<int>(N);
+  a.out_ld = static_cast<int>(G * N);
   a.out_group_cols = static_cast<int>(N);
   a.err = d->flags;
   a.early_b = 0;  // the launch just before this one may have written W
   a.qa_x = x;
-  a.qa_ld = K;
+  a.qa_ld = G * K;
   a.qa_gs_static = dyn ? nullptr : gs;
   a.qa_gs_out = dyn ? gs : nullptr;
-  const int64_t tiles = N / kBlockN;
+  const int64_t tiles = G * (N / kBlockN);
+  // a dense linear's CTAs may take several tiles (all of group 0); groups need one tile per CTA
   const int grid = static_cast<int>(tiles < d->sms ? tiles : d->sms);
   NV_CUDA(launch_gemm_quant_a(tb, a, grid, s), "fused linear launch");
   return NVFP4_OK;
 }
 
-static bool linear_fusable(int64_t M, int64_t K) {
-  return M >= 1 && M <= kABoxRows && K <= kQuantMaxK && M * K <= kQuantMaxElems;
+static bool linear_fusable(const DeviceInfo *d, int64_t M, int64_t G, int64_t K, int64_t N) {
+  return M >= 1 && M <= kABoxRows && K <= kQuantMaxK && M * K <= kQuantMaxElems &&
+         M * G * K <= 4 * kQuantMaxElems && (G == 1 || G * (N / kBlockN) <= d->sms);
 }
 
 #define NV_CHECK_GEMM_SHAPE(M, K, N)                                                                          \
@@ -584,7 +586,7 @@ nvfp4_status nvfp4_linear(const void *x, int64_t M, int64_t K, int64_t N, const 
   if ((st = device_info(__func__, &d)) != NVFP4_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const bool dyn = gs_mode == NVFP4_GS_DYNAMIC;
-  if (linear_fusable(M, K)) return linear_fused(__func__, d, x, M, K, N, w, w_sf, ws2, dyn, gs, y, s);
+  if (linear_fusable(d, M, 1, K, N)) return linear_fused(__func__, d, x, M, 1, K, N, w, w_sf, ws2, dyn, gs, y, s);
   uint8_t *xq = at<uint8_t>(ws, L.xq), *xsf = at<uint8_t>(ws, L.xsf);
   uint32_t *partials = dyn ? at<uint32_t>(ws, L.partials) : nullptr;
   NV_CUDA(launch_act_quant(x, M, K, K, dyn, partials, gs, gs, xq, xsf, NVFP4_SF_SWIZZLED, s), "quantize kernel launch");
@@ -640,7 +642,7 @@ nvfp4_status nvfp4_linear_noalloc(const void *x, int64_t M, int64_t K, int64_t N
   if ((st = noalloc_scratch(__func__, &scratch)) != NVFP4_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const bool dyn = gs_mode == NVFP4_GS_DYNAMIC;
-  if (linear_fusable(M, K)) return linear_fused(__func__, d, x, M, K, N, w, w_sf, ws2, dyn, gs, y, s);
+  if (linear_fusable(d, M, 1, K, N)) return linear_fused(__func__, d, x, M, 1, K, N, w, w_sf, ws2, dyn, gs, y, s);
   uint8_t *xq = at<uint8_t>(scratch, L.xq), *xsf = at<uint8_t>(scratch, L.xsf);
   uint32_t *partials = dyn ? at<uint32_t>(scratch, L.partials) : nullptr;
   NV_CUDA(launch_act_quant(x, M, K, K, dyn, partials, gs, gs, xq, xsf, NVFP4_SF_SWIZZLED, s), "quantize kernel launch");
@@ -671,8 +673,9 @@ nvfp4_status nvfp4_grouped_linear(const void *x, int64_t M, int64_t G, int64_t K
   DeviceInfo *d;
   if ((st = device_info(__func__, &d)) != NVFP4_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  uint8_t *xq = at<uint8_t>(ws, L.xq), *xsf = at<uint8_t>(ws, L.xsf);
   const bool dyn = gs_mode == NVFP4_GS_DYNAMIC;
+  if (linear_fusable(d, M, G, K, N)) return linear_fused(__func__, d, x, M, G, K, N, w, w_sf, ws2, dyn, gs, y, s);
+  uint8_t *xq = at<uint8_t>(ws, L.xq), *xsf = at<uint8_t>(ws, L.xsf);
   uint32_t *partials = dyn ? at<uint32_t>(ws, L.partials) : nullptr;
   NV_CUDA(launch_act_quant(x, M, G * K, G * K, dyn, partials, gs, gs, xq, xsf, NVFP4_SF_SWIZZLED, s),
           "quantize kernel launch");

@@ -76,30 +76,32 @@ __device__ __forceinline__ void named_barrier_sync(int id, int threads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
 }
 
-// Fused activation quantisation (dense linear, dense_M <= 32 rows): the four epilogue
-// warps (tid 0..127, named barrier 1) take gs = fl32(amax / 2688) over x (or the static
-// scale), then encode every 16-element block with the activation quantiser's arithmetic
-// into the resident A boxes (one 32-row, 128-byte-swizzled 4 KB box per 256-element K
-// stage: 16-byte chunk c of row r sits at chunk c ^ (r & 7)) and their scale blocks
-// (row r's four scales of a 64-element K step at 16 r in that step's 512-byte block).
-// CTA 0 writes gs out; every CTA returns the same gs.
-__device__ float quantize_resident_a(const GemmArgs &a, uint8_t *sA, uint8_t *sSFA, uint32_t *scratch, int tid) {
+// Fused activation quantisation (dense_M <= 32 rows): the four epilogue warps (tid
+// 0..127, named barrier 1) take gs = fl32(amax / 2688) over all qa_ld columns of x (or
+// the static scale), then encode the K columns of group g (columns g*K .. g*K+K-1; g = 0
+// for a dense linear) with the activation quantiser's arithmetic into the resident A
+// boxes (one 32-row, 128-byte-swizzled 4 KB box per 256-element K stage: 16-byte chunk
+// c of row r sits at chunk c ^ (r & 7)) and their scale blocks (row r's four scales of a
+// 64-element K step at 16 r in that step's 512-byte block).  CTA 0 writes gs out; every
+// CTA returns the same gs.
+__device__ float quantize_resident_a(const GemmArgs &a, int g, uint8_t *sA, uint8_t *sSFA, uint32_t *scratch,
+                                     int tid) {
   const int64_t M = a.dense_M, K = a.K, ld = a.qa_ld;
   const uint16_t *x = static_cast<const uint16_t *>(a.qa_x);
   const int warp = tid >> 5, lane = tid & 31;
   float gs;
   if (a.qa_gs_static == nullptr) {
     uint32_t m = 0;
-    const int64_t chunks = K / 8, n = M * chunks;
-    for (int64_t i0 = tid; i0 < n; i0 += 4 * 128) {  // four 16-byte loads in flight per thread
-      uint4 v[4];
+    const int64_t chunks = ld / 8, n = M * chunks;
+    for (int64_t i0 = tid; i0 < n; i0 += 8 * 128) {  // eight 16-byte loads in flight per thread
+      uint4 v[8];
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
+      for (int u = 0; u < 8; ++u) {
         const int64_t i = i0 + u * 128, r = i / chunks;
         v[u] = i < n ? __ldg(reinterpret_cast<const uint4 *>(x + r * ld) + (i - r * chunks)) : make_uint4(0, 0, 0, 0);
       }
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
+      for (int u = 0; u < 8; ++u) {
         const uint32_t w[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
 #pragma unroll
         for (int k = 0; k < 4; ++k) m = max(m, max(w[k] & 0x7FFFu, (w[k] >> 16) & 0x7FFFu));
@@ -119,8 +121,8 @@ __device__ float quantize_resident_a(const GemmArgs &a, uint8_t *sA, uint8_t *sS
   const int64_t kb = K / 16;
 #pragma unroll 2
   for (int64_t i = tid; i < M * kb; i += 128) {
-    const int64_t r = i / kb, c = i - r * kb;  // row, 16-element block
-    const uint4 *src = reinterpret_cast<const uint4 *>(x + r * ld + c * 16);
+    const int64_t r = i / kb, c = i - r * kb;  // row, 16-element block of the group
+    const uint4 *src = reinterpret_cast<const uint4 *>(x + r * ld + static_cast<int64_t>(g) * K + c * 16);
     const uint4 p = __ldg(src), q = __ldg(src + 1);
     const uint32_t w[8] = {p.x, p.y, p.z, p.w, q.x, q.y, q.z, q.w};
     float v[16];
@@ -376,7 +378,9 @@ __global__ void __launch_bounds__(kGemmThreads, kQuantA ? 1 : kCtasPerSm)
     const int m = quarter * 32 + lane;
     float gs_scalar = 0.f;
     if constexpr (kQuantA) {
-      gs_scalar = quantize_resident_a(args, sA, sSFA, q_scratch, threadIdx.x - 2 * 32);
+      // one tile per CTA (the launch guarantees it): its group's K columns
+      const int g = static_cast<int>(blockIdx.x) < total_tiles ? tile_entry(args, blockIdx.x / n_tiles).x : 0;
+      gs_scalar = quantize_resident_a(args, g, sA, sSFA, q_scratch, threadIdx.x - 2 * 32);
     } else if constexpr (kEpi != static_cast<int>(Epi::kW2)) {
       gs_scalar = __ldg(args.gs_a);
     }

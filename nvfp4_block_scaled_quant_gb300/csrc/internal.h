@@ -117,8 +117,9 @@ struct GemmArgs {
   int early_b;              // 1: B tiles and the tile schedule may be read before the
                             // previous kernel completes (the caller's chain guarantees
                             // they were written two or more launches back)
-  // kQuantA: the bf16 activations (dense_M rows of K, row stride qa_ld elements), the
-  // static scale (null: dynamic amax/2688) and where CTA 0 writes the dynamic scale.
+  // kQuantA: the bf16 activations (dense_M rows of qa_ld = G*K elements; group g uses
+  // columns g*K..), the static scale (null: dynamic amax/2688 over all columns) and
+  // where CTA 0 writes the dynamic scale.  The tiles of a CTA all belong to one group.
   const void *qa_x;
   int64_t qa_ld;
   const float *qa_gs_static;
@@ -191,8 +192,8 @@ cudaError_t launch_finalize(const float *y_acc, int64_t n, void *y, cudaStream_t
 cudaError_t launch_gemm(Epi epi, const CUtensorMap &ta, const CUtensorMap &tb,
                         const CUtensorMap &tbs, const GemmArgs &args, int grid, bool one_per_sm,
                         bool small_a, cudaStream_t s);
-// Dense linear with the activation quantisation fused (kQuantA): 1 <= M <= 32, K <= kQuantMaxK,
-// grid <= SM count.
+// Dense or fixed-group linear with the activation quantisation fused (kQuantA): 1 <= M <= 32,
+// K <= kQuantMaxK, grid = tiles <= SM count (one tile per CTA).
 cudaError_t launch_gemm_quant_a(const CUtensorMap &tb, const GemmArgs &args, int grid, cudaStream_t s);
 cudaError_t launch_wait_timeout_probe(uint32_t timeout_us, uint32_t *err, cudaStream_t s);
 
