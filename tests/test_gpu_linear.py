@@ -37,11 +37,12 @@ def test_linear_ragged_shapes(M, K, N):
 
 
 @pytest.mark.parametrize("M,K,N", [(10, 1536, 256), (11, 1536, 256), (4, 4096, 384), (1, 4096, 128), (1, 4160, 128),
-                                   (2, 64, 1024)])
+                                   (2, 64, 1024), (2, 256, 20480)])
 def test_linear_fused_quantisation_edges(M, K, N):
     """Small M: the GEMM CTAs quantise x themselves (up to 16K elements, K <= 4096, every K stage
     resident); just beyond those limits the separate quantise launch runs.  Both give the same
-    result and the same dynamic gs."""
+    result and the same dynamic gs.  N = 20480 has more tiles (160) than SMs, so CTAs reuse
+    their resident A for a second tile."""
     x = workloads.activations(M, K, seed=M * 31 + K, device="cpu", outliers=True)
     wp, sfp, ws2, wq = _weights(N, K, seed=M + N)
     y, gs = ops.linear(x.to(DEV), wp, sfp, ws2, N)
