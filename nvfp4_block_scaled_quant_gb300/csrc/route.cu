@@ -126,8 +126,8 @@ __device__ void route_block(const int32_t *__restrict__ ids, int T, int topk, in
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     for (int g = threadIdx.x; g < G; g += blockDim.x) s_cnt[g] = 0;
     __syncthreads();
-    // histogram: one shared-memory atomic per distinct expert of each 32 entries; each
-    // warp has kHistUnroll loads in flight before it uses the first
+    // histogram: one shared-memory atomic per entry (cheaper than grouping equal ids with
+    // a warp match first); each warp has kHistUnroll loads in flight before it uses the first
     for (int f0 = warp * 32; f0 < Tk; f0 += blockDim.x * kHistUnroll) {
       int ev[kHistUnroll];
 #pragma unroll
@@ -143,8 +143,7 @@ __device__ void route_block(const int32_t *__restrict__ ids, int T, int topk, in
           raise_device_error(err, NVFP4_DEVERR_BAD_EXPERT_ID);
           e = -1;
         }
-        const unsigned peers = __match_any_sync(0xffffffffu, e);
-        if (e >= 0 && lane == __ffs(peers) - 1) atomicAdd(&s_cnt[e], __popc(peers));
+        if (e >= 0) atomicAdd(&s_cnt[e], 1);
       }
     }
     if (has_shared && threadIdx.x == 0) s_cnt[E] = T;
@@ -214,9 +213,7 @@ __device__ void route_block(const int32_t *__restrict__ ids, int T, int topk, in
       for (int j = 0; j < kRankPerWarp / 32; ++j) {
         const int e = load_id(w0 + 32 * j + lane);
         my_e[j] = e;
-        const unsigned peers = __match_any_sync(0xffffffffu, e);
-        if (e >= 0 && lane == __ffs(peers) - 1) my_cnt[e] += __popc(peers);
-        __syncwarp();
+        if (e >= 0) atomicAdd(&my_cnt[e], 1);  // counts only: the order of the atomics is free
       }
       __syncthreads();
       for (int e = threadIdx.x; e < E; e += blockDim.x) {
