@@ -11,7 +11,7 @@ constexpr int kRouteThreads = 512;
 constexpr int kDispatchThreads = 256;
 constexpr int kDestRegs = 8;  // destination rows held in registers (top-k up to 8)
 constexpr int kRankWarps = kRouteThreads / 32;
-constexpr int kRankPerWarp = 256;                      // entries per warp and chunk
+constexpr int kRankPerWarp = 512;                      // entries per warp and chunk
 constexpr int kRankChunk = kRankWarps * kRankPerWarp;  // entries ranked per pass
 constexpr int kSmallRank = 256;                        // up to this many entries one warp ranks
 constexpr int kHistUnroll = 8;                         // id loads in flight per histogram step
