@@ -244,12 +244,13 @@ __device__ __forceinline__ void st_global_v8(void *p, const uint32_t (&w)[8]) {
                : "memory");
 }
 
-// y[0..3] += (a, b, c, d): a 16-byte fp32 vector reduction in L2 that returns nothing.
-// Written out so the scatter-add stays a reduction whatever else the kernel contains
-// (a value-returning atomic costs the w2 scatter about 2.4x at 4096 tokens).
-__device__ __forceinline__ void red_add_v4(float4 *p, float a, float b, float c, float d) {
-  asm volatile("red.relaxed.gpu.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p), "f"(a), "f"(b), "f"(c),
-               "f"(d)
+// y[0..3] += (a, b, c, d): a 16-byte fp32 vector reduction in L2 that returns nothing,
+// with an L2 cache policy.  Written out so the scatter-add stays a reduction whatever
+// else the kernel contains (a value-returning atomic costs the w2 scatter about 2.4x at
+// 4096 tokens).
+__device__ __forceinline__ void red_add_v4(float4 *p, float a, float b, float c, float d, uint64_t policy) {
+  asm volatile("red.relaxed.gpu.global.add.L2::cache_hint.v4.f32 [%0], {%1, %2, %3, %4}, %5;" ::"l"(p), "f"(a),
+               "f"(b), "f"(c), "f"(d), "l"(policy)
                : "memory");
 }
 

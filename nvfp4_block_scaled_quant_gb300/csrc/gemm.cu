@@ -552,6 +552,9 @@ __global__ void __launch_bounds__(kGemmThreads, kQuantA ? 1 : kCtasPerSm)
       } else {  // kW2
         const float scale = w2_scale;
         const int64_t tok = w2_tok;
+        // the accumulator rows stay in L2 between the k + 1 contributions to a token while
+        // the weights stream past with evict_first
+        const uint64_t pol_y = policy_evict_last();
         float4 *dst = reinterpret_cast<float4 *>(static_cast<float *>(args.out) +
                                                  tok * args.out_ld + t.nt * kBlockN);
 #pragma unroll
@@ -568,7 +571,7 @@ __global__ void __launch_bounds__(kGemmThreads, kQuantA ? 1 : kCtasPerSm)
               for (int i = 0; i < 4; ++i)
                 red_add_v4(dst + h * 16 + q * 4 + i, __uint_as_float(r[q][4 * i]) * scale,
                            __uint_as_float(r[q][4 * i + 1]) * scale, __uint_as_float(r[q][4 * i + 2]) * scale,
-                           __uint_as_float(r[q][4 * i + 3]) * scale);
+                           __uint_as_float(r[q][4 * i + 3]) * scale, pol_y);
           }
         }
       }
