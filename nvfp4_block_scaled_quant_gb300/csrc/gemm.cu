@@ -213,6 +213,12 @@ __global__ void __launch_bounds__(kGemmThreads, kQuantA ? 1 : kCtasPerSm)
   const int total_mtiles = args.counts ? __ldg(args.tile_offsets + args.G)
                                        : args.G * ((args.dense_M + kBlockM - 1) / kBlockM);
   const int total_tiles = total_mtiles * n_tiles;
+  // The tiles of a launch cost the same, so the CTAs taking part are trimmed to
+  // ceil(tiles / waves): every wave, the last included, is (nearly) full instead of
+  // leaving the last fraction of the run to a fraction of the CTAs.  CTAs beyond take none.
+  const int waves = (total_tiles + static_cast<int>(gridDim.x) - 1) / static_cast<int>(gridDim.x);
+  const int grid = waves > 0 ? (total_tiles + waves - 1) / waves : static_cast<int>(gridDim.x);
+  const int first = static_cast<int>(blockIdx.x) < grid ? static_cast<int>(blockIdx.x) : total_tiles;
 
   if (warp == 0) {
     if (lane == 0) {
@@ -231,8 +237,8 @@ __global__ void __launch_bounds__(kGemmThreads, kQuantA ? 1 : kCtasPerSm)
       // Weights of the first stages of this CTA's first tile, before the previous kernel ends.
       int early = 0;
       if (args.early_b) {
-        if (static_cast<int>(blockIdx.x) < total_tiles) {
-          const Tile t = make_tile(tile_entry(args, blockIdx.x / n_tiles), blockIdx.x, n_tiles);
+        if (first < total_tiles) {
+          const Tile t = make_tile(tile_entry(args, first / n_tiles), first, n_tiles);
           const CUtensorMap *mb;
           int b_row0;
           const uint8_t *sfb;
@@ -255,12 +261,10 @@ __global__ void __launch_bounds__(kGemmThreads, kQuantA ? 1 : kCtasPerSm)
       uint32_t issued = 0;  // bit s: stage s has a load in flight with parity bit (s+8)
       int n_issued = 0;     // stages issued so far (the first `early` already hold their B)
       bool ok = true;
-      int4 next = static_cast<int>(blockIdx.x) < total_tiles ? tile_entry(args, blockIdx.x / n_tiles)
-                                                             : make_int4(0, 0, 0, 0);
-      for (int idx = blockIdx.x; ok && idx < total_tiles; idx += gridDim.x) {
+      int4 next = first < total_tiles ? tile_entry(args, first / n_tiles) : make_int4(0, 0, 0, 0);
+      for (int idx = first; ok && idx < total_tiles; idx += grid) {
         const Tile t = make_tile(next, idx, n_tiles);
-        if (idx + static_cast<int>(gridDim.x) < total_tiles)
-          next = tile_entry(args, (idx + gridDim.x) / n_tiles);
+        if (idx + grid < total_tiles) next = tile_entry(args, (idx + grid) / n_tiles);
         const CUtensorMap *mb;
         int b_row0;
         const uint8_t *sfb;
@@ -326,7 +330,7 @@ __global__ void __launch_bounds__(kGemmThreads, kQuantA ? 1 : kCtasPerSm)
       int it = 0;
       bool ok = true;
       const uint32_t sA0 = smem_u32(sA), sB0 = smem_u32(sB);
-      for (int idx = blockIdx.x; ok && idx < total_tiles; idx += gridDim.x, ++it) {
+      for (int idx = first; ok && idx < total_tiles; idx += grid, ++it) {
         const int acc = kAccBufs == 2 ? (it & 1) : 0;
         const uint32_t acc_phase = kAccBufs == 2 ? ((it >> 1) & 1) : (it & 1);
         if (!mbar_wait_bounded(&tempty[acc], acc_phase ^ 1, abort_flag, args.err,
@@ -379,7 +383,7 @@ __global__ void __launch_bounds__(kGemmThreads, kQuantA ? 1 : kCtasPerSm)
     float gs_scalar = 0.f;
     if constexpr (kQuantA) {
       // one tile per CTA (the launch guarantees it): its group's K columns
-      const int g = static_cast<int>(blockIdx.x) < total_tiles ? tile_entry(args, blockIdx.x / n_tiles).x : 0;
+      const int g = first < total_tiles ? tile_entry(args, first / n_tiles).x : 0;
       gs_scalar = quantize_resident_a(args, g, sA, sSFA, q_scratch, threadIdx.x - 2 * 32);
     } else if constexpr (kEpi != static_cast<int>(Epi::kW2)) {
       gs_scalar = __ldg(args.gs_a);
@@ -394,12 +398,10 @@ __global__ void __launch_bounds__(kGemmThreads, kQuantA ? 1 : kCtasPerSm)
     int sstage = 0;
     uint32_t sphase = 0;
     int it = 0;
-    int4 next = static_cast<int>(blockIdx.x) < total_tiles ? tile_entry(args, blockIdx.x / n_tiles)
-                                                           : make_int4(0, 0, 0, 0);
-    for (int idx = blockIdx.x; idx < total_tiles; idx += gridDim.x, ++it) {
+    int4 next = first < total_tiles ? tile_entry(args, first / n_tiles) : make_int4(0, 0, 0, 0);
+    for (int idx = first; idx < total_tiles; idx += grid, ++it) {
       const Tile t = make_tile(next, idx, n_tiles);
-      if (idx + static_cast<int>(gridDim.x) < total_tiles)
-        next = tile_entry(args, (idx + gridDim.x) / n_tiles);
+      if (idx + grid < total_tiles) next = tile_entry(args, (idx + grid) / n_tiles);
       const int acc = kAccBufs == 2 ? (it & 1) : 0;
       const uint32_t acc_phase = kAccBufs == 2 ? ((it >> 1) & 1) : (it & 1);
       // Per-tile epilogue scalars, loaded before this tile's main loop so that their
