@@ -177,7 +177,9 @@ nvfp4_moe_ws_layout moe_layout(int64_t T, int64_t H, int64_t I, int64_t E, int t
   L.sorted_idx = take(static_cast<size_t>(Tk > 0 ? Tk : 1) * 4);
   L.inv_idx = take(static_cast<size_t>(Tk > 0 ? Tk : 1) * 4);
   L.dest_rows = take(static_cast<size_t>(Tk > 0 ? Tk : 1) * 4);
-  L.tile_table = take(rc / kBlockM * 16 + 16);
+  // one entry per tile; with kABoxRows-row tiles a group of c rows takes ceil(c / 32)
+  // <= 4 ceil(c / 128) entries, and the 128-row padded segments sum to at most rc
+  L.tile_table = take(rc / kABoxRows * 16 + 16);
   L.amax_partials = take(kMaxPartials * 4);
   L.xq = take(rc * static_cast<size_t>(H / 2));
   L.xsf = take(sf_bytes(L.rows_capacity, H));
@@ -224,6 +226,7 @@ RouteBufs route_bufs(void *ws, const nvfp4_moe_ws_layout &L) {
   rb.inv_idx = at<int>(ws, L.inv_idx);
   rb.dest_rows = at<int>(ws, L.dest_rows);
   rb.tile_table = at<int4>(ws, L.tile_table);
+  rb.tile_shift = 7;  // kBlockM-row tiles unless the caller sets moe_tile_shift(T)
   return rb;
 }
 
@@ -234,6 +237,7 @@ nvfp4_status moe_dispatch_impl(const char *fn, DeviceInfo *d, const void *x, int
                                float *a1_gs, void *ws, cudaStream_t s) {
   const nvfp4_moe_ws_layout L = moe_layout(T, H, I, E, topk, has_shared);
   RouteBufs rb = route_bufs(ws, L);
+  rb.tile_shift = moe_tile_shift(T);  // the GEMM launches on this workspace use the same T
   const bool dyn = a1_gs_mode == NVFP4_GS_DYNAMIC;
   const int nparts = amax_partial_count(T, H);
   uint32_t *partials = dyn ? at<uint32_t>(ws, L.amax_partials) : nullptr;
@@ -298,9 +302,9 @@ nvfp4_status moe_gemm_impl(const char *fn, DeviceInfo *d, Epi epi, int64_t T, in
     a.topk_w = topk_w;
     a.topk = topk;
   }
-  // A routed group holds at most T*topk rows (duplicate ids included) and the shared one T:
-  // when both stay within one 32-row box, the ring with 4 small stages applies.
-  const bool small_a = T * topk <= kABoxRows && T <= kABoxRows;
+  // The routing cut the groups into tiles of moe_tile_rows(T) rows: 32-row tiles fit one
+  // A box each, so the ring with 4 small stages applies.
+  const bool small_a = moe_tile_rows(T) == kABoxRows;
   NV_CUDA(launch_gemm(epi, ta, tb, tbs, a, d->sms * kCtasPerSm, false, small_a, s), "grouped GEMM launch");
   return NVFP4_OK;
 }
@@ -742,7 +746,7 @@ nvfp4_status nvfp4_moe_route(const int32_t *ids, int64_t T, int topk, int64_t E,
   DeviceInfo *d;
   nvfp4_status st = device_info(__func__, &d);
   if (st != NVFP4_OK) return st;
-  RouteBufs rb{counts, offsets, nullptr, nullptr, sorted_idx, inv_idx, nullptr, nullptr};
+  RouteBufs rb{counts, offsets, nullptr, nullptr, sorted_idx, inv_idx, nullptr, nullptr, moe_tile_shift(T)};
   NV_CUDA(launch_route_amax(ids, static_cast<int>(T), topk, static_cast<int>(E), 0, rb, nullptr, 0, nullptr, 0,
                             nullptr, d->flags, static_cast<cudaStream_t>(stream)),
           "route kernel launch");

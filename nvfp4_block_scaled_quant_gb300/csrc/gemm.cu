@@ -62,6 +62,15 @@ __device__ __forceinline__ Tile make_tile(const int4 e, int idx, int n_tiles) {
   return t;
 }
 
+// Word c of the result is word (c + j) & 3 of v.  A 32-row tile whose first row is
+// 32 j into its 128-row scale block needs the scales of its rows, which sit in word j
+// of each 16-byte chunk, where the MMA reads the scales of rows 0..31: word 0.
+__device__ __forceinline__ uint4 rotate_words(uint4 v, int j) {
+  if (j & 2) v = make_uint4(v.z, v.w, v.x, v.y);
+  if (j & 1) v = make_uint4(v.y, v.z, v.w, v.x);
+  return v;
+}
+
 // instruction descriptor: E2M1 x E2M1, UE4M3 scales, K-major A and B, M=128, N=128
 constexpr uint32_t kIdesc = (1u << 7) | (1u << 10) | ((uint32_t(kBlockN) >> 3) << 17) |
                             ((uint32_t(kBlockM) >> 4) << 24);
@@ -416,6 +425,10 @@ __global__ void __launch_bounds__(kGemmThreads, kQuantA ? 1 : kCtasPerSm)
         if (!sh) seg_base = __ldg(args.offsets + t.g);
       }
       const bool row_ok = m < t.rows;
+      // MoE small-A tiles are 32 rows high and may start 32 j rows into a scale block
+      // (dense and uniform-group tiles start at row 0)
+      constexpr bool kRotA = kSmallA && kEpi != static_cast<int>(Epi::kLinear);
+      const int sfa_rot = kRotA ? (t.a_row0 / kABoxRows) & 3 : 0;
       bool ok = true;
       for (int ks = 0; ks < k_stages; ++ks) {
         const int kv = min(4, k_steps - 4 * ks);
@@ -434,6 +447,15 @@ __global__ void __launch_bounds__(kGemmThreads, kQuantA ? 1 : kCtasPerSm)
           ra[4 * j] = wa.x, ra[4 * j + 1] = wa.y, ra[4 * j + 2] = wa.z, ra[4 * j + 3] = wa.w;
           rb[4 * j] = wb.x, rb[4 * j + 1] = wb.y, rb[4 * j + 2] = wb.z, rb[4 * j + 3] = wb.w;
         }
+        // Warp-uniform and rare: only a group of more than 32 rows (an expert listed twice
+        // by a token) has small-A tiles that do not start a scale block.
+        if (kRotA && __builtin_expect(sfa_rot != 0, 0)) {
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const uint4 v = rotate_words(make_uint4(ra[4 * j], ra[4 * j + 1], ra[4 * j + 2], ra[4 * j + 3]), sfa_rot);
+            ra[4 * j] = v.x, ra[4 * j + 1] = v.y, ra[4 * j + 2] = v.z, ra[4 * j + 3] = v.w;
+          }
+        }
         tmem_st16(sf_lane + sstage * kTmemSfCols, ra);
         tmem_st16(sf_lane + sstage * kTmemSfCols + 16, rb);
         tmem_st_wait();
@@ -451,7 +473,7 @@ __global__ void __launch_bounds__(kGemmThreads, kQuantA ? 1 : kCtasPerSm)
       int64_t w2_tok = 0;
       if constexpr (kEpi == static_cast<int>(Epi::kW2)) {
         if (row_ok) {
-          const int seg_row = t.mt * kBlockM + m;
+          const int seg_row = t.mt * (kSmallA ? kABoxRows : kBlockM) + m;
           float w = 1.f;
           if (sh) {
             w2_tok = seg_row;

@@ -90,8 +90,9 @@ struct GemmArgs {
   const int *pad_offsets;   // [G+1]
   const int *tile_offsets;  // [G+1]
   const int4 *tile_table;   // per m tile in tile order: group, m tile in group, live rows,
-                            // first A row (written by the routing kernel); null: every group
-                            // has dense_M rows
+                            // first A row (written by the routing kernel; the tiles are
+                            // kABoxRows high in the small-A ring, else kBlockM); null: every
+                            // group has dense_M rows
   int shared_group;         // group using the *_shared weights, or -1
   // scale factors
   const uint8_t *a_sf;      // swizzled, 128-row blocks aligned with the A rows
@@ -177,8 +178,17 @@ cudaError_t launch_prepare(const uint8_t *w, const uint8_t *sf, int64_t G, int64
 
 struct RouteBufs {
   int *counts, *offsets, *pad_offsets, *tile_offsets, *sorted_idx, *inv_idx, *dest_rows;
-  int4 *tile_table;  // per 128-row tile: group, tile in group, live rows, first row (or null)
+  int4 *tile_table;  // per tile: group, tile in group, live rows, first row (or null)
+  int tile_shift;    // log2 of the tile height: moe_tile_rows(T)
 };
+
+// Height of the MoE GEMMs' m tiles.  Up to kABoxRows tokens the groups are cut into
+// kABoxRows-row tiles, so every tile fits one A box and the GEMMs take the small-A ring;
+// a group holds at most T rows unless a token lists an expert twice, and such a group
+// simply spans several tiles.  Larger batches use kBlockM-row tiles.
+inline int moe_tile_rows(int64_t T) { return T <= kABoxRows ? kABoxRows : kBlockM; }
+inline int moe_tile_shift(int64_t T) { return T <= kABoxRows ? 5 : 7; }
+static_assert((1 << 5) == kABoxRows && (1 << 7) == kBlockM, "tile shifts");
 cudaError_t launch_route_amax(const int32_t *ids, int T, int topk, int E, int has_shared,
                               RouteBufs rb, const void *x, int64_t H, uint32_t *partials,
                               int nparts, float *y_acc, uint32_t *err, cudaStream_t s);

@@ -22,11 +22,13 @@ size_t route_smem_bytes(int E) {
   return sizeof(int) * (static_cast<size_t>(E) * (6 + kRankWarps) + 1 + 96 + 6);
 }
 
-// Block-wide exclusive scan of three int sequences of length n (n <= 4 * blockDim).
-// Writes out_x[0..n] (n+1 entries, the last one the total; n >= 1); out_pad and
-// out_tiles may be null.
-__device__ void block_scan3(const int *in_count, int n, int *out_off, int *out_pad,
+// Block-wide exclusive scans over n counts (n <= 4 * blockDim): the counts, the counts
+// rounded up to 128 rows, and the tiles of 2^tile_shift rows they take.  Writes
+// out_x[0..n] (n+1 entries, the last one the total; n >= 1); out_pad and out_tiles may
+// be null.
+__device__ void block_scan3(const int *in_count, int n, int tile_shift, int *out_off, int *out_pad,
                             int *out_tiles, int *tmp /* 3 * 32 ints */) {
+  const int tile_round = (1 << tile_shift) - 1;
   const int per = (n + blockDim.x - 1) / blockDim.x;  // <= 4
   const int lo = threadIdx.x * per;
   int s0 = 0, s1 = 0, s2 = 0;
@@ -36,7 +38,7 @@ __device__ void block_scan3(const int *in_count, int n, int *out_off, int *out_p
       const int c = in_count[idx];
       s0 += c;
       s1 += (c + 127) & ~127;
-      s2 += (c + 127) >> 7;
+      s2 += (c + tile_round) >> tile_shift;
     }
   }
   // inclusive warp scan of the thread sums
@@ -89,7 +91,7 @@ __device__ void block_scan3(const int *in_count, int n, int *out_off, int *out_p
       const int c = in_count[idx];
       e0 += c;
       e1 += (c + 127) & ~127;
-      e2 += (c + 127) >> 7;
+      e2 += (c + tile_round) >> tile_shift;
     }
     if (idx == n - 1) {
       out_off[n] = e0;
@@ -148,7 +150,7 @@ __device__ void route_block(const int32_t *__restrict__ ids, int T, int topk, in
     }
     if (has_shared && threadIdx.x == 0) s_cnt[E] = T;
     __syncthreads();
-    block_scan3(s_cnt, G, s_off, s_pad, s_tiles, s_tmp);
+    block_scan3(s_cnt, G, rb.tile_shift, s_off, s_pad, s_tiles, s_tmp);
     __syncthreads();
     for (int g = threadIdx.x; g <= G; g += blockDim.x) {
       if (g < G) rb.counts[g] = s_cnt[g];
@@ -160,13 +162,16 @@ __device__ void route_block(const int32_t *__restrict__ ids, int T, int topk, in
       s_cursor[e] = s_off[e];
       s_delta[e] = s_pad[e] - s_off[e];
     }
-    // the GEMMs' tile schedule: one entry per 128-row tile of the permuted buffers
-    if (rb.tile_table)
+    // the GEMMs' tile schedule: one entry per tile of 2^tile_shift rows of each group's
+    // segment in the permuted buffers
+    if (rb.tile_table) {
+      const int tr = 1 << rb.tile_shift;
       for (int g = threadIdx.x; g < G; g += blockDim.x) {
         const int c = s_cnt[g], t0 = s_tiles[g], p0 = s_pad[g];
-        for (int mt = 0; mt * kBlockM < c; ++mt)
-          rb.tile_table[t0 + mt] = make_int4(g, mt, min(kBlockM, c - mt * kBlockM), p0 + mt * kBlockM);
+        for (int mt = 0; mt * tr < c; ++mt)
+          rb.tile_table[t0 + mt] = make_int4(g, mt, min(tr, c - mt * tr), p0 + mt * tr);
       }
+    }
     __syncthreads();
     // Hand out positions to the 32 entries starting at f0 (warp-uniform), taking
     // each expert's next position from slot[e] and advancing it.

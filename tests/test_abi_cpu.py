@@ -3,6 +3,7 @@ symbol, and rejects bad arguments on the host before touching a device."""
 
 import ctypes
 
+import numpy as np
 import pytest
 
 from nvfp4_block_scaled_quant_gb300 import _lib
@@ -91,7 +92,8 @@ def test_valid_call_without_a_gpu_fails_cleanly(L):
 
 
 @pytest.mark.parametrize("T,H,I,E,k,sh", [(16, 256, 128, 8, 2, 0), (16, 256, 128, 8, 2, 1), (1, 7168, 2048, 384, 8, 1),
-                                          (128, 7168, 2048, 384, 8, 1), (4096, 7168, 2048, 384, 8, 1), (0, 256, 64, 4, 1, 1)])
+                                          (128, 7168, 2048, 384, 8, 1), (4096, 7168, 2048, 384, 8, 1), (0, 256, 64, 4, 1, 1),
+                                          (8, 7168, 2048, 384, 8, 1), (32, 256, 64, 4, 8, 1), (33, 256, 64, 4, 8, 0)])
 def test_moe_workspace_layout(L, T, H, I, E, k, sh):
     lay = _lib.MoeWsLayout()
     assert L.nvfp4_moe_workspace_layout(T, H, I, E, k, sh, ctypes.byref(lay)) == 0
@@ -105,7 +107,17 @@ def test_moe_workspace_layout(L, T, H, I, E, k, sh):
     assert rc % 128 == 0
     # the padded segments always fit: sum_e roundup(c_e, 128) <= T*k + 127 * min(E, T*k), plus the shared rows
     assert rc >= T * k + (127 * min(E, T * k)) // 128 * 128 + (((T + 127) // 128) * 128 if sh else 0)
-    assert lay.amax_partials - lay.tile_table >= rc // 128 * 16   # one int32x4 entry per 128-row tile
+    # one int32x4 entry per m tile; tiles are 32 rows high up to T = 32, and a group of c rows
+    # takes ceil(c / 32) <= 4 ceil(c / 128) of them, so rc / 32 entries always suffice
+    assert lay.amax_partials - lay.tile_table >= rc // 32 * 16
+    R = 32 if T <= 32 else 128
+    rng = np.random.default_rng(T * 7 + k)
+    for ids in (rng.integers(0, E, (T, k)), np.zeros((T, k), np.int64), np.arange(T * k).reshape(T, k) % E):
+        c = np.bincount(ids.reshape(-1), minlength=E)
+        if sh:
+            c = np.append(c, T)
+        assert int(((c + 127) // 128 * 128).sum()) <= rc
+        assert int(((c + R - 1) // R).sum()) * 16 <= lay.amax_partials - lay.tile_table
     assert lay.xsf - lay.xq >= rc * H // 2 and lay.hq - lay.xsf >= O.sf_bytes(rc, H)
     assert lay.hsf - lay.hq >= rc * I // 2 and lay.y_acc - lay.hsf >= O.sf_bytes(rc, I)
     assert lay.total - lay.y_acc >= T * H * 4

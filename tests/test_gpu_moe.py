@@ -69,7 +69,8 @@ def run_moe_check(x, ids, w, W: ops.MoEWeights, oe, tokens, shared: bool, strict
     np.testing.assert_array_equal(counts, want_counts)
     np.testing.assert_array_equal(offsets, np.concatenate([[0], np.cumsum(want_counts)]))
     np.testing.assert_array_equal(pad, np.concatenate([[0], np.cumsum((want_counts + 127) // 128 * 128)]))
-    np.testing.assert_array_equal(tiles, np.concatenate([[0], np.cumsum((want_counts + 127) // 128)]))
+    R = 32 if T <= 32 else 128  # m-tile height: 32-row tiles up to 32 tokens
+    np.testing.assert_array_equal(tiles, np.concatenate([[0], np.cumsum((want_counts + R - 1) // R)]))
     np.testing.assert_array_equal(sorted_idx, ref.routing.sorted_idx)
     np.testing.assert_array_equal(inv_idx, ref.routing.inv_idx)
     dest_rows = _region(ws, L.dest_rows, T * k, torch.int32).cpu().numpy()
@@ -171,16 +172,39 @@ def test_moe_tiny_duplicates_and_skew():
     run_moe_check(x, ids, w, W, oe, list(range(0, T, 7)), True)
 
 
-@pytest.mark.parametrize("T", [1, 2, 3, 4, 5])
+@pytest.mark.parametrize("T", [1, 2, 3, 4, 5, 32, 33])
 def test_moe_small_batches_all_tokens(T):
-    """Decode-sized calls, all tokens: T*k <= 32 takes the GEMM ring with 4 small A stages (one
-    32-row box per tile); T = 5 (T*k = 40) the regular one."""
+    """Decode-sized calls, all tokens: up to 32 tokens the groups are cut into 32-row tiles and
+    the GEMMs take the ring with 4 small A stages (one 32-row box per tile); T = 33 the regular
+    one with 128-row tiles."""
     cfg = workloads.MoEConfig("small", T, 256, 128, 16, 8, True, "softmax", False)
     base = 109
     W = model.make_moe_weights(cfg.E, cfg.H, cfg.I, base, DEV, shared=True)
     oe = oracle_expert_fn(base, cfg.H, cfg.I, DEV)
     x = workloads.activations(T, cfg.H, seed=110 + T, device="cpu")
     ids, w = workloads.routing(cfg, seed=120 + T, device="cpu")
+    run_moe_check(x, ids, w, W, oe, list(range(T)), True)
+
+
+@pytest.mark.parametrize("T,E,k,mode", [(32, 4, 8, "random"), (20, 2, 8, "random"), (32, 1, 8, "same"),
+                                         (9, 2, 8, "random")])
+def test_moe_small_batch_duplicate_ids(T, E, k, mode):
+    """Up to 32 tokens, with ids repeated inside a token: a group then holds more than T rows and
+    spans several 32-row tiles, which start 32, 64 or 96 rows into a 128-row scale block (the
+    A scales are rotated into place) and run past the first block.  All tokens are checked."""
+    H, I = 256, 128
+    base = 131
+    W = model.make_moe_weights(E, H, I, base, DEV, shared=True)
+    oe = oracle_expert_fn(base, H, I, DEV)
+    x = workloads.activations(T, H, seed=132 + T, device="cpu")
+    rng = np.random.default_rng(133 + T * E)
+    if mode == "same":
+        ids = torch.zeros(T, k, dtype=torch.int32)
+    else:
+        ids = torch.from_numpy(rng.integers(0, E, (T, k)).astype(np.int32))
+    w = torch.softmax(torch.from_numpy(rng.standard_normal((T, k)).astype(np.float32)), -1).contiguous()
+    counts = np.bincount(ids.numpy().reshape(-1), minlength=E)
+    assert counts.max() > 32, "the case must put more than 32 rows in a group"
     run_moe_check(x, ids, w, W, oe, list(range(T)), True)
 
 
