@@ -55,7 +55,7 @@
 extern "C" {
 #endif
 
-#define NVFP4_ABI_VERSION 3
+#define NVFP4_ABI_VERSION 4
 
 /* Exported symbols: the library builds with hidden visibility by default. */
 #if defined(NVFP4_BUILD) && defined(__GNUC__)
@@ -276,13 +276,14 @@ typedef struct nvfp4_moe_ws_layout {
   size_t offsets;       /* int32 [G+1]      exclusive scan of counts                 */
   size_t pad_offsets;   /* int32 [G+1]      exclusive scan of counts rounded to 128  */
   size_t tile_offsets;  /* int32 [G+1]      exclusive scan of ceil(counts / R), R the
-                           m-tile height: 32 when T <= 32, else 128                 */
+                           m-tile height: 32 when T <= 128, else 128                */
   size_t sorted_idx;    /* int32 [T*topk]                                            */
   size_t inv_idx;       /* int32 [T*topk]                                            */
   size_t dest_rows;     /* int32 [T*topk]   permuted row of each flat entry (-1 dropped) */
   size_t tile_table;    /* int32x4 [rows_capacity/32] per R-row tile of the permuted
-                           buffers, in tile order: group, tile index inside the group,
-                           live rows (1..R), first permuted row                      */
+                           buffers, in tile order: group, tile index inside the group
+                           (bit 30 set when the group spans several tiles), live rows
+                           (1..R), first permuted row                                */
   size_t amax_partials; /* uint32 [1024]    block maxima of |x| as bf16 bits         */
   size_t xq;            /* uint8 [rows_capacity, H/2]  x quantised, permuted rows    */
   size_t xsf;           /* uint8 nvfp4_sf_bytes(rows_capacity, H)                    */

@@ -38,6 +38,7 @@ struct Tile {
   int nt;      // n tile
   int rows;    // live rows of this m tile (1..128)
   int a_row0;  // first A row (permuted/padded row index)
+  bool multi;  // the group spans several m tiles, which read the same weights
 };
 
 // Schedule entry of m tile mtg: group, m tile inside the group, live rows, first A row.
@@ -49,13 +50,15 @@ __device__ __forceinline__ int4 tile_entry(const GemmArgs &a, int mtg) {
   const int mt_per_group = (a.dense_M + kBlockM - 1) / kBlockM;
   const int g = mtg / mt_per_group;
   const int mt = mtg - g * mt_per_group;
-  return make_int4(g, mt, min(kBlockM, a.dense_M - mt * kBlockM), mt * kBlockM);
+  return make_int4(g, mt | (a.dense_M > kBlockM ? kTileMulti : 0), min(kBlockM, a.dense_M - mt * kBlockM),
+                   mt * kBlockM);
 }
 
 __device__ __forceinline__ Tile make_tile(const int4 e, int idx, int n_tiles) {
   Tile t;
   t.g = e.x;
-  t.mt = e.y;
+  t.mt = e.y & ~kTileMulti;
+  t.multi = (e.y & kTileMulti) != 0;
   t.rows = e.z;
   t.a_row0 = e.w;
   t.nt = idx - (idx / n_tiles) * n_tiles;
@@ -243,6 +246,9 @@ __global__ void __launch_bounds__(kGemmThreads, kQuantA ? 1 : kCtasPerSm)
         sfb = (sh ? args.b_sf_shared : args.b_sf + static_cast<size_t>(t.g) * args.N * (args.K / 16)) +
               static_cast<size_t>(t.nt) * k_steps * kSfBytesPerKStep;
       };
+      // Weights of a group whose other m tiles read them too stay in L2 (evict_normal);
+      // the weights of a single-tile group stream with evict_first.
+      auto weight_policy = [&](const Tile &t) { return t.multi ? pol_reuse : pol_stream; };
       // Weights of the first stages of this CTA's first tile, before the previous kernel ends.
       int early = 0;
       if (args.early_b) {
@@ -252,7 +258,7 @@ __global__ void __launch_bounds__(kGemmThreads, kQuantA ? 1 : kCtasPerSm)
           int b_row0;
           const uint8_t *sfb;
           b_src(t, mb, b_row0, sfb);
-          const uint64_t pol_w = (t.mt > 0 || t.rows == kBlockM) ? pol_reuse : pol_stream;
+          const uint64_t pol_w = weight_policy(t);
           early = min(S, k_stages);
           for (int s = 0; s < early; ++s) {
             const int kv = min(4, k_steps - 4 * s);
@@ -278,8 +284,7 @@ __global__ void __launch_bounds__(kGemmThreads, kQuantA ? 1 : kCtasPerSm)
         int b_row0;
         const uint8_t *sfb;
         b_src(t, mb, b_row0, sfb);
-        // weights of a group with further m tiles are read again by them
-        const uint64_t pol_w = (t.mt > 0 || t.rows == kBlockM) ? pol_reuse : pol_stream;
+        const uint64_t pol_w = weight_policy(t);
         const uint8_t *sfa =
             args.a_sf + (static_cast<size_t>(t.a_row0 / kBlockM) * args.a_kc_total +
                          static_cast<size_t>(t.g) * args.a_group_koff) * kSfBytesPerKStep;

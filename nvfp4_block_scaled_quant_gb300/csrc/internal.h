@@ -182,12 +182,19 @@ struct RouteBufs {
   int tile_shift;    // log2 of the tile height: moe_tile_rows(T)
 };
 
-// Height of the MoE GEMMs' m tiles.  Up to kABoxRows tokens the groups are cut into
-// kABoxRows-row tiles, so every tile fits one A box and the GEMMs take the small-A ring;
-// a group holds at most T rows unless a token lists an expert twice, and such a group
-// simply spans several tiles.  Larger batches use kBlockM-row tiles.
-inline int moe_tile_rows(int64_t T) { return T <= kABoxRows ? kABoxRows : kBlockM; }
-inline int moe_tile_shift(int64_t T) { return T <= kABoxRows ? 5 : 7; }
+// Height of the MoE GEMMs' m tiles.  Up to kSmallTileMaxT tokens (a decode batch or a
+// 128-token prefill chunk) the groups are cut into kABoxRows-row tiles, so every tile
+// fits one A box and the GEMMs take the small-A ring with its fourth stage.  Most groups
+// then hold one tile; the few with more rows (the shared expert, popular experts, or an
+// expert listed twice by a token) span several, which run concurrently and share their
+// weights through L2.  Larger batches, where popular experts hold thousands of rows,
+// use kBlockM-row tiles.
+constexpr int64_t kSmallTileMaxT = 128;
+// Flag in a tile-table entry's second field (tile index inside the group): the group
+// spans more than one tile.
+constexpr int kTileMulti = 1 << 30;
+inline int moe_tile_rows(int64_t T) { return T <= kSmallTileMaxT ? kABoxRows : kBlockM; }
+inline int moe_tile_shift(int64_t T) { return T <= kSmallTileMaxT ? 5 : 7; }
 static_assert((1 << 5) == kABoxRows && (1 << 7) == kBlockM, "tile shifts");
 cudaError_t launch_route_amax(const int32_t *ids, int T, int topk, int E, int has_shared,
                               RouteBufs rb, const void *x, int64_t H, uint32_t *partials,

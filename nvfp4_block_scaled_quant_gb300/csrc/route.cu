@@ -163,13 +163,15 @@ __device__ void route_block(const int32_t *__restrict__ ids, int T, int topk, in
       s_delta[e] = s_pad[e] - s_off[e];
     }
     // the GEMMs' tile schedule: one entry per tile of 2^tile_shift rows of each group's
-    // segment in the permuted buffers
+    // segment in the permuted buffers; kTileMulti marks the tiles of a group that spans
+    // several (they read the same weights)
     if (rb.tile_table) {
       const int tr = 1 << rb.tile_shift;
       for (int g = threadIdx.x; g < G; g += blockDim.x) {
         const int c = s_cnt[g], t0 = s_tiles[g], p0 = s_pad[g];
+        const int multi = c > tr ? kTileMulti : 0;
         for (int mt = 0; mt * tr < c; ++mt)
-          rb.tile_table[t0 + mt] = make_int4(g, mt, min(tr, c - mt * tr), p0 + mt * tr);
+          rb.tile_table[t0 + mt] = make_int4(g, mt | multi, min(tr, c - mt * tr), p0 + mt * tr);
       }
     }
     __syncthreads();

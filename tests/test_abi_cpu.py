@@ -107,10 +107,10 @@ def test_moe_workspace_layout(L, T, H, I, E, k, sh):
     assert rc % 128 == 0
     # the padded segments always fit: sum_e roundup(c_e, 128) <= T*k + 127 * min(E, T*k), plus the shared rows
     assert rc >= T * k + (127 * min(E, T * k)) // 128 * 128 + (((T + 127) // 128) * 128 if sh else 0)
-    # one int32x4 entry per m tile; tiles are 32 rows high up to T = 32, and a group of c rows
+    # one int32x4 entry per m tile; tiles are 32 rows high up to T = 128, and a group of c rows
     # takes ceil(c / 32) <= 4 ceil(c / 128) of them, so rc / 32 entries always suffice
     assert lay.amax_partials - lay.tile_table >= rc // 32 * 16
-    R = 32 if T <= 32 else 128
+    R = 32 if T <= 128 else 128
     rng = np.random.default_rng(T * 7 + k)
     for ids in (rng.integers(0, E, (T, k)), np.zeros((T, k), np.int64), np.arange(T * k).reshape(T, k) % E):
         c = np.bincount(ids.reshape(-1), minlength=E)

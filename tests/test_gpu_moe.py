@@ -69,8 +69,14 @@ def run_moe_check(x, ids, w, W: ops.MoEWeights, oe, tokens, shared: bool, strict
     np.testing.assert_array_equal(counts, want_counts)
     np.testing.assert_array_equal(offsets, np.concatenate([[0], np.cumsum(want_counts)]))
     np.testing.assert_array_equal(pad, np.concatenate([[0], np.cumsum((want_counts + 127) // 128 * 128)]))
-    R = 32 if T <= 32 else 128  # m-tile height: 32-row tiles up to 32 tokens
+    R = 32 if T <= 128 else 128  # m-tile height: 32-row tiles up to 128 tokens
     np.testing.assert_array_equal(tiles, np.concatenate([[0], np.cumsum((want_counts + R - 1) // R)]))
+    # the GEMMs' schedule: per tile (group, tile in group | bit 30 when the group spans several
+    # tiles, live rows, first permuted row)
+    table = _region(ws, L.tile_table, 4 * int(tiles[-1]), torch.int32).view(-1, 4).cpu().numpy()
+    want_table = [(g, mt | ((1 << 30) if c > R else 0), min(R, c - mt * R), int(pad[g]) + mt * R)
+                  for g, c in enumerate(want_counts.tolist()) for mt in range((c + R - 1) // R)]
+    np.testing.assert_array_equal(table, np.array(want_table, dtype=np.int64).reshape(-1, 4))
     np.testing.assert_array_equal(sorted_idx, ref.routing.sorted_idx)
     np.testing.assert_array_equal(inv_idx, ref.routing.inv_idx)
     dest_rows = _region(ws, L.dest_rows, T * k, torch.int32).cpu().numpy()
@@ -172,11 +178,12 @@ def test_moe_tiny_duplicates_and_skew():
     run_moe_check(x, ids, w, W, oe, list(range(0, T, 7)), True)
 
 
-@pytest.mark.parametrize("T", [1, 2, 3, 4, 5, 32, 33])
+@pytest.mark.parametrize("T", [1, 2, 3, 4, 5, 33, 128, 129])
 def test_moe_small_batches_all_tokens(T):
-    """Decode-sized calls, all tokens: up to 32 tokens the groups are cut into 32-row tiles and
-    the GEMMs take the ring with 4 small A stages (one 32-row box per tile); T = 33 the regular
-    one with 128-row tiles."""
+    """Small calls, all tokens: up to 128 tokens the groups are cut into 32-row tiles and the
+    GEMMs take the ring with 4 small A stages (one 32-row box per tile); at T = 128 the 16
+    experts hold about 64 rows each and the shared one 128, so their tiles start 32, 64 and
+    96 rows into a scale block.  T = 129 takes 128-row tiles and the regular ring."""
     cfg = workloads.MoEConfig("small", T, 256, 128, 16, 8, True, "softmax", False)
     base = 109
     W = model.make_moe_weights(cfg.E, cfg.H, cfg.I, base, DEV, shared=True)
