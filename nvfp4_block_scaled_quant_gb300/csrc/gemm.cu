@@ -452,8 +452,9 @@ __global__ void __launch_bounds__(kGemmThreads, kQuantA ? 1 : kCtasPerSm)
           ra[4 * j] = wa.x, ra[4 * j + 1] = wa.y, ra[4 * j + 2] = wa.z, ra[4 * j + 3] = wa.w;
           rb[4 * j] = wb.x, rb[4 * j + 1] = wb.y, rb[4 * j + 2] = wb.z, rb[4 * j + 3] = wb.w;
         }
-        // Warp-uniform and rare: only a group of more than 32 rows (an expert listed twice
-        // by a token) has small-A tiles that do not start a scale block.
+        // Warp-uniform and taken by few tiles: only a group of more than 32 rows (the shared
+        // expert above 32 tokens, a popular expert, an expert listed twice by a token) has
+        // small-A tiles that do not start a scale block.
         if (kRotA && __builtin_expect(sfa_rot != 0, 0)) {
 #pragma unroll
           for (int j = 0; j < 4; ++j) {

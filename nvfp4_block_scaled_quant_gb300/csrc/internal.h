@@ -89,10 +89,10 @@ struct GemmArgs {
   const int *offsets;       // [G+1] unpadded (sorted order)
   const int *pad_offsets;   // [G+1]
   const int *tile_offsets;  // [G+1]
-  const int4 *tile_table;   // per m tile in tile order: group, m tile in group, live rows,
-                            // first A row (written by the routing kernel; the tiles are
-                            // kABoxRows high in the small-A ring, else kBlockM); null: every
-                            // group has dense_M rows
+  const int4 *tile_table;   // per m tile in tile order: group, m tile in group (| kTileMulti
+                            // when the group spans several), live rows, first A row (written
+                            // by the routing kernel; the tiles are kABoxRows high in the
+                            // small-A ring, else kBlockM); null: every group has dense_M rows
   int shared_group;         // group using the *_shared weights, or -1
   // scale factors
   const uint8_t *a_sf;      // swizzled, 128-row blocks aligned with the A rows
@@ -178,7 +178,7 @@ cudaError_t launch_prepare(const uint8_t *w, const uint8_t *sf, int64_t G, int64
 
 struct RouteBufs {
   int *counts, *offsets, *pad_offsets, *tile_offsets, *sorted_idx, *inv_idx, *dest_rows;
-  int4 *tile_table;  // per tile: group, tile in group, live rows, first row (or null)
+  int4 *tile_table;  // per tile: group, tile in group | kTileMulti, live rows, first row (or null)
   int tile_shift;    // log2 of the tile height: moe_tile_rows(T)
 };
 
