@@ -21,6 +21,7 @@ import re
 import statistics
 import subprocess
 import sys
+import tempfile
 import time
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
@@ -95,7 +96,9 @@ class ClockSampler:
     def __init__(self, index: int):
         self.index = index
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_gpu{index}.csv")
+        # the raw samples go to NVFP4_BENCH_LOG_DIR when set (kept), else to the temp directory
+        out_dir = os.environ.get("NVFP4_BENCH_LOG_DIR") or tempfile.gettempdir()
+        self.path = os.path.join(out_dir, f"nvfp4_clocks_gpu{index}_{os.getpid()}.csv")
 
     def start(self):
         os.makedirs(os.path.dirname(self.path), exist_ok=True)
