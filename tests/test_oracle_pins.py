@@ -212,6 +212,23 @@ def test_sf_layout_is_a_padded_bijection(rows, K):
     assert not buf[pad].any()
 
 
+def test_sf_layout_32_row_slices_fill_one_word_per_chunk():
+    """A 32-row slice starting 32 j rows into a 128-row block owns 32-bit word j of every one
+    of the block's 32 sixteen-byte chunks, one chunk per row (what a 32-row GEMM tile's scale
+    staging relies on when it moves word j into place)."""
+    rows, K = 256, 512
+    off = O.sf_swizzle_offsets(rows, K)
+    for b in range(rows // 128):
+        for j in range(4):
+            sl = off[128 * b + 32 * j:128 * b + 32 * (j + 1), :]
+            for q in range(sl.shape[1] // 4):  # each 512-byte block of 4 scale columns
+                blk = sl[:, 4 * q:4 * q + 4]
+                assert len(set((blk // 512).ravel().tolist())) == 1
+                assert set(((blk % 16) // 4).ravel().tolist()) == {j}
+                chunks = (blk[:, 0] % 512) // 16
+                assert sorted(chunks.tolist()) == list(range(32))
+
+
 # --------------------------------------------------------------------------- linear
 
 def _frac_f32(v):
