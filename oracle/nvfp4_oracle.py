@@ -440,10 +440,18 @@ class MoEResult:
     rows: Dict[tuple, ExpertResult]  # (token, slot) -> per-row result; slot -1 = shared
 
 
+def _expert_job(job) -> ExpertResult:
+    """One expert's share of the MoE: ``job`` = (expert or expert source, expert id, the
+    quantised rows routed to it, its static a2 scale).  Module level so a process pool can run it."""
+    src, e, xq_rows, a2 = job
+    ex = src if isinstance(src, Expert) else src(e)
+    return expert_forward(xq_rows, ex, a2)
+
+
 def moe_forward(x: np.ndarray, ids: np.ndarray, topk_w: np.ndarray,
                 experts: Callable[[int], Expert], E: int, a2_gs: Sequence[float],
                 shared: Optional[Expert] = None, a1_gs: Optional[float] = None,
-                tokens: Optional[Sequence[int]] = None) -> MoEResult:
+                tokens: Optional[Sequence[int]] = None, mapper=map) -> MoEResult:
     """Routed MoE with an optional always-active shared expert.
 
     For each token t and slot j with e = ids[t, j]:
@@ -453,6 +461,12 @@ def moe_forward(x: np.ndarray, ids: np.ndarray, topk_w: np.ndarray,
     of h uses the static per-expert scale a2_gs[e] (a2_gs[E] for the shared
     expert).  ``tokens`` restricts the output rows computed (all by default);
     the global scale and routing always cover all T tokens.
+
+    The rows routed to one expert go through that expert together (its weights
+    are dequantised once); every row's result is the same per-row definition.
+    ``mapper`` (the builtin ``map`` by default, or a process pool's ``imap``)
+    runs the per-expert jobs; ``experts`` must then be picklable.  Each token's
+    sum is taken in slot order, then the shared expert.
     """
     x = np.asarray(x, dtype=np.float32)
     T, H = x.shape
@@ -460,22 +474,30 @@ def moe_forward(x: np.ndarray, ids: np.ndarray, topk_w: np.ndarray,
     xq = quantize(x, gs=a1_gs)
     routing = route(ids, E)
     toks = list(range(T)) if tokens is None else [int(t) for t in tokens]
-    y = np.zeros((len(toks), H), dtype=np.float64)
-    rows: Dict[tuple, ExpertResult] = {}
-    cache: Dict[int, Expert] = {}
-    for i, t in enumerate(toks):
-        xr = Quantized(xq.codes[t:t + 1], xq.sf[t:t + 1], xq.gs)
+    slots_of: Dict[int, list] = {}
+    for t in toks:
         for j in range(k):
-            e = int(ids[t, j])
-            if e not in cache:
-                cache[e] = experts(e)
-            res = expert_forward(xr, cache[e], a2_gs[e])
-            rows[(t, j)] = res
-            y[i] += float(topk_w[t, j]) * res.o[0]
+            slots_of.setdefault(int(ids[t, j]), []).append((t, j))
+    jobs = [(experts, e, slots_of[e]) for e in sorted(slots_of)]
+    if shared is not None:
+        jobs.append((shared, E, [(t, -1) for t in toks]))
+
+    def payload(job):
+        src, e, slots = job
+        ts = [t for t, _ in slots]
+        return src, e, Quantized(xq.codes[ts], xq.sf[ts], xq.gs), a2_gs[e]
+
+    rows: Dict[tuple, ExpertResult] = {}
+    for (_, _, slots), res in zip(jobs, mapper(_expert_job, [payload(jb) for jb in jobs])):
+        for r, s in enumerate(slots):
+            rows[s] = ExpertResult(res.h[r:r + 1], Quantized(res.hq.codes[r:r + 1], res.hq.sf[r:r + 1], res.hq.gs),
+                                   res.o[r:r + 1])
+    y = np.zeros((len(toks), H), dtype=np.float64)
+    for i, t in enumerate(toks):
+        for j in range(k):
+            y[i] += float(topk_w[t, j]) * rows[(t, j)].o[0]
         if shared is not None:
-            res = expert_forward(xr, shared, a2_gs[E])
-            rows[(t, -1)] = res
-            y[i] += res.o[0]
+            y[i] += rows[(t, -1)].o[0]
     return MoEResult(y, xq, routing, rows)
 
 

@@ -337,6 +337,43 @@ def test_router_weight_fp8_roundtrip_precision(golden):
     np.testing.assert_array_equal(O.bf16_bits_to_f32(O.f32_to_bf16_bits(wg.astype(np.float32))), wg)  # bf16 values
 
 
+def _router_weight_by_library_casts(codes, sf, ws2, e2m1_table, bf16_before_fp8=True):
+    """The gate weight's dequantise -> FP8-E4M3 round trip built from torch's own casts: the OCP
+    E2M1 table (golden), torch's float8_e4m3fn decode of the scales, fp32 products, torch's bf16
+    cast, fp32 amax / 448 and reciprocal, torch's float8_e4m3fn cast, and a final bf16 cast."""
+    vals = torch.tensor([float(e2m1_table[str(c)]) for c in range(16)], dtype=torch.float32)
+    scale = torch.from_numpy(np.repeat(sf, 16, axis=1)[:, : codes.shape[1]].copy()).view(torch.float8_e4m3fn).float()
+    w = (vals[torch.from_numpy(codes.astype(np.int64))] * scale) * torch.tensor(ws2, dtype=torch.float32)
+    if bf16_before_fp8:
+        w = w.to(torch.bfloat16).float()
+    s = w.abs().max() / torch.tensor(448.0, dtype=torch.float32)
+    q = (w * (torch.tensor(1.0, dtype=torch.float32) / s)).to(torch.float8_e4m3fn)
+    return q.view(torch.uint8).numpy(), (q.float() * s).to(torch.bfloat16).float().numpy()
+
+
+def test_router_weight_against_library_casts(golden):
+    """router_weight equals the same chain spelled with library casts, element for element, on a
+    random gate and on a hand-picked one where the bf16 rounding ahead of the FP8 step changes
+    FP8 codes (page 1, the router-gate FP8 round trip: NVFP4 dequantised to bf16 first)."""
+    table = golden("e2m1_values.json")["codes_to_values"]
+    rng = np.random.default_rng(17)
+    wq = O.quantize((rng.standard_normal((64, 1024)) * 0.02).astype(np.float32))
+    _, want = _router_weight_by_library_casts(wq.codes, wq.sf, wq.gs, table)
+    np.testing.assert_array_equal(O.router_weight(wq.codes, wq.sf, wq.gs), want)
+    # two 16-element blocks with different scales: without the bf16 rounding, codes 7, 12 and 13
+    # of the FP8 tensor come out one step higher
+    codes = np.array([[8, 4, 4, 0, 1, 0, 2, 13, 10, 14, 8, 9, 15, 11, 10, 8,
+                       8, 14, 4, 13, 10, 0, 6, 13, 8, 0, 12, 11, 13, 2, 1, 13]], dtype=np.uint8)
+    sf = np.array([[41, 86]], dtype=np.uint8)
+    ws2 = np.float32(float.fromhex("0x1.a3d184p-8"))
+    q_bf16, want = _router_weight_by_library_casts(codes, sf, ws2, table)
+    q_plain, plain = _router_weight_by_library_casts(codes, sf, ws2, table, bf16_before_fp8=False)
+    assert (q_bf16 != q_plain).sum() == 3
+    got = O.router_weight(codes, sf, ws2)
+    np.testing.assert_array_equal(got, want)
+    assert not np.array_equal(got, plain)
+
+
 def test_router_topk_against_library():
     rng = np.random.default_rng(16)
     x = rng.standard_normal((40, 64))
@@ -449,5 +486,10 @@ def test_moe_token_permutation_equivariance():
     base = O.moe_forward(x, ids, w, lambda e: exps[e], E, a2)
     perm = O.moe_forward(x[p], ids[p], w[p], lambda e: exps[e], E, a2)
     np.testing.assert_allclose(perm.y, base.y[p], rtol=1e-13, atol=1e-16)
+    # a subset of tokens gives the same rows (the global scale and routing still cover all
+    # tokens); only the fp64 summation order of the batched library matmul may differ
     sub = O.moe_forward(x, ids, w, lambda e: exps[e], E, a2, tokens=[4, 1])
-    np.testing.assert_allclose(sub.y, base.y[[4, 1]], rtol=0, atol=0)
+    np.testing.assert_allclose(sub.y, base.y[[4, 1]], rtol=1e-13, atol=1e-18)
+    # per-expert jobs through another mapper (as a process pool runs them) give the same result
+    mapped = O.moe_forward(x, ids, w, lambda e: exps[e], E, a2, mapper=lambda f, jobs: [f(j) for j in jobs[::-1]][::-1])
+    np.testing.assert_array_equal(mapped.y, base.y)
