@@ -86,16 +86,42 @@ def test_linear_static_gs_and_empty():
     assert y0.shape == (0, N)
 
 
-@pytest.mark.parametrize("M", [1024])
-def test_gemm_sweep_sampled_rows(M):
-    """Large GEMM (K = N = 7168): full GPU run; the oracle checks a seeded sample of rows."""
+@pytest.fixture(scope="module")
+def sweep_weight():
+    """The 7168 x 7168 weight of the large-GEMM sweep, library- and oracle-side."""
+    _, K, N = workloads.DENSE_GEMM[1024]
+    return _weights(N, K, seed=31)
+
+
+def _sweep_rows(M: int, n: int) -> np.ndarray:
+    """n seeded rows, always including the first and the last."""
+    rows = set(np.random.default_rng(M).choice(M, n - 2, replace=False).tolist()) | {0, M - 1}
+    rng = np.random.default_rng(M + 1)
+    while len(rows) < n:
+        rows.add(int(rng.integers(0, M)))
+    return np.array(sorted(rows))
+
+
+@pytest.mark.parametrize("M,n_rows", [(1024, 48), (4096, 32), (16384, 32)])
+def test_gemm_sweep_sampled_rows(sweep_weight, M, n_rows):
+    """Large GEMM (K = N = 7168) at the sweep's sizes, in the benchmark's launch configuration:
+    the full GPU run through nvfp4_gemm (on quantised activations) and through nvfp4_linear
+    (quantisation included); the oracle checks every column of seeded rows.  The global scale
+    covers all M rows on both sides."""
+    wp, sfp, ws2, wq = sweep_weight
     _, K, N = workloads.DENSE_GEMM[M]
     x = workloads.activations(M, K, seed=30 + M, device="cpu")
-    wp, sfp, ws2, wq = _weights(N, K, seed=31)
-    q, sf, gs = ops.quantize_act(x.to(DEV))
+    xd = x.to(DEV)
+    q, sf, gs = ops.quantize_act(xd)
     y = ops.gemm(q, sf, gs, K, wp, sfp, ws2, N)
+    y_lin, gs_lin = ops.linear(xd, wp, sfp, ws2, N)
     torch.cuda.synchronize()
-    xq = O.quantize(x.float().numpy())
-    rows = np.sort(np.random.default_rng(M).choice(M, 48, replace=False))
-    sub = O.Quantized(xq.codes[rows], xq.sf[rows], xq.gs)
-    assert_parity(bf16_to_np(y)[rows], O.linear(sub, wq.codes, wq.sf, wq.gs), what=f"gemm M={M}")
+    assert ops.device_error() == (0, 0)
+    xf = x.float().numpy()
+    g = O.global_scale(xf)
+    assert gs.item() == float(g) and gs_lin.item() == float(g)
+    rows = _sweep_rows(M, n_rows)
+    sub = O.quantize(xf[rows], gs=g)
+    ref = O.linear(sub, wq.codes, wq.sf, wq.gs)
+    assert_parity(bf16_to_np(y)[rows], ref, what=f"gemm M={M}")
+    assert_parity(bf16_to_np(y_lin)[rows], ref, what=f"linear M={M}")

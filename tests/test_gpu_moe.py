@@ -20,7 +20,7 @@ import torch
 
 from nvfp4_block_scaled_quant_gb300 import model, ops, workloads
 from oracle import nvfp4_oracle as O
-from tests.helpers import assert_parity, bf16_to_np, oracle_expert_fn
+from tests.helpers import assert_parity, bf16_to_np, oracle_expert_fn, oracle_pool
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
@@ -38,15 +38,21 @@ def calibrate_a2(res: O.MoEResult, E: int) -> np.ndarray:
     return np.full(E + 1, F32(F32(amax) / F32(2688.0)), dtype=np.float32)
 
 
-def run_moe_check(x, ids, w, W: ops.MoEWeights, oe, tokens, shared: bool, strict_all=False):
+def run_moe_check(x, ids, w, W: ops.MoEWeights, oe, tokens, shared: bool, strict_all=False, mapper=map,
+                  calib_tokens=None):
+    """Stage-by-stage check of the tokens listed.  The static scale of h is calibrated on
+    ``calib_tokens`` (default: the tokens checked); rows of other tokens whose h exceeds it
+    saturate their E4M3 scale identically on both sides.  ``mapper`` runs the oracle's
+    per-expert jobs (a process pool's imap for the full-size workloads)."""
     T, H = x.shape
     k = ids.shape[1]
     E, I = W.E, W.I
     xnp, idsnp, wnp = x.float().numpy(), ids.numpy(), w.numpy()
     sh = oe(E) if shared else None
-    cal = O.moe_forward(xnp, idsnp, wnp, oe, E, np.ones(E + 1, F32), shared=sh, tokens=tokens)
+    cal = O.moe_forward(xnp, idsnp, wnp, oe, E, np.ones(E + 1, F32), shared=sh,
+                        tokens=tokens if calib_tokens is None else calib_tokens, mapper=mapper)
     a2 = calibrate_a2(cal, E)
-    ref = O.moe_forward(xnp, idsnp, wnp, oe, E, a2, shared=sh, tokens=tokens)
+    ref = O.moe_forward(xnp, idsnp, wnp, oe, E, a2, shared=sh, tokens=tokens, mapper=mapper)
 
     xd, idsd, wd, a2d = x.to(DEV), ids.to(DEV), w.to(DEV), torch.from_numpy(a2).to(DEV)
     L = ops.moe_workspace_layout(T, H, I, E, k, shared)
@@ -261,30 +267,84 @@ def big_weights():
     torch.cuda.empty_cache()
 
 
+@pytest.fixture(scope="module")
+def oracle_map():
+    """The oracle's per-expert jobs of the full-size workloads run in a spawned process pool."""
+    pool = oracle_pool()
+
+    def mapper(fn, jobs):
+        it = pool.imap(fn, jobs, chunksize=1)
+        for _ in range(len(jobs)):
+            yield it.next(timeout=900)  # a worker that cannot start fails the test, not hangs it
+
+    yield mapper
+    pool.terminate()
+    pool.join()
+
+
+def segment_rows(ids: np.ndarray, e: int) -> np.ndarray:
+    """Tokens of expert e's routed rows in segment order (the routing is stable by flat index)."""
+    k = ids.shape[1]
+    return np.nonzero(ids.reshape(-1) == e)[0] // k
+
+
+def chunk_tokens(ids: np.ndarray, n: int, seed: int, R: int = 32) -> list:
+    """At least n tokens of a 128-token chunk that reach every kind of m tile: one token in each
+    R-row tile of the shared expert (its row i is token i), the last row of every tile of the two
+    most popular experts (groups of several tiles, later ones with rotated A scales), a token of a
+    one-row group; seeded others fill up to n."""
+    T = ids.shape[0]
+    counts = np.bincount(ids.reshape(-1), minlength=int(ids.max()) + 1)
+    chosen = {tile * R + (7 * tile + 3) % R for tile in range(T // R)}
+    hot = np.argsort(-counts, kind="stable")[:2]
+    assert counts[hot[0]] > R, "the chunk must hold a group of several tiles"
+    for e in hot:
+        toks = segment_rows(ids, int(e))
+        chosen.update(int(toks[min(len(toks) - 1, t * R + R - 1)]) for t in range((len(toks) + R - 1) // R))
+    single = np.nonzero(counts == 1)[0]
+    assert len(single), "the chunk must hold a one-row group"
+    chosen.add(int(segment_rows(ids, int(single[0]))[0]))
+    rng = np.random.default_rng(seed)
+    while len(chosen) < n:
+        chosen.add(int(rng.integers(0, T)))
+    return sorted(chosen)
+
+
 @pytest.mark.parametrize("T", [1, 8, 64])
-def test_moe_decode_sampled(big_weights, T):
+def test_moe_decode_all_tokens(big_weights, oracle_map, T):
+    """The decode batches of the 384-expert layer (32-row tiles, the small-A ring), every token."""
     W, oe = big_weights
     x, ids, w = workloads.decode_step(T, device="cpu")
-    tokens = [0] if T == 1 else [0, T - 1]
-    run_moe_check(x, ids, w, W, oe, tokens, True)
+    run_moe_check(x, ids, w, W, oe, list(range(T)), True, mapper=oracle_map, calib_tokens=[0])
 
 
 @pytest.mark.parametrize("chunk", [0, 31])
-def test_moe_prefill_bench_chunk_sampled(big_weights, chunk):
+def test_moe_prefill_bench_chunk_tiles(big_weights, oracle_map, chunk):
+    """Prefill chunks of the benchmark (its seeds and weights): 16+ tokens covering every 32-row
+    tile of the shared expert, every tile of the two most popular experts and a one-row group."""
     W, oe = big_weights
     x, ids, w = workloads.prefill_chunk(chunk, device="cpu")
-    run_moe_check(x, ids, w, W, oe, [3, 127], True)
+    tokens = chunk_tokens(ids.numpy(), 16, seed=chunk)
+    assert len(tokens) >= 16
+    run_moe_check(x, ids, w, W, oe, tokens, True, mapper=oracle_map, calib_tokens=tokens[:2])
 
 
-def test_moe_prefill_whole_4096_sampled(big_weights):
-    """4096 tokens in one call: hot experts span many m tiles (their weights are re-read from L2)."""
+def test_moe_prefill_whole_4096_hot_experts(big_weights, oracle_map):
+    """4096 tokens in one call (128-row tiles; the hottest experts span many m tiles and re-read
+    their weights from L2): the last row of each of the three hottest experts, the first and last
+    token and seeded others."""
     W, oe = big_weights
     x, ids, w = workloads.prefill_whole(device="cpu")
-    counts = np.bincount(ids.numpy().ravel(), minlength=384)
+    idn = ids.numpy()
+    counts = np.bincount(idn.ravel(), minlength=384)
     assert counts.max() > 1000  # the hottest expert spans 8+ m tiles
-    hot = int(np.argmax(counts))
-    tok_hot = int(np.nonzero((ids.numpy() == hot).any(axis=1))[0][-1])  # last row of the hottest expert
-    run_moe_check(x, ids, w, W, oe, [0, tok_hot], True)
+    hot = np.argsort(-counts, kind="stable")[:3]
+    tokens = {0, x.shape[0] - 1} | {int(segment_rows(idn, int(e))[-1]) for e in hot}
+    rng = np.random.default_rng(4096)
+    while len(tokens) < 8:
+        tokens.add(int(rng.integers(0, x.shape[0])))
+    tokens = sorted(tokens)
+    run_moe_check(x, ids, w, W, oe, tokens, True, mapper=oracle_map, calib_tokens=tokens[:2])
 
 
 def test_moe_forward_cuda_graph_replay():

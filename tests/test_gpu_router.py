@@ -2,7 +2,7 @@
 
 The prepared gate weight (NVFP4 -> bf16 -> FP8-E4M3 round trip -> bf16) is bit-exact; logits
 meet the GEMM bound; ids match exactly for every token whose oracle probabilities are separated
-by more than 1e-4 (relative) around the top-k boundary and between chosen experts, and the
+by more than 1e-5 (relative) around the top-k boundary and between chosen experts, and the
 renormalised weights agree to 1e-4.  The router's output also drives the routed MoE end to end.
 """
 
@@ -35,10 +35,12 @@ def _check_router(x, wg, wg_ref, k):
     rid, rw, p = O.router(x.float().numpy(), wg_ref, k)
     lref = x.float().numpy().astype(np.float64) @ wg_ref.astype(np.float64).T
     assert_parity(logits.cpu().numpy(), lref, what="router logits")
+    # fp32 logits over H terms are accurate to ~1e-6 relative; a token is "clear" when its top-k+1
+    # probabilities are 1e-5 (relative) apart, and at most 1% of the tokens (rounded down) may not be
     ps = -np.sort(-p, axis=1)[:, : k + 1]
     gaps = (ps[:, :-1] - ps[:, 1:]) / ps[:, :-1]
-    clear = (gaps > 1e-4).all(axis=1)
-    assert clear.mean() > 0.9
+    clear = (gaps > 1e-5).all(axis=1)
+    assert clear.sum() >= int(np.floor(0.99 * len(clear))), f"{(~clear).sum()} of {len(clear)} tokens not clear"
     np.testing.assert_array_equal(ids.cpu().numpy()[clear], rid[clear])
     np.testing.assert_allclose(w.cpu().numpy()[clear], rw[clear], rtol=1e-4, atol=1e-7)
     np.testing.assert_allclose(w.cpu().numpy().sum(1), 1.0, rtol=1e-5)
