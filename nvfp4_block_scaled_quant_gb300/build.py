@@ -19,7 +19,7 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libnvfp4_gb300.so")
-SOURCES = ["abi.cu", "quant.cu", "route.cu", "gemm.cu", "norm.cu", "router.cu"]
+SOURCES = ["abi.cu", "quant.cu", "route.cu", "gemm.cu", "gemm_pair.cu", "norm.cu", "router.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",
          "--expt-relaxed-constexpr", f"-I{os.path.join(ROOT, 'include')}", "-DNVFP4_BUILD"]

@@ -485,8 +485,10 @@ static nvfp4_status gemm_dense(const char *fn, DeviceInfo *d, const uint8_t *xq,
                                int64_t M, int64_t K, int64_t N, const uint8_t *w, const uint8_t *w_sf,
                                const float *ws2, void *y, cudaStream_t s, int early_b = 0, int64_t G = 1) {
   if (M == 0) return NVFP4_OK;
+  // many rows and N a multiple of 256: 256 x 256 tiles on CTA pairs
+  const int pair_clusters = (G == 1 && N % 256 == 0 && M >= kPairMinM) ? gemm_pair_max_clusters() : 0;
   CUtensorMap ta, tb;
-  nvfp4_status st = make_map(fn, &ta, xq, G * K / 2, M, G * K / 2, kABoxRows);
+  nvfp4_status st = make_map(fn, &ta, xq, G * K / 2, M, G * K / 2, pair_clusters > 0 ? 128 : kABoxRows);
   if (st != NVFP4_OK) return st;
   if ((st = make_map(fn, &tb, w, K / 2, G * N, K / 2, kBlockN)) != NVFP4_OK) return st;
   GemmArgs a;
@@ -507,6 +509,12 @@ static nvfp4_status gemm_dense(const char *fn, DeviceInfo *d, const uint8_t *xq,
   a.out_group_cols = static_cast<int>(N);
   a.err = d->flags;
   a.early_b = early_b;
+  if (pair_clusters > 0) {
+    const int64_t pair_tiles = ((M + 255) / 256) * (N / 256);
+    const int clusters = static_cast<int>(pair_tiles < pair_clusters ? pair_tiles : pair_clusters);
+    NV_CUDA(launch_gemm_pair(ta, tb, a, clusters, s), "pair GEMM launch");
+    return NVFP4_OK;
+  }
   const int64_t tiles = G * ((M + kBlockM - 1) / kBlockM) * (N / kBlockN);
   const int grid = static_cast<int>(tiles < d->sms * kCtasPerSm ? tiles : d->sms * kCtasPerSm);
   // M <= 32: every tile has at most one 32-row A box, so the ring with 4 small stages applies

@@ -212,6 +212,13 @@ cudaError_t launch_gemm(Epi epi, const CUtensorMap &ta, const CUtensorMap &tb,
 // Dense or fixed-group linear with the activation quantisation fused (kQuantA): 1 <= M <= 32,
 // K <= kQuantMaxK, grid = tiles <= SM count (one tile per CTA).
 cudaError_t launch_gemm_quant_a(const CUtensorMap &tb, const GemmArgs &args, int grid, cudaStream_t s);
+// Dense GEMM on CTA pairs (256 x 256 tiles, tcgen05 cta_group::2): N % 256 == 0, A read
+// through a tensor map with 128-row boxes.  gemm_pair_max_clusters: clusters of 2 that fit
+// on the current device at once (0 if the query fails).
+constexpr int64_t kPairMinM = 512;   // fewer rows: the one-SM tiles spread over more SMs
+int gemm_pair_max_clusters();
+cudaError_t launch_gemm_pair(const CUtensorMap &ta, const CUtensorMap &tb, const GemmArgs &args, int clusters,
+                             cudaStream_t s);
 cudaError_t launch_wait_timeout_probe(uint32_t timeout_us, uint32_t *err, cudaStream_t s);
 
 }  // namespace nvfp4

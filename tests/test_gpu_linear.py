@@ -36,6 +36,28 @@ def test_linear_ragged_shapes(M, K, N):
     assert_parity(bf16_to_np(y), O.linear(xq, wq.codes, wq.sf, wq.gs), what=f"linear {M}x{K}x{N}")
 
 
+@pytest.mark.parametrize("M,K,N", [(512, 256, 256), (700, 320, 512), (640, 1536, 768), (1000, 64, 256),
+                                   (1300, 7168, 512), (2049, 512, 1024)])
+def test_linear_pair_tiles_ragged(M, K, N):
+    """Shapes of the CTA-pair path (M >= 512, N % 256 == 0, 256 x 256 tiles): M not a multiple
+    of 256 (a last tile whose second half starts past the padded scale rows at M = 640 and
+    M = 2049), K with a short last stage (K = 320, 64), every output checked, through
+    nvfp4_linear and nvfp4_gemm."""
+    x = workloads.activations(M, K, seed=M + 3 * K + N, device="cpu", outliers=True)
+    wp, sfp, ws2, wq = _weights(N, K, seed=M + N)
+    xd = x.to(DEV)
+    y, gs = ops.linear(xd, wp, sfp, ws2, N)
+    q, sf, gq = ops.quantize_act(xd)
+    y2 = ops.gemm(q, sf, gq, K, wp, sfp, ws2, N)
+    torch.cuda.synchronize()
+    assert ops.device_error() == (0, 0)
+    xq = O.quantize(x.float().numpy())
+    assert gs.item() == float(xq.gs)
+    ref = O.linear(xq, wq.codes, wq.sf, wq.gs)
+    assert_parity(bf16_to_np(y), ref, what=f"pair linear {M}x{K}x{N}")
+    assert_parity(bf16_to_np(y2), ref, what=f"pair gemm {M}x{K}x{N}")
+
+
 @pytest.mark.parametrize("M,K,N", [(10, 1536, 256), (11, 1536, 256), (4, 4096, 384), (1, 4096, 128), (1, 4160, 128),
                                    (2, 64, 1024), (2, 256, 20480)])
 def test_linear_fused_quantisation_edges(M, K, N):
