@@ -43,6 +43,10 @@ def parse():
     p.add_argument("--impl", default="native", choices=["native", "reference"])
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-secondary", action="store_true")
+    # internal: the oracle timing of the CPU baseline, run in a child process whose BLAS is
+    # pinned to one thread before numpy loads
+    p.add_argument("--cpu-baseline-child", nargs=3, type=int, metavar=("TOKENS", "REPEATS", "THREADS"),
+                   help=argparse.SUPPRESS)
     return p.parse_args()
 
 
@@ -534,6 +538,82 @@ def run_secondary(state, args):
                     "note": "quantise + grouped GEMM; 16 weight copies rotated (300 MB > L2), replayed as one CUDA "
                             "graph (eager_us_per_call: plain calls, bounded by the host)"})
         del gws
+    # routing + dispatch (stages a and b): latency-bound at small T, reported in microseconds
+    for T in (1, 8, 64, 128, 4096):
+        cfg = workloads.DECODE.get(T) or (workloads.PREFILL if T == 128 else workloads.PREFILL_WHOLE)
+        if T in workloads.DECODE:
+            ins = [workloads.decode_step(T, step=i, device=dev)[:2] for i in range(16)]
+        elif T == 128:
+            ins = [workloads.prefill_chunk(c, device=dev)[:2] for c in range(16)]
+        else:
+            x, ids, _ = workloads.prefill_whole(device="cpu")
+            ins = [(x.to(dev), ids.to(dev))]
+        wsr = ops.moe_workspace(T, cfg.H, cfg.I, cfg.E, cfg.topk, True, dev)
+        g1 = torch.empty(1, dtype=torch.float32, device=dev)
+
+        def disp(st, ins=ins, wsr=wsr, g1=g1):
+            for x, ids in ins:
+                ops.moe_dispatch(x, ids, W, g1, True, wsr, stream=st)
+
+        ms = graph_time_fn(disp, len(ins), 16 if len(ins) > 1 else 64)
+        rows = T * cfg.topk + T
+        b = T * cfg.H * 2 * 2 + rows * cfg.H * (0.5 + 1 / 16) + T * cfg.H * 4
+        out.append({"workload": f"route_dispatch_T{T}", "us_per_call": ms * 1e3, "hbm_gbs": b / (ms / 1e3) / 1e9,
+                    "hbm_frac": b / (ms / 1e3) / 1e9 / hbm,
+                    "note": "nvfp4_moe_dispatch: routing (histogram, scans, stable ranks, tile table) + amax + "
+                            "quantise/permute of x into the k+1 segments + zeroing of the fp32 accumulator; "
+                            "CUDA-graph replay over rotated inputs"})
+        del wsr
+    # fused RMSNorm -> NVFP4 (the quantiser's producer): 2 B read + 0.5625 B written per element
+    K = 7168
+    gamma = workloads.norm_weight(K, seed=5, device=dev)
+    for M in (1, 128, 4096):
+        nin = 16 if M < 4096 else 4  # > L2 in total
+        xs = [workloads.activations(M, K, seed=500 + i, device=dev, outliers=True) for i in range(nin)]
+        q = torch.empty(M, K // 2, dtype=torch.uint8, device=dev)
+        sfq = torch.empty(int(ops.sf_bytes(M, K)), dtype=torch.uint8, device=dev)
+        gq = torch.empty(1, dtype=torch.float32, device=dev)
+        wsn = torch.empty(int(ops.lib().nvfp4_rmsnorm_quantize_workspace_bytes(M, K)), dtype=torch.uint8,
+                          device=dev)
+
+        def norm(st, xs=xs, q=q, sfq=sfq, gq=gq, wsn=wsn, M=M):
+            for x in xs:
+                ops.call("nvfp4_rmsnorm_quantize", x.data_ptr(), M, K, K, gamma.data_ptr(), workloads.RMSNORM_EPS,
+                         0, gq.data_ptr(), q.data_ptr(), sfq.data_ptr(), 0, None, wsn.data_ptr(), wsn.numel(),
+                         st.cuda_stream)
+
+        ms = graph_time_fn(norm, nin, 16)
+        b = M * K * (2 + 0.5 + 1 / 16) + K * 2
+        out.append({"workload": f"rmsnorm_quantize_M{M}_K{K}", "us_per_call": ms * 1e3,
+                    "hbm_gbs": b / (ms / 1e3) / 1e9, "hbm_frac": b / (ms / 1e3) / 1e9 / hbm,
+                    "note": "fused RMSNorm -> NVFP4 with dynamic gs (statistics + encode launches); rotated inputs, "
+                            "CUDA-graph replay"})
+        del xs
+    # router gate: logits over E experts, softmax, top-k; 32 rotated gate weights (176 MB > L2)
+    for T in sorted(workloads.ROUTER):
+        _, Hr, Er, kr = workloads.ROUTER[T]
+        gates = []
+        for i in range(32):
+            q, sfw, ws2 = model.quantize_weight(workloads.weight(Er, Hr, workloads.ROUTER_WEIGHT_SEED + i, dev))
+            gates.append(ops.router_prepare(q, sfw, ws2, Er, Hr))
+        x = workloads.activations(T, Hr, seed=40 + T, device=dev)
+        ids = torch.empty(T, kr, dtype=torch.int32, device=dev)
+        wts = torch.empty(T, kr, dtype=torch.float32, device=dev)
+        lg = torch.empty(T, Er, dtype=torch.float32, device=dev)
+
+        def route(st, gates=gates, x=x, ids=ids, wts=wts, lg=lg, T=T, Hr=Hr, Er=Er, kr=kr):
+            for wg in gates:
+                ops.call("nvfp4_router", x.data_ptr(), T, Hr, wg.data_ptr(), Er, kr, ids.data_ptr(), wts.data_ptr(),
+                         lg.data_ptr(), None, 0, st.cuda_stream)
+
+        ms = graph_time_fn(route, 32, 8)
+        b = Er * Hr * 2 + T * Hr * 2 + T * Er * 4
+        out.append({"workload": f"router_T{T}_H{Hr}_E{Er}_k{kr}", "us_per_call": ms * 1e3,
+                    "hbm_gbs": b / (ms / 1e3) / 1e9, "hbm_frac": b / (ms / 1e3) / 1e9 / hbm,
+                    "tflops": 2 * T * Er * Hr / (ms / 1e3) / 1e12,
+                    "note": "bf16 gate (FP8 round trip applied once at load) x activations -> fp32 logits, softmax, "
+                            "top-k; 32 rotated gate copies, CUDA-graph replay"})
+        del gates
     K = N = 7168
     dw = model.make_dense_weight(N, K, seed=70, device=dev)
     for M in (1024, 4096, 16384):
@@ -572,14 +652,30 @@ def oracle_sample(n_tokens: int, chunk: int = 0, device="cpu"):
     return cfg, x.float().numpy(), ids.numpy(), w.numpy(), experts, a2, tokens
 
 
-def time_oracle(n_tokens: int, reps: int, device="cpu"):
+def thread_mapper(threads: int):
+    """The oracle's per-expert jobs on a pool of host threads (numpy releases the GIL in its
+    array loops and contractions)."""
+    from concurrent.futures import ThreadPoolExecutor
+    ex = ThreadPoolExecutor(max_workers=threads)
+    return (lambda fn, jobs: ex.map(fn, jobs)), ex
+
+
+def time_oracle(n_tokens: int, reps: int, device="cpu", threads: int = 1):
+    """Seconds per oracle MoE forward of n tokens (experts prepared beforehand, untimed), ``reps``
+    times; threads > 1 runs the per-expert jobs on that many host threads."""
     from oracle import nvfp4_oracle as O
     cfg, x, ids, w, experts, a2, tokens = oracle_sample(n_tokens, device=device)
+    mapper, ex = thread_mapper(threads) if threads > 1 else (map, None)
     times = []
-    for _ in range(reps):
-        t0 = time.perf_counter()
-        O.moe_forward(x, ids, w, experts.__getitem__, cfg.E, a2, shared=experts[cfg.E], tokens=tokens)
-        times.append(time.perf_counter() - t0)
+    try:
+        for _ in range(reps):
+            t0 = time.perf_counter()
+            O.moe_forward(x, ids, w, experts.__getitem__, cfg.E, a2, shared=experts[cfg.E], tokens=tokens,
+                          mapper=mapper)
+            times.append(time.perf_counter() - t0)
+    finally:
+        if ex is not None:
+            ex.shutdown()
     return cfg, times
 
 
@@ -590,21 +686,52 @@ def cpu_cores() -> int:
         return os.cpu_count() or 1
 
 
-def cpu_baseline(device):
-    cfg, times = time_oracle(2, 1, device=device)
-    return {"value": 2 / times[0], "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
-            "sample": f"2 tokens of prefill chunk 0 (8 routed experts each + shared), full oracle MoE forward "
-                      f"(fp64 dequant + contractions; numpy BLAS threads up to the {cpu_cores()} cores); "
-                      f"{times[0]:.1f} s",
-            "threads_note": "numpy matmul may use every core in the affinity set"}
+CPU_BASELINE_TOKENS = 2
+CPU_BASELINE_REPEATS = 3
+SINGLE_THREAD_ENV = {k: "1" for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS")}
+
+
+def cpu_baseline_child(n_tokens: int, reps: int, threads: int):
+    """Child process (BLAS pinned to one thread by its environment): the oracle on one thread
+    (the builtin map) and on ``threads`` host threads, ``reps`` times each; prints one JSON line."""
+    import torch
+    device = "cuda" if torch.cuda.is_available() else "cpu"
+    _, t1 = time_oracle(n_tokens, reps, device=device, threads=1)
+    _, tn = time_oracle(n_tokens, reps, device=device, threads=threads)
+    print(json.dumps({"t1": t1, "tn": tn, "weights_drawn_on": device}), flush=True)
+
+
+def cpu_baseline():
+    """The oracle as it stands, on this host's cores: a bounded sample of the workload (the
+    first tokens of prefill chunk 0), 1 thread and all cores, several repeats each."""
+    cores = cpu_cores()
+    env = dict(os.environ, **SINGLE_THREAD_ENV)
+    r = subprocess.run([sys.executable, os.path.abspath(__file__), "--cpu-baseline-child", str(CPU_BASELINE_TOKENS),
+                        str(CPU_BASELINE_REPEATS), str(cores)], env=env, capture_output=True, text=True,
+                       timeout=1800)
+    if r.returncode != 0:
+        return {"value": None, "unit": UNIT, "cores": cores, "kind": "oracle",
+                "error": (r.stderr or r.stdout).strip().splitlines()[-1:]}
+    d = json.loads(r.stdout.strip().splitlines()[-1])
+    t1, tn = statistics.median(d["t1"]), statistics.median(d["tn"])
+    n = CPU_BASELINE_TOKENS
+    return {"value": n / tn, "unit": UNIT, "cores": cores, "kind": "oracle",
+            "value_1t": n / t1, "value_nt": n / tn, "threads_nt": cores, "repeats": CPU_BASELINE_REPEATS,
+            "seconds_1t": d["t1"], "seconds_nt": d["tn"],
+            "sample": f"{n} tokens of prefill chunk 0 (8 routed experts each + the shared expert), the full oracle "
+                      f"MoE forward (fp64 dequantisation and contractions), experts prepared beforehand; "
+                      f"median of {CPU_BASELINE_REPEATS} runs on 1 thread (BLAS pinned to 1) and on {cores} host "
+                      f"threads (per-expert jobs split over the cores); value = the {cores}-thread figure"}
 
 
 def run_reference(args, rank: int, world: int):
     if rank != 0:
         return None
     import torch
+    cores = cpu_cores()
     # the weights are drawn on the GPU, like the native arm's; the oracle itself runs on the host cores
-    cfg, times = time_oracle(1, args.warmup + args.steps, device="cuda" if torch.cuda.is_available() else "cpu")
+    cfg, times = time_oracle(1, args.warmup + args.steps, device="cuda" if torch.cuda.is_available() else "cpu",
+                             threads=cores)
     timed = times[args.warmup:]
     total = sum(timed)
     value = len(timed) / total
@@ -612,16 +739,36 @@ def run_reference(args, rank: int, world: int):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / len(timed),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64 (oracle)",
             "data": "synthetic (seeded), same workload", "config": {"workload": cfg.name, "oracle_tokens_per_step": 1},
-            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
-                             "sample": "each step: 1 token of prefill chunk 0 through the full oracle MoE forward"},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                             "sample": f"each step: 1 token of prefill chunk 0 through the full oracle MoE forward, "
+                                       f"per-expert jobs on {cores} host threads"},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def relaunch(n: int) -> int:
+    """Start n local ranks of this benchmark (one per GPU) and return their exit status."""
+    import socket
+    with socket.socket() as so:
+        so.bind(("127.0.0.1", 0))
+        port = so.getsockname()[1]
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", f"--nproc-per-node={n}",
+           "--master-addr", "127.0.0.1", f"--master-port={port}", os.path.abspath(__file__), *sys.argv[1:]]
+    return subprocess.run(cmd).returncode
 
 
 def main():
     args = parse()
-    rank = int(os.environ.get("RANK", "0"))
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.cpu_baseline_child:
+        cpu_baseline_child(*args.cpu_baseline_child)
+        return
+    from nvfp4_block_scaled_quant_gb300 import replicas
+    action, why = replicas.launch_plan(args.gpus, os.environ)
+    if action == "error":
+        print(f"bench.py: {why}", file=sys.stderr)
+        sys.exit(2)
+    if action == "relaunch":
+        sys.exit(relaunch(args.gpus))
+    rank, world, local_rank = replicas.env_ranks()
     if args.impl == "reference":
         if rank == 0:
             print(json.dumps(run_reference(args, rank, world)), flush=True)
@@ -638,7 +785,7 @@ def main():
         if not args.no_cpu_baseline and world == 1:
             del state
             torch.cuda.empty_cache()
-            result["cpu_baseline"] = cpu_baseline(device=f"cuda:{local_rank}")
+            result["cpu_baseline"] = cpu_baseline()
         print(json.dumps(result), flush=True)
     if world > 1:
         import torch.distributed as dist

@@ -9,7 +9,7 @@ throughput is the units all ranks processed divided by the slowest rank's time.
 from __future__ import annotations
 
 import os
-from typing import Optional, Tuple
+from typing import Mapping, Optional, Tuple
 
 import torch
 
@@ -38,3 +38,20 @@ def replica_throughput(local_ms: float, local_units: float,
     dist.all_reduce(u, op=dist.ReduceOp.SUM)
     max_ms, units = float(t.item()), float(u.item())
     return units / (max_ms / 1e3), max_ms, units
+
+
+def launch_plan(gpus: int, env: Mapping[str, str]) -> Tuple[str, str]:
+    """What a benchmark asked for ``gpus`` GPUs does, given the launcher's environment.
+
+    ("run", "")        run in this process: one GPU, or one rank of a launcher with WORLD_SIZE == gpus;
+    ("relaunch", "")   no launcher and gpus > 1: start gpus local ranks (one per GPU) and wait;
+    ("error", why)     gpus < 1, or a launcher whose WORLD_SIZE differs from gpus.
+    """
+    if gpus < 1:
+        return "error", f"--gpus {gpus}: at least one GPU"
+    world = env.get("WORLD_SIZE")
+    if world is None:
+        return ("relaunch", "") if gpus > 1 else ("run", "")
+    if int(world) != gpus:
+        return "error", f"--gpus {gpus} but the launcher started WORLD_SIZE={world} ranks"
+    return "run", ""

@@ -56,3 +56,20 @@ def test_two_gloo_ranks_aggregate_max_time_and_all_units(times_ms, units):
 
 def test_single_process_is_the_local_figure():
     assert replicas.replica_throughput(250.0, 1000.0) == (4000.0, 250.0, 1000.0)
+
+
+@pytest.mark.parametrize("gpus,env,want", [
+    (1, {}, "run"),
+    (8, {}, "relaunch"),
+    (2, {"WORLD_SIZE": "2", "RANK": "1"}, "run"),
+    (1, {"WORLD_SIZE": "1"}, "run"),
+    (8, {"WORLD_SIZE": "4"}, "error"),
+    (1, {"WORLD_SIZE": "2"}, "error"),
+    (0, {}, "error"),
+])
+def test_launch_plan_of_the_gpus_flag(gpus, env, want):
+    """--gpus N without a launcher starts N local ranks; under a launcher it must agree with
+    WORLD_SIZE (a silent one-GPU run for --gpus 8 is an error)."""
+    action, why = replicas.launch_plan(gpus, env)
+    assert action == want
+    assert (why != "") == (want == "error")
