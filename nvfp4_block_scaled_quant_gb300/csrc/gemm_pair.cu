@@ -290,26 +290,33 @@ __global__ void __launch_bounds__(kPThreads, 1)
       const uint32_t tbase = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + static_cast<uint32_t>(half * 128);
       __nv_bfloat16 *y = static_cast<__nv_bfloat16 *>(args.out) + static_cast<int64_t>(row) * args.out_ld +
                          nt * kPN + half * 128;
+      // two batches of 64 columns, one tensor-memory wait each: the accumulator goes back to
+      // the issuer after two load round trips instead of eight
 #pragma unroll 1
-      for (int c = 0; c < 8; ++c) {
-        uint32_t r[16];
-        tmem_ld16(tbase + c * 16, r);
-        tmem_ld_wait();
-        if (c == 7) release();
-        if (row_ok) {
-          uint32_t packed[8];
+      for (int b = 0; b < 2; ++b) {
+        uint32_t r[4][16];
 #pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            const __nv_bfloat162 v =
-                __floats2bfloat162_rn(__uint_as_float(r[2 * i]) * alpha, __uint_as_float(r[2 * i + 1]) * alpha);
-            packed[i] = *reinterpret_cast<const uint32_t *>(&v);
-          }
-          if (out32) {
-            st_global_v8(y + c * 16, packed);
-          } else {
-            uint4 *dst = reinterpret_cast<uint4 *>(y + c * 16);
-            dst[0] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
-            dst[1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
+        for (int q = 0; q < 4; ++q) tmem_ld16(tbase + b * 64 + q * 16, r[q]);
+        tmem_ld_wait();
+        if (b == 1) release();
+        if (row_ok) {
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            uint32_t packed[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              const __nv_bfloat162 v = __floats2bfloat162_rn(__uint_as_float(r[q][2 * i]) * alpha,
+                                                             __uint_as_float(r[q][2 * i + 1]) * alpha);
+              packed[i] = *reinterpret_cast<const uint32_t *>(&v);
+            }
+            __nv_bfloat16 *dst = y + b * 64 + q * 16;
+            if (out32) {
+              st_global_v8(dst, packed);
+            } else {
+              uint4 *d4 = reinterpret_cast<uint4 *>(dst);
+              d4[0] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+              d4[1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
+            }
           }
         }
       }
