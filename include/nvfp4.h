@@ -4,14 +4,14 @@
  * NVFP4 tensors: 4-bit E2M1 codes, two per byte (element 2j in the low nibble),
  * one unsigned E4M3 scale per 16 consecutive elements along K, and one FP32
  * global multiplier.  A value decodes as e2m1(code) * e4m3(scale) * global
- * (nvfp4-megamoe-kernel commit log, page 2, paragraph "Critical bug fix:
- * weight_scale_2 ... was being dropped": lut[w] * weight_scale * weight_scale_2).
- * Activations carry gs = amax / (6 * 448) as their global multiplier (page 3,
- * paragraph "The activation global scale = amax / (6.0 * 448.0)"); weights
- * carry ws2 = weight_scale_2 and nothing else (page 2, paragraph "input_scale
- * is the activation quantization scale").  A GEMM therefore computes
+ * (nvfp4-megamoe-kernel commit log, page 2 = commit efe63ca, single_shot_inference.py:
+ * the weight_scale_2 fix, i.e. the NVFP4 dequantisation formula).  Activations carry
+ * gs = amax / (6 * 448) as their global multiplier (page 3 = commit 4c6464e, vllm: the
+ * activation global-scale passage); weights carry ws2 = weight_scale_2 and nothing else
+ * (page 2: the input_scale passage, which keeps the checkpoint input_scale out of the
+ * weight side).  A GEMM therefore computes
  * y = (gs * ws2) * sum_k e2m1(a) e4m3(sa) e2m1(b) e4m3(sb)
- * (page 1, opening paragraph: y = (x * scale_a * gsa) @ (w * scale_b * gsb)).
+ * (page 1: the scale-semantics passage, y = (x * scale_a * gsa) @ (w * scale_b * gsb)).
  *
  * Conventions for every entry point:
  *  - Pointers are DEVICE pointers owned by the caller unless stated otherwise;
@@ -33,8 +33,8 @@
  *    nvfp4_sf_bytes(rows, K) bytes: rows padded to a multiple of 128 and scale
  *    columns (K/16) to a multiple of 4, grouped into 512-byte blocks of
  *    128 rows x 4 columns stored row-group-major; the four scales of row r sit
- *    at byte 16*(r%32) + 4*((r%128)/32) of their block (page 3, paragraph
- *    "This time the GEMM impl correctly": A-side scales padded and swizzled).
+ *    at byte 16*(r%32) + 4*((r%128)/32) of their block (page 3: the grouped-GEMM
+ *    launch contract, A-side scales padded and swizzled).
  *  - Errors: argument problems are detected on the host and returned before
  *    anything is enqueued; nothing throws across the ABI.  A detail string for
  *    the last failing call on the calling thread is available from
@@ -123,9 +123,10 @@ NVFP4_API nvfp4_status nvfp4_quantize_act(const void *x, int64_t M, int64_t K, i
                                 size_t ws_bytes, void *stream);
 
 /* -------------------------------------------------- RMSNorm -> quantize
- * RMSNorm feeding the activation quantiser (the fused "P4" path of page 1, paragraph
- * "Added --ab-compare flag", whose A/B harness compares x_normed, the global scale, the
- * FP4 data and the GEMM outputs of the fused and unfused paths).  Per row r:
+ * RMSNorm feeding the activation quantiser (the fused "P4" path of page 1 = commit
+ * 1121cd7, single_shot_inference.py: the fused-RMSNorm A/B passage, whose harness compares
+ * x_normed, the global scale, the FP4 data and the GEMM outputs of the fused and unfused
+ * paths).  Per row r:
  *   inv_r = 1 / sqrt(fl32(sum_k x^2) / K + eps)        (correctly rounded sqrt, divide)
  *   x_normed[r,k] = bf16(fl32(fl32(x[r,k] * inv_r) * gamma[k]))
  * gamma is a bf16 vector of K.  nvfp4_rmsnorm writes x_normed (M, K) bf16 (the unfused
@@ -144,9 +145,8 @@ NVFP4_API nvfp4_status nvfp4_rmsnorm_quantize(const void *x, int64_t M, int64_t 
 
 /* ------------------------------------------------------------ weight prepare
  * Checkpoint-layout weights of G groups (experts): codes w (G, N, K/2) and
- * row-major E4M3 scales sf (G, N, K/16) used as stored, no transpose (page 2,
- * paragraph "Critical bug: checkpoint weights are (N_packed, K_packed)
- * N-major ... scales are (N, K_sf)").  Writes w_out (G, N, K/2) and sf_out
+ * row-major E4M3 scales sf (G, N, K/16) used as stored, no transpose (page 2: the
+ * checkpoint-layout fix, N-major codes and untransposed scales).  Writes w_out (G, N, K/2) and sf_out
  * (G blocks of nvfp4_sf_bytes(N, K)).  NVFP4_PREP_W13_INTERLEAVE reorders the
  * rows of a fused gate/up projection so that every 128-row tile holds 64 gate
  * rows followed by the 64 matching up rows (needs N % 128 == 0).  Run once at
@@ -159,7 +159,7 @@ NVFP4_API nvfp4_status nvfp4_prepare_weights(const uint8_t *w, const uint8_t *sf
  * y (M, N) bf16 = alpha * deq(xq) @ deq(W)^T with alpha = gs * ws2, where xq is
  * x (M, K) bf16 quantised at run time (gs_mode as for nvfp4_quantize_act,
  * *gs written in dynamic mode) and W is a prepared (N, K/2) + swizzled sf
- * weight with device scalar ws2 (Nvfp4Linear, page 2 paragraph "Fixes in:").
+ * weight with device scalar ws2 (Nvfp4Linear, page 2: the ws2-folding fixes).
  * K % 64 == 0, N % 128 == 0.  Workspace: quantised x + scales + partials. */
 NVFP4_API size_t nvfp4_linear_workspace_bytes(int64_t M, int64_t K);
 NVFP4_API nvfp4_status nvfp4_linear(const void *x, int64_t M, int64_t K, int64_t N, const uint8_t *w,
@@ -210,9 +210,9 @@ NVFP4_API nvfp4_status nvfp4_gemm(const uint8_t *xq, const uint8_t *xsf, const f
  * multiplies its K columns by its own NVFP4 weight W_g (N, K/2) with ws2[g]:
  *   y[:, g*N:(g+1)*N] = (gs * ws2[g]) * deq(xq[:, g*K:(g+1)*K]) @ deq(W_g)^T
  * with one activation gs over all of x (gs_mode as for nvfp4_quantize_act).
- * This is the grouped o-projection of page 3 (paragraph "The BF16 wo_a path was
- * calling self.wo_a": a per-group BMM with in_features 4096; paragraph "Instead of
- * fighting DeepGEMM": an NVFP4 grouped linear with n_local_groups = 8).  w is
+ * This is the grouped o-projection of page 3 (the wo_a o-projection passage: a per-group
+ * BMM with in_features 4096; the ScaledGroupedGemm passage: an NVFP4 grouped linear with
+ * n_local_groups = 8).  w is
  * (G, N, K/2) prepared with NVFP4_PREP_PLAIN and w_sf G blocks of
  * nvfp4_sf_bytes(N, K); ws2 (G) fp32; y (M, G*N) bf16.  K % 64 == 0, N % 128 == 0. */
 NVFP4_API size_t nvfp4_grouped_linear_workspace_bytes(int64_t M, int64_t G, int64_t K);
@@ -222,7 +222,7 @@ NVFP4_API nvfp4_status nvfp4_grouped_linear(const void *x, int64_t M, int64_t G,
                                             size_t ws_bytes, void *stream);
 
 /* --------------------------------------------------------------- router gate
- * The dense router of page 1 (paragraph "Router gate: FP8_E4M3 quantize"): the NVFP4 gate
+ * The dense router of page 1 (the router-gate FP8 round-trip passage): the NVFP4 gate
  * weight (E, H/2) codes with row-major scales (E, H/16) and device scalar ws2 is
  * dequantised to bf16, quantised to FP8-E4M3 with one per-tensor scale s = amax / 448 and
  * dequantised back to bf16 (nvfp4_router_prepare, once):
@@ -244,7 +244,7 @@ NVFP4_API nvfp4_status nvfp4_router(const void *x, int64_t T, int64_t H, const v
 /* -------------------------------------------------------------- (b) routing
  * Groups the T*topk flat entries f = t*topk + j of ids (T, topk) int32 by
  * expert: counts[e] (E), offsets (E+1, exclusive prefix sum, int32 as the
- * grouped GEMM wants: page 3, paragraph "This time the GEMM impl correctly"),
+ * grouped GEMM wants: page 3, the grouped-GEMM launch contract),
  * sorted_idx (T*topk) = the flat indices ordered by expert, increasing f
  * within an expert, and inv_idx (T*topk) = position of f in sorted_idx.
  * Ids outside [0, E) are dropped (inv_idx = -1) and raise
@@ -267,9 +267,8 @@ NVFP4_API nvfp4_status nvfp4_moe_route(const int32_t *ids, int64_t T, int topk, 
  * with xq = x quantised with one global scale over all T tokens (a1_gs_mode as
  * above, *a1_gs written in dynamic mode) and a2_gs (E+1 entries, last = shared
  * expert) the static global scales of the re-quantised intermediate h
- * (warm-up calibrated, page 3 paragraph "The checkpoint's input_scale ...").
- * y (T, H) bf16; the output width is H (page 3, paragraph "K comes from
- * hidden_states.size(-1)").  H % 128 == 0, I % 64 == 0. */
+ * (warm-up calibrated, page 3: the warm-up calibration passage).
+ * y (T, H) bf16; the output width is H (page 3: the MoE shape-rules passage).  H % 128 == 0, I % 64 == 0. */
 typedef struct nvfp4_moe_ws_layout {
   /* byte offsets into the workspace */
   size_t counts;        /* int32 [G]        rows per group (G = E + has_shared)     */

@@ -15,19 +15,16 @@ Everything here is written to be checked by eye against the definitions:
 
 Sources (the three commit-log pages of the "nvfp4-megamoe-kernel" project):
 
-* page 2 (commit efe63ca, single_shot_inference.py), paragraph "Critical bug
-  fix: weight_scale_2 ... was being dropped": a weight decodes as
-  lut[w] * weight_scale * weight_scale_2;
-* page 1 (commit 1121cd7), opening paragraph: the GEMM is
-  y = (x * scale_a * gsa) @ (w * scale_b * gsb); the global scalars of both
-  sides fold into one multiplier;
-* page 3 (commit 4c6464e, vllm), paragraph "The activation global scale =
-  amax / (6.0 * 448.0)": gs is the dequantisation multiplier, not its
-  inverse;
-* page 3, paragraph "This time the GEMM impl correctly": int32 expert
-  offsets, padded and swizzled A-side scales;
-* page 3, paragraph "K comes from hidden_states.size(-1)": the MoE output
-  width is the hidden size.
+* page 2 (commit efe63ca, single_shot_inference.py), the weight_scale_2 fix:
+  a weight decodes as lut[w] * weight_scale * weight_scale_2;
+* page 1 (commit 1121cd7, single_shot_inference.py), the scale-semantics
+  passage: the GEMM is y = (x * scale_a * gsa) @ (w * scale_b * gsb); the
+  global scalars of both sides fold into one multiplier;
+* page 3 (commit 4c6464e, vllm), the activation global-scale passage: gs =
+  amax / (6 * 448) is the dequantisation multiplier, not its inverse;
+* page 3, the grouped-GEMM launch contract: int32 expert offsets, padded and
+  swizzled A-side scales;
+* page 3, the MoE shape rules: the MoE output width is the hidden size.
 
 Readings taken where the pages are silent (each is also listed in the design
 notes): E2M1 and E4M3 conversions round to nearest, ties to even, saturating
@@ -257,7 +254,7 @@ def rmsnorm(x: np.ndarray, gamma: np.ndarray, eps: float):
 
     Returns (y rounded to bf16 through fp32, as fp32 values; y in fp64; inv_rms fp64).  The
     normalised activations that feed the NVFP4 quantiser are bf16, as the unfused path of page 1
-    (paragraph "Added --ab-compare flag") hands x_normed to the quantiser.
+    (the fused-RMSNorm A/B passage) hands x_normed to the quantiser.
     """
     x64 = np.asarray(x, dtype=np.float64)
     inv = 1.0 / np.sqrt(np.mean(x64 * x64, axis=1) + eps)
@@ -273,8 +270,8 @@ def rmsnorm(x: np.ndarray, gamma: np.ndarray, eps: float):
 def linear(xq: Quantized, w_codes: np.ndarray, w_sf: np.ndarray, ws2: float) -> np.ndarray:
     """y[m, n] = sum_k deq(xq)[m, k] * deq(W)[n, k] in fp64.
 
-    The activation side carries gs, the weight side ws2 only (page 2, paragraph
-    "input_scale is the activation quantization scale").
+    The activation side carries gs, the weight side ws2 only (page 2, the input_scale
+    passage: the checkpoint input_scale stays off the weight side).
     """
     a = dequantize(xq.codes, xq.sf, xq.gs)
     b = dequantize(w_codes, w_sf, ws2)
@@ -286,8 +283,8 @@ def grouped_linear(xq: Quantized, w_codes: Sequence[np.ndarray], w_sf: Sequence[
     """Fixed-group linear: the input features split into G equal groups, group g of x times W_g.
 
     y[:, g*N:(g+1)*N] = deq(xq[:, g*K:(g+1)*K]) @ deq(W_g)^T with W_g's own ws2 and the
-    activation's single gs (page 3, paragraph "The BF16 wo_a path was calling self.wo_a": wo_a is
-    a per-group BMM with in_features 4096 per group; paragraph "Instead of fighting DeepGEMM":
+    activation's single gs (page 3, the wo_a o-projection passage: wo_a is
+    a per-group BMM with in_features 4096 per group; the ScaledGroupedGemm passage:
     an NVFP4 grouped linear with n_local_groups = 8).
     """
     G = len(w_codes)
@@ -316,7 +313,7 @@ def e4m3_decode_signed(b: np.ndarray) -> np.ndarray:
 
 
 def router_weight(w_codes: np.ndarray, w_sf: np.ndarray, ws2: float) -> np.ndarray:
-    """Gate weight as the router uses it (page 1, paragraph "Router gate: FP8_E4M3 quantize"):
+    """Gate weight as the router uses it (page 1, the router-gate FP8 round-trip passage):
     dequantise the NVFP4 checkpoint to bf16, quantise to FP8-E4M3 with one per-tensor scale
     s = amax / 448, dequantise back to bf16.  Steps in fp32:
       w  = bf16(fl32(fl32(e2m1 * e4m3) * ws2))
