@@ -600,19 +600,20 @@ def run_secondary(state, args):
         ids = torch.empty(T, kr, dtype=torch.int32, device=dev)
         wts = torch.empty(T, kr, dtype=torch.float32, device=dev)
         lg = torch.empty(T, Er, dtype=torch.float32, device=dev)
+        wsr = torch.empty(max(256, int(ops.lib().nvfp4_router_workspace_bytes(T, Er))), dtype=torch.uint8, device=dev)
 
-        def route(st, gates=gates, x=x, ids=ids, wts=wts, lg=lg, T=T, Hr=Hr, Er=Er, kr=kr):
+        def route(st, gates=gates, x=x, ids=ids, wts=wts, lg=lg, wsr=wsr, T=T, Hr=Hr, Er=Er, kr=kr):
             for wg in gates:
                 ops.call("nvfp4_router", x.data_ptr(), T, Hr, wg.data_ptr(), Er, kr, ids.data_ptr(), wts.data_ptr(),
-                         lg.data_ptr(), None, 0, st.cuda_stream)
+                         lg.data_ptr(), wsr.data_ptr(), wsr.numel(), st.cuda_stream)
 
         ms = graph_time_fn(route, 32, 8)
         b = Er * Hr * 2 + T * Hr * 2 + T * Er * 4
         out.append({"workload": f"router_T{T}_H{Hr}_E{Er}_k{kr}", "us_per_call": ms * 1e3,
                     "hbm_gbs": b / (ms / 1e3) / 1e9, "hbm_frac": b / (ms / 1e3) / 1e9 / hbm,
                     "tflops": 2 * T * Er * Hr / (ms / 1e3) / 1e12,
-                    "note": "bf16 gate (FP8 round trip applied once at load) x activations -> fp32 logits, softmax, "
-                            "top-k; 32 rotated gate copies, CUDA-graph replay"})
+                    "note": "bf16 gate (FP8 round trip applied once at load) x activations -> fp32 logits on the "
+                            "tensor cores (split over H), softmax, top-k; 32 rotated gate copies, CUDA-graph replay"})
         del gates
     K = N = 7168
     dw = model.make_dense_weight(N, K, seed=70, device=dev)

@@ -55,7 +55,7 @@
 extern "C" {
 #endif
 
-#define NVFP4_ABI_VERSION 4
+#define NVFP4_ABI_VERSION 5
 
 /* Exported symbols: the library builds with hidden visibility by default. */
 #if defined(NVFP4_BUILD) && defined(__GNUC__)
@@ -231,8 +231,11 @@ NVFP4_API nvfp4_status nvfp4_grouped_linear(const void *x, int64_t M, int64_t G,
  * Per call (nvfp4_router): logits = x (T, H) bf16 @ wg^T in fp32, softmax over the E
  * experts, the topk largest probabilities (lower expert id first on ties) as ids (T, topk)
  * int32 and weights (T, topk) fp32 renormalised to sum 1 -- the inputs of the routing
- * stage.  logits (T, E) fp32 may be given to receive the logits; otherwise the workspace
- * holds them.  E <= 1024, topk <= min(32, E), H % 64 == 0. */
+ * stage.  The logits run on the tensor cores split over H; the workspace
+ * (nvfp4_router_workspace_bytes, always required) holds the splits' fp32 partials, which
+ * are summed in a fixed order, so repeated calls give identical logits.  logits (T, E) fp32,
+ * if not NULL, receives the summed logits.  E <= 1024, topk <= min(32, E), H % 64 == 0,
+ * T and H below 2^24.  Two launches. */
 NVFP4_API size_t nvfp4_router_prepare_workspace_bytes(int64_t E, int64_t H);
 NVFP4_API nvfp4_status nvfp4_router_prepare(const uint8_t *w, const uint8_t *w_sf, const float *ws2, int64_t E,
                                             int64_t H, void *wg, void *ws, size_t ws_bytes, void *stream);

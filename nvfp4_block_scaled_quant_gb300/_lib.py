@@ -37,7 +37,7 @@ DEVERR_INTERNAL = 4
 LINEAR_NOALLOC_MAX_BYTES = 4 << 20
 
 
-ABI_VERSION = 4  # NVFP4_ABI_VERSION of the header these signatures follow
+ABI_VERSION = 5  # NVFP4_ABI_VERSION of the header these signatures follow
 
 
 class MoeWsLayout(Structure):

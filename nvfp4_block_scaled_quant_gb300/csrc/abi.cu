@@ -718,7 +718,9 @@ nvfp4_status nvfp4_router_prepare(const uint8_t *w, const uint8_t *w_sf, const f
 
 size_t nvfp4_router_workspace_bytes(int64_t T, int64_t E) {
   if (T < 0 || E < 0) return 0;
-  return align256(static_cast<size_t>(T) * static_cast<size_t>(E) * sizeof(float));
+  // the K splits' partial logits; the split count is largest when H is (any H % 64 == 0)
+  const int64_t splits = router_splits(T, E, int64_t(1) << 24);
+  return align256(static_cast<size_t>(splits) * static_cast<size_t>(T) * static_cast<size_t>(E) * sizeof(float));
 }
 
 nvfp4_status nvfp4_router(const void *x, int64_t T, int64_t H, const void *wg, int64_t E, int topk, int32_t *ids,
@@ -730,13 +732,18 @@ nvfp4_status nvfp4_router(const void *x, int64_t T, int64_t H, const void *wg, i
   NV_REQUIRE(wg && ((x && ids && weights) || T == 0), NVFP4_ERR_INVALID_ARG, "NULL pointer argument");
   NV_REQUIRE(aligned(x, 16) && aligned(wg, 16) && aligned(ids, 4) && aligned(weights, 4) && aligned(logits, 4),
              NVFP4_ERR_MISALIGNED, "x and wg must be 16-byte aligned");
-  nvfp4_status st = NVFP4_OK;
-  if (!logits && (st = check_ws(__func__, ws, ws_bytes, nvfp4_router_workspace_bytes(T, E))) != NVFP4_OK) return st;
+  NV_REQUIRE(T < (int64_t(1) << 24) && H < (int64_t(1) << 24), NVFP4_ERR_UNSUPPORTED_SHAPE, "sizes too large");
+  nvfp4_status st = check_ws(__func__, ws, ws_bytes, nvfp4_router_workspace_bytes(T, E));
+  if (st != NVFP4_OK) return st;
   DeviceInfo *d;
   if ((st = device_info(__func__, &d)) != NVFP4_OK) return st;
   if (T == 0) return NVFP4_OK;
-  float *lg = logits ? logits : static_cast<float *>(ws);
-  NV_CUDA(launch_router(x, T, H, wg, E, topk, ids, weights, lg, static_cast<cudaStream_t>(stream)), "router launch");
+  CUtensorMap tx, tw;
+  if ((st = make_map(__func__, &tx, x, 2 * H, T, 2 * H, 128)) != NVFP4_OK) return st;
+  if ((st = make_map(__func__, &tw, wg, 2 * H, E, 2 * H, 128)) != NVFP4_OK) return st;
+  NV_CUDA(launch_router(tx, tw, T, H, E, topk, ids, weights, logits, static_cast<float *>(ws), d->flags,
+                        static_cast<cudaStream_t>(stream)),
+          "router launch");
   return NVFP4_OK;
 }
 

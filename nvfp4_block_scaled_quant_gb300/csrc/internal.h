@@ -171,8 +171,14 @@ cudaError_t launch_rmsnorm_quantize(const void *x, int64_t M, int64_t K, int64_t
 int router_partial_count(int64_t nblocks);
 cudaError_t launch_router_prepare(const uint8_t *w, const uint8_t *sf, const float *ws2, int64_t E, int64_t H,
                                   uint32_t *partials, void *wg, cudaStream_t s);
-cudaError_t launch_router(const void *x, int64_t T, int64_t H, const void *wg, int64_t E, int topk, int32_t *ids,
-                          float *weights, float *logits, cudaStream_t s);
+// Router logits on the tensor cores, split over K into router_splits(T, E, H) fp32 partials
+// (partial: splits x T x E floats), then softmax + top-k over their sum.  tm_x / tm_w: byte
+// tensor maps of x (T rows of 2H bytes) and wg (E rows) with 128-byte x 128-row boxes.
+constexpr int64_t kRouterTargetCtas = 144;  // tiles x splits aimed for
+constexpr int64_t kRouterMaxSplits = 48;
+int router_splits(int64_t T, int64_t E, int64_t H);
+cudaError_t launch_router(const CUtensorMap &tm_x, const CUtensorMap &tm_w, int64_t T, int64_t H, int64_t E, int topk,
+                          int32_t *ids, float *weights, float *logits, float *partial, uint32_t *err, cudaStream_t s);
 cudaError_t launch_prepare(const uint8_t *w, const uint8_t *sf, int64_t G, int64_t N, int64_t K,
                            int flags, uint8_t *w_out, uint8_t *sf_out, cudaStream_t s);
 

@@ -1,7 +1,10 @@
 // Router gate: the NVFP4 gate weight dequantised to bf16, round-tripped through FP8-E4M3 with
-// one per-tensor scale s = amax / 448 (prepare, once), then per call logits = x @ wg^T in fp32
-// on the CUDA cores (a small contraction next to the expert GEMMs: 384 x 7168 per token), a
-// softmax over the experts and the top-k with weights renormalised over the k chosen.
+// one per-tensor scale s = amax / 448 (prepare, once), then per call logits = x @ wg^T on the
+// tensor cores (tcgen05.mma kind::f16: bf16 operands staged by TMA, fp32 accumulators in
+// TMEM; 128-token x 128-expert tiles split over K so that a decode or chunk-sized batch still
+// spreads over the SMs), a softmax over the experts and the top-k with weights renormalised
+// over the k chosen.  The K splits write fp32 partial logits; the softmax kernel sums them in
+// a fixed order, so the logits do not depend on the order in which the splits finish.
 #include "common.cuh"
 
 namespace nvfp4 {
@@ -9,8 +12,6 @@ namespace nvfp4 {
 namespace {
 
 constexpr int kPrepThreads = 256;
-constexpr int kGateExperts = 8;   // experts per block (one warp each)
-constexpr int kGateTokens = 32;   // tokens per block
 
 // bf16 value of one dequantised NVFP4 weight: bf16(fl32(fl32(e2m1 * e4m3) * ws2))
 __device__ __forceinline__ float nvfp4_weight_bf16(uint32_t code, float scale, float ws2) {
@@ -107,43 +108,173 @@ __global__ void __launch_bounds__(kPrepThreads) router_qdq_kernel(const uint8_t 
   }
 }
 
-// logits[t][e] = sum_h x[t][h] * wg[e][h]; warp w of a block owns expert e, lanes stride the
-// row in 8-element chunks (fp32 products and sums), then a butterfly reduction.
-__global__ void __launch_bounds__(kGateExperts * 32) router_logits_kernel(const uint16_t *__restrict__ x,
-                                                                          const uint16_t *__restrict__ wg, int64_t T,
-                                                                          int64_t E, int64_t H,
-                                                                          float *__restrict__ logits) {
-  pdl_wait();
-  pdl_trigger();
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int64_t e = static_cast<int64_t>(blockIdx.x) * kGateExperts + warp;
-  if (e >= E) return;
-  const int64_t t0 = static_cast<int64_t>(blockIdx.y) * kGateTokens;
-  const int64_t t1 = min(T, t0 + kGateTokens);
-  const uint4 *wrow = reinterpret_cast<const uint4 *>(wg + e * H);
-  const int64_t chunks = H / 8;
-  for (int64_t t = t0; t < t1; ++t) {
-    const uint4 *xrow = reinterpret_cast<const uint4 *>(x + t * H);
-    float acc = 0.f;
-    for (int64_t c = lane; c < chunks; c += 32) {
-      const uint4 a = __ldg(xrow + c), b = __ldg(wrow + c);
-      const uint32_t aw[4] = {a.x, a.y, a.z, a.w}, bw[4] = {b.x, b.y, b.z, b.w};
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        acc = __fadd_rn(acc, __fmul_rn(__uint_as_float(aw[i] << 16), __uint_as_float(bw[i] << 16)));
-        acc = __fadd_rn(acc, __fmul_rn(__uint_as_float(aw[i] & 0xFFFF0000u), __uint_as_float(bw[i] & 0xFFFF0000u)));
-      }
-    }
-#pragma unroll
-    for (int o = 16; o; o >>= 1) acc = __fadd_rn(acc, __shfl_xor_sync(0xffffffffu, acc, o));
-    if (lane == 0) logits[t * E + e] = acc;
-  }
+// ---------------------------------------------------------------- logits on the tensor cores
+
+constexpr int kRtTile = 128;            // tokens (MMA M) and experts (MMA N) per tile
+constexpr int kRtStageK = 64;           // bf16 elements of K per stage: 128 bytes per row
+constexpr int kRtStages = 4;
+constexpr int kRtBox = kRtTile * kRtStageK * 2;  // 16 KiB per operand and stage
+constexpr int kRtThreads = 192;         // warp 0 TMA, warp 1 MMA + TMEM, warps 2..5 epilogue
+constexpr size_t kRtSmem = 1024 + 2 * kRtStages * kRtBox + 128;
+// bf16 x bf16 -> fp32, K-major A and B, M = 128, N = 128
+constexpr uint32_t kRtIdesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t(kRtTile) >> 3) << 17) |
+                              ((uint32_t(kRtTile) >> 4) << 24);
+
+// D(tmem, fp32) (+)= A(smem, bf16) * B(smem, bf16)^T, M = 128, N = 128, K = 16.
+__device__ __forceinline__ void tc_mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                            uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
 }
 
-// One warp per token: softmax over E (<= 1024) logits, then top-k by repeated warp arg-max
-// (larger probability first, lower expert id on ties), weights renormalised over the k chosen.
-__global__ void router_topk_kernel(const float *__restrict__ logits, int64_t T, int64_t E, int topk,
-                                   int32_t *__restrict__ ids, float *__restrict__ weights) {
+// One CTA per (token tile, expert tile, K split): partial[split][t][e] = sum over the split's
+// K range of x[t][k] * wg[e][k] (fp32 from exact bf16 products), for t < T and e < E.  A
+// split with an empty K range writes zeros.
+__global__ void __launch_bounds__(kRtThreads, 1)
+    router_logits_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
+                            int T, int E, int H, int splits, int stages_per_split, float *__restrict__ partial,
+                            uint32_t *err) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                              ~static_cast<uintptr_t>(1023));
+  uint8_t *sA = smem;
+  uint8_t *sB = sA + kRtStages * kRtBox;
+  uint64_t *full = reinterpret_cast<uint64_t *>(sB + kRtStages * kRtBox);
+  uint64_t *empty = full + kRtStages;
+  uint64_t *done = empty + kRtStages;
+  uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(done + 1);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_holder + 1);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int n_tiles = (E + kRtTile - 1) / kRtTile;
+  const int split = static_cast<int>(blockIdx.x) % splits;
+  const int nt = (static_cast<int>(blockIdx.x) / splits) % n_tiles;
+  const int mt = static_cast<int>(blockIdx.x) / (splits * n_tiles);
+  const int k_total = H / kRtStageK;
+  const int k0 = min(k_total, split * stages_per_split), k1 = min(k_total, k0 + stages_per_split);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kRtStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    mbar_init(done, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    prefetch_tensormap(&tmX);
+    prefetch_tensormap(&tmW);
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_holder, kRtTile);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_holder;
+  pdl_wait();
+  pdl_trigger();
+
+  if (warp == 0) {
+    if (lane == 0 && k1 > k0) {
+      // ------------------------------------------------------------ TMA producer
+      const uint64_t pol_x = policy_evict_last();   // the token rows are re-read by every expert tile
+      const uint64_t pol_w = policy_evict_first();  // each gate row is read once per call
+      uint32_t issued = 0;
+      bool ok = true;
+      for (int k = k0; k < k1; ++k) {
+        const int i = k - k0, s = i % kRtStages;
+        const uint32_t ph = (i / kRtStages) & 1u;
+        if (!mbar_wait_bounded(&empty[s], ph ^ 1, abort_flag, err, kPipelineTimeoutNs)) {
+          ok = false;
+          break;
+        }
+        mbar_arrive_expect_tx(&full[s], 2 * kRtBox);
+        tma_load_2d(sA + s * kRtBox, &tmX, k * kRtStageK * 2, mt * kRtTile, &full[s], pol_x);
+        tma_load_2d(sB + s * kRtBox, &tmW, k * kRtStageK * 2, nt * kRtTile, &full[s], pol_w);
+        issued = (issued & ~(0x101u << s)) | (1u << s) | (ph << (s + 8));
+      }
+      if (!ok) {  // let the copies in flight land before the CTA leaves
+        volatile int never = 0;
+        for (int s = 0; s < kRtStages; ++s)
+          if (issued & (1u << s)) mbar_wait_bounded(&full[s], (issued >> (s + 8)) & 1u, &never, nullptr, 100000000ull);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0 && k1 > k0) {
+      // ------------------------------------------------------------ MMA issuer
+      bool ok = true;
+      const uint32_t sA0 = smem_u32(sA), sB0 = smem_u32(sB);
+      for (int k = k0; k < k1; ++k) {
+        const int i = k - k0, s = i % kRtStages;
+        if (!mbar_wait_bounded(&full[s], (i / kRtStages) & 1u, abort_flag, err, kPipelineTimeoutNs)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint64_t adesc = smem_desc(sA0 + s * kRtBox, 16, 1024, 2);
+        const uint64_t bdesc = smem_desc(sB0 + s * kRtBox, 16, 1024, 2);
+#pragma unroll
+        for (int j = 0; j < kRtStageK / 16; ++j)  // K = 16 per MMA: +32 bytes in the 128-byte row
+          tc_mma_bf16(tmem_base, adesc + 2 * j, bdesc + 2 * j, kRtIdesc, (i | j) != 0);
+        tc_commit(&empty[s]);
+      }
+      (void)ok;
+      tc_commit(done);  // fires once every MMA issued above has completed
+    }
+  } else {
+    // -------------------------------------------------------------- epilogue
+    const int quarter = warp & 3;
+    const int t = mt * kRtTile + quarter * 32 + lane;
+    bool ok = true;
+    if (k1 > k0) {
+      ok = mbar_wait_bounded(done, 0, abort_flag, err, kPipelineTimeoutNs);
+      ok = __all_sync(0xffffffffu, ok);
+      tc_fence_after();
+    }
+    float *dst = partial + (static_cast<int64_t>(split) * T + t) * E + nt * kRtTile;
+    const int e_live = min(kRtTile, E - nt * kRtTile);
+#pragma unroll 1
+    for (int c = 0; c < kRtTile / 16; ++c) {
+      uint32_t r[16];
+      if (k1 > k0 && ok) {
+        tmem_ld16(tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + c * 16, r);
+        tmem_ld_wait();
+      } else {
+#pragma unroll
+        for (int q = 0; q < 16; ++q) r[q] = 0u;
+      }
+      if (t < T && c * 16 < e_live) {  // E % 16 == 0 is not required: the tail is written one by one
+        if (c * 16 + 16 <= e_live) {
+          float4 *d4 = reinterpret_cast<float4 *>(dst + c * 16);
+#pragma unroll
+          for (int q = 0; q < 4; ++q)
+            d4[q] = make_float4(__uint_as_float(r[4 * q]), __uint_as_float(r[4 * q + 1]), __uint_as_float(r[4 * q + 2]),
+                                __uint_as_float(r[4 * q + 3]));
+        } else {
+          for (int q = 0; q < e_live - c * 16; ++q) dst[c * 16 + q] = __uint_as_float(r[q]);
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem_base, kRtTile);
+}
+
+// One warp per token: the logits are the sum of the K splits' partials (in split order), then
+// a softmax over E (<= 1024) logits, then top-k by repeated warp arg-max (larger probability
+// first, lower expert id on ties), weights renormalised over the k chosen.  logits (optional)
+// receives the summed logits.
+__global__ void router_topk_kernel(const float *__restrict__ partial, int splits, int64_t T, int64_t E, int topk,
+                                   int32_t *__restrict__ ids, float *__restrict__ weights,
+                                   float *__restrict__ logits) {
   pdl_wait();
   pdl_trigger();
   const int lane = threadIdx.x & 31;
@@ -155,7 +286,14 @@ __global__ void router_topk_kernel(const float *__restrict__ logits, int64_t T, 
 #pragma unroll
   for (int i = 0; i < kPer; ++i) {
     const int64_t e = lane + 32 * i;
-    p[i] = e < E ? logits[t * E + e] : -INFINITY;
+    if (e < E) {
+      float v = 0.f;
+      for (int sp = 0; sp < splits; ++sp) v = __fadd_rn(v, __ldg(partial + (sp * T + t) * E + e));
+      if (logits != nullptr) logits[t * E + e] = v;
+      p[i] = v;
+    } else {
+      p[i] = -INFINITY;
+    }
     mx = fmaxf(mx, p[i]);
   }
 #pragma unroll
@@ -225,16 +363,38 @@ cudaError_t launch_router_prepare(const uint8_t *w, const uint8_t *sf, const flo
                     static_cast<const uint32_t *>(partials), nparts, static_cast<uint16_t *>(wg));
 }
 
-cudaError_t launch_router(const void *x, int64_t T, int64_t H, const void *wg, int64_t E, int topk, int32_t *ids,
-                          float *weights, float *logits, cudaStream_t s) {
-  const dim3 grid(static_cast<unsigned>((E + kGateExperts - 1) / kGateExperts),
-                  static_cast<unsigned>((T + kGateTokens - 1) / kGateTokens));
-  cudaError_t e = launch_pdl(router_logits_kernel, grid, dim3(kGateExperts * 32), 0, s,
-                             static_cast<const uint16_t *>(x), static_cast<const uint16_t *>(wg), T, E, H, logits);
+int router_splits(int64_t T, int64_t E, int64_t H) {
+  const int64_t tiles = ((T + kRtTile - 1) / kRtTile) * ((E + kRtTile - 1) / kRtTile);
+  const int64_t k_total = H / kRtStageK;
+  int64_t splits = tiles > 0 ? kRouterTargetCtas / tiles : 1;
+  splits = splits < 1 ? 1 : (splits > kRouterMaxSplits ? kRouterMaxSplits : splits);
+  if (splits > k_total) splits = k_total > 0 ? k_total : 1;
+  const int64_t per = (k_total + splits - 1) / splits;  // no split is left without K stages
+  return static_cast<int>(per > 0 ? (k_total + per - 1) / per : 1);
+}
+
+cudaError_t launch_router(const CUtensorMap &tm_x, const CUtensorMap &tm_w, int64_t T, int64_t H, int64_t E, int topk,
+                          int32_t *ids, float *weights, float *logits, float *partial, uint32_t *err, cudaStream_t s) {
+  static bool attr_done[64] = {false};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 64 && !attr_done[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(router_logits_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(kRtSmem));
+    if (e != cudaSuccess) return e;
+    attr_done[dev] = true;
+  }
+  const int splits = router_splits(T, E, H);
+  const int64_t k_total = H / kRtStageK;
+  const int per = static_cast<int>((k_total + splits - 1) / splits);
+  const int64_t ctas = ((T + kRtTile - 1) / kRtTile) * ((E + kRtTile - 1) / kRtTile) * splits;
+  cudaError_t e = launch_pdl(router_logits_tc_kernel, dim3(static_cast<unsigned>(ctas)), dim3(kRtThreads), kRtSmem, s,
+                             tm_x, tm_w, static_cast<int>(T), static_cast<int>(E), static_cast<int>(H), splits, per,
+                             partial, err);
   if (e != cudaSuccess) return e;
   const int64_t blocks = (T + 7) / 8;
   return launch_pdl(router_topk_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, s,
-                    static_cast<const float *>(logits), T, E, topk, ids, weights);
+                    static_cast<const float *>(partial), splits, T, E, topk, ids, weights, logits);
 }
 
 }  // namespace nvfp4

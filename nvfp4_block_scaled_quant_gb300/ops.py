@@ -179,9 +179,9 @@ def router(x: torch.Tensor, wg: torch.Tensor, topk: int, want_logits: bool = Fal
     w = torch.empty(T, topk, dtype=torch.float32, device=x.device)
     logits = torch.empty(T, E, dtype=torch.float32, device=x.device) if want_logits else None
     n = int(lib().nvfp4_router_workspace_bytes(T, E))
-    ws = None if want_logits else _u8(max(n, 256), device=x.device)
+    ws = _u8(max(n, 256), device=x.device)
     call("nvfp4_router", x.data_ptr(), T, H, wg.data_ptr(), E, topk, ids.data_ptr(), w.data_ptr(), _ptr(logits),
-         _ptr(ws), 0 if ws is None else ws.numel(), _stream(stream))
+         ws.data_ptr(), ws.numel(), _stream(stream))
     return ids, w, logits
 
 

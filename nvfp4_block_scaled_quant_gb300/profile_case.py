@@ -4,12 +4,22 @@
     python -m nvfp4_block_scaled_quant_gb300.profile_case decode --T 1 --experts 384 --iters 8
     python -m nvfp4_block_scaled_quant_gb300.profile_case gemm --M 4096 --iters 3
     python -m nvfp4_block_scaled_quant_gb300.profile_case linear --M 32 --iters 3
+    python -m nvfp4_block_scaled_quant_gb300.profile_case dispatch --T 128 --iters 3
+    python -m nvfp4_block_scaled_quant_gb300.profile_case norm --M 128 --iters 3
+    python -m nvfp4_block_scaled_quant_gb300.profile_case router --T 128 --iters 3
+    python -m nvfp4_block_scaled_quant_gb300.profile_case quant --M 4096 --iters 3
 
 ``moe`` runs 128-token prefill chunks (hidden 7168, intermediate 2048, top-8
 Zipf(1.1) routing, shared expert) over ``--experts`` experts, so the weights
 held on the device stay a few GB while the per-tile work of every kernel is
 the same as in the 384-expert layer.  The kernels launch in the same order and
-configuration as in the benchmark.
+configuration as in the benchmark.  ``dispatch`` runs routing + amax + the
+quantise/permute of x for a 384-expert layer (the prefill chunks' routing at
+T = 128, the decode routing below, the 32 chunks at once for T = 4096; no expert
+weights are needed); ``norm`` the fused RMSNorm -> NVFP4 quantiser over hidden
+7168; ``router`` the router gate (384 experts, hidden 7168, top-8); ``quant``
+the activation quantiser over K = 7168 (M = 1024 .. 16384 are the large-GEMM
+sweep's activations).
 """
 
 from __future__ import annotations
@@ -24,7 +34,7 @@ from . import build as B
 
 def main(argv=None):
     p = argparse.ArgumentParser()
-    p.add_argument("case", choices=["moe", "decode", "gemm", "linear"])
+    p.add_argument("case", choices=["moe", "decode", "gemm", "linear", "dispatch", "norm", "router", "quant"])
     p.add_argument("--T", type=int, default=1)
     p.add_argument("--experts", type=int, default=64)
     p.add_argument("--M", type=int, default=4096)
@@ -67,6 +77,39 @@ def main(argv=None):
         y = torch.empty(a.M, N, dtype=torch.bfloat16, device=dev)
         for _ in range(a.iters):
             ops.gemm(q, sf, gs, K, dw.w, dw.sf, dw.ws2, N, out=y)
+    elif a.case == "dispatch":
+        T = a.T
+        cfg = workloads.PREFILL if T == 128 else (workloads.PREFILL_WHOLE if T == 4096 else workloads.DECODE[T])
+        W = ops.MoEWeights(cfg.E, cfg.H, cfg.I, *([torch.empty(0, device=dev)] * 6))  # shapes only
+        W.sh_w13 = torch.empty(0, device=dev)
+        ws = ops.moe_workspace(T, cfg.H, cfg.I, cfg.E, cfg.topk, True, dev)
+        g = torch.empty(1, dtype=torch.float32, device=dev)
+        if T == 4096:
+            x, ids, _ = workloads.prefill_whole(device="cpu")
+            ins = [(x.to(dev), ids.to(dev))] * a.iters
+        elif T == 128:
+            ins = [workloads.prefill_chunk(i, device=dev)[:2] for i in range(a.iters)]
+        else:
+            ins = [workloads.decode_step(T, step=i, device=dev)[:2] for i in range(a.iters)]
+        for x, ids in ins:
+            ops.moe_dispatch(x, ids, W, g, True, ws)
+    elif a.case == "norm":
+        K = 7168
+        gamma = workloads.norm_weight(K, seed=5, device=dev)
+        for i in range(a.iters):
+            x = workloads.activations(a.M, K, seed=500 + i, device=dev, outliers=True)
+            ops.rmsnorm_quantize(x, gamma, workloads.RMSNORM_EPS)
+    elif a.case == "router":
+        _, H, E, k = workloads.ROUTER[a.T]
+        q, sfw, ws2 = model.quantize_weight(workloads.weight(E, H, workloads.ROUTER_WEIGHT_SEED, dev))
+        wg = ops.router_prepare(q, sfw, ws2, E, H)
+        for i in range(a.iters):
+            x = workloads.activations(a.T, H, seed=40 + i, device=dev)
+            ops.router(x, wg, k)
+    elif a.case == "quant":
+        for i in range(a.iters):
+            x = workloads.activations(a.M, 7168, seed=80 + i, device=dev)
+            ops.quantize_act(x)
     else:
         K, N = 1536, 16384
         dw = model.make_dense_weight(N, K, seed=50, device=dev)
