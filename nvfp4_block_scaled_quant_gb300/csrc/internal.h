@@ -148,6 +148,10 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
 }
 
 // launchers (return cudaError_t of the launch)
+// Grid of the streaming kernels (quantisers): kStreamCtasPerSm CTAs of 256 threads per SM,
+// each walking its share of the blocks.
+constexpr int kStreamCtasPerSm = 4;
+int stream_grid_cap();
 cudaError_t launch_amax_partials(const void *x, int64_t M, int64_t K, int64_t ldx,
                                  uint32_t *partials, int nparts, cudaStream_t s);
 int amax_partial_count(int64_t M, int64_t K);

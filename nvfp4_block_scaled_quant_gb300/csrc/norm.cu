@@ -24,6 +24,10 @@ __device__ __forceinline__ float normed(float x, float inv, float g) {
   return bf16_round(__fmul_rn(__fmul_rn(x, inv), g));
 }
 
+// Chunks of 8 elements a thread keeps in registers between the two passes over a row: rows of
+// up to kNormCache * 256 * 8 elements are read once; longer rows are read again (from L2).
+constexpr int kNormCache = 4;
+
 __global__ void __launch_bounds__(kNormThreads) rmsnorm_stats_kernel(
     const uint16_t *__restrict__ x, int64_t M, int64_t K, int64_t ldx, const uint16_t *__restrict__ gamma,
     float eps, float *__restrict__ inv_rms, uint32_t *__restrict__ partials, uint16_t *__restrict__ y) {
@@ -33,12 +37,20 @@ __global__ void __launch_bounds__(kNormThreads) rmsnorm_stats_kernel(
   pdl_trigger();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nwarps = blockDim.x >> 5;
   const int64_t chunks = K / 8;
+  const bool cached = chunks <= static_cast<int64_t>(kNormCache) * blockDim.x;
   uint32_t m = 0;
   for (int64_t r = blockIdx.x; r < M; r += gridDim.x) {
     const uint4 *row = reinterpret_cast<const uint4 *>(x + r * ldx);
+    uint4 keep[kNormCache];
+    if (cached) {  // every chunk of the row is loaded before any is used
+#pragma unroll
+      for (int u = 0; u < kNormCache; ++u) {
+        const int64_t c = threadIdx.x + u * static_cast<int64_t>(blockDim.x);
+        keep[u] = c < chunks ? __ldg(row + c) : make_uint4(0u, 0u, 0u, 0u);
+      }
+    }
     float acc = 0.f;
-    for (int64_t c = threadIdx.x; c < chunks; c += blockDim.x) {
-      const uint4 v = __ldg(row + c);
+    auto add_squares = [&](const uint4 v) {
       const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
@@ -46,6 +58,14 @@ __global__ void __launch_bounds__(kNormThreads) rmsnorm_stats_kernel(
         acc = __fadd_rn(acc, __fmul_rn(a, a));
         acc = __fadd_rn(acc, __fmul_rn(b, b));
       }
+    };
+    // each thread sums its chunks c = tid, tid + 256, ... in increasing order (both paths)
+    if (cached) {
+#pragma unroll
+      for (int u = 0; u < kNormCache; ++u)
+        if (threadIdx.x + u * static_cast<int64_t>(blockDim.x) < chunks) add_squares(keep[u]);
+    } else {
+      for (int64_t c = threadIdx.x; c < chunks; c += blockDim.x) add_squares(__ldg(row + c));
     }
 #pragma unroll
     for (int o = 16; o; o >>= 1) acc = __fadd_rn(acc, __shfl_xor_sync(0xffffffffu, acc, o));
@@ -65,8 +85,8 @@ __global__ void __launch_bounds__(kNormThreads) rmsnorm_stats_kernel(
     __syncthreads();
     const float inv = s_inv;
     const uint4 *grow = reinterpret_cast<const uint4 *>(gamma);
-    for (int64_t c = threadIdx.x; c < chunks; c += blockDim.x) {
-      const uint4 v = __ldg(row + c), gv = __ldg(grow + c);
+    auto normalise = [&](int64_t c, const uint4 v) {
+      const uint4 gv = __ldg(grow + c);
       const uint32_t w[4] = {v.x, v.y, v.z, v.w}, gw[4] = {gv.x, gv.y, gv.z, gv.w};
       uint32_t o[4];
 #pragma unroll
@@ -78,6 +98,15 @@ __global__ void __launch_bounds__(kNormThreads) rmsnorm_stats_kernel(
         o[i] = bl | (bh << 16);
       }
       if (y) reinterpret_cast<uint4 *>(y + r * K)[c] = make_uint4(o[0], o[1], o[2], o[3]);
+    };
+    if (cached) {
+#pragma unroll
+      for (int u = 0; u < kNormCache; ++u) {
+        const int64_t c = threadIdx.x + u * static_cast<int64_t>(blockDim.x);
+        if (c < chunks) normalise(c, keep[u]);
+      }
+    } else {
+      for (int64_t c = threadIdx.x; c < chunks; c += blockDim.x) normalise(c, __ldg(row + c));
     }
     __syncthreads();  // red / s_inv are reused by the next row
   }
@@ -94,8 +123,10 @@ __global__ void __launch_bounds__(kNormThreads) rmsnorm_stats_kernel(
   }
 }
 
-// One thread per 16-element block of the normalised rows; layout as the plain quantiser.
-__global__ void __launch_bounds__(kNormThreads) rmsnorm_quantize_kernel(
+// 16-element blocks of the normalised rows, walked by a fixed grid as the plain quantiser
+// (kNormUnroll blocks' loads in flight per thread, gs derived once per CTA); same layouts.
+constexpr int kNormUnroll = 2;
+__global__ void __launch_bounds__(kNormThreads, kStreamCtasPerSm) rmsnorm_quantize_kernel(
     const uint16_t *__restrict__ x, int64_t M, int64_t K, int64_t ldx, const uint16_t *__restrict__ gamma,
     const float *__restrict__ inv_rms, const uint32_t *__restrict__ partials, int nparts,
     const float *__restrict__ gs_static, float *__restrict__ gs_out, uint8_t *__restrict__ q,
@@ -103,6 +134,31 @@ __global__ void __launch_bounds__(kNormThreads) rmsnorm_quantize_kernel(
   __shared__ uint32_t scratch[32];
   pdl_wait();
   pdl_trigger();
+  const int64_t kb = K / 16;
+  const int64_t total = rows_total * kb;
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  const int lane = threadIdx.x & 31;
+  const int64_t wbase0 = static_cast<int64_t>(blockIdx.x) * blockDim.x + (threadIdx.x & ~31);
+  uint4 a[kNormUnroll], b[kNormUnroll];
+  float inv[kNormUnroll];
+  auto load = [&](int64_t wb) {
+#pragma unroll
+    for (int u = 0; u < kNormUnroll; ++u) {
+      const int64_t g = wb + u * stride + lane;
+      a[u] = b[u] = make_uint4(0u, 0u, 0u, 0u);
+      inv[u] = 0.f;
+      if (g < total) {
+        const int64_t r = g / kb, c = g - r * kb;
+        if (r < M) {
+          const uint4 *src = reinterpret_cast<const uint4 *>(x + r * ldx + c * 16);
+          a[u] = __ldg(src);
+          b[u] = __ldg(src + 1);
+          inv[u] = __ldg(inv_rms + r);
+        }
+      }
+    }
+  };
+  load(wbase0);
   float gs;
   if (partials) {
     gs = gs_from_partials(partials, nparts, scratch);
@@ -111,39 +167,40 @@ __global__ void __launch_bounds__(kNormThreads) rmsnorm_quantize_kernel(
     gs = *gs_static;
   }
   const float six_gs = __fmul_rn(6.0f, gs);
-  const int64_t kb = K / 16;
-  const int64_t gb = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-  const bool valid = gb < rows_total * kb;
-  const int64_t r = valid ? gb / kb : 0;
-  const int64_t c = valid ? gb - r * kb : 0;
-  const bool live = valid && r < M;
-  uint32_t sfb = 0;
-  if (live) {
-    const uint4 *src = reinterpret_cast<const uint4 *>(x + r * ldx + c * 16);
-    const uint4 *gsrc = reinterpret_cast<const uint4 *>(gamma + c * 16);
-    const uint4 a = __ldg(src), b = __ldg(src + 1), ga = __ldg(gsrc), gb2 = __ldg(gsrc + 1);
-    const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
-    const uint32_t g[8] = {ga.x, ga.y, ga.z, ga.w, gb2.x, gb2.y, gb2.z, gb2.w};
-    const float inv = __ldg(inv_rms + r);
-    float v[16];
+  for (int64_t wb = wbase0; wb < total; wb += kNormUnroll * stride) {  // uniform over the warp
+    if (wb != wbase0) load(wb);
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      v[2 * i] = normed(__uint_as_float(w[i] << 16), inv, __uint_as_float(g[i] << 16));
-      v[2 * i + 1] = normed(__uint_as_float(w[i] & 0xFFFF0000u), inv, __uint_as_float(g[i] & 0xFFFF0000u));
+    for (int u = 0; u < kNormUnroll; ++u) {
+      const int64_t g = wb + u * stride + lane;
+      const bool valid = g < total;
+      const int64_t r = valid ? g / kb : 0, c = valid ? g - r * kb : 0;
+      const bool live = valid && r < M;
+      uint32_t sfb = 0;
+      if (live) {
+        const uint4 *gsrc = reinterpret_cast<const uint4 *>(gamma + c * 16);
+        const uint4 ga = __ldg(gsrc), gb2 = __ldg(gsrc + 1);
+        const uint32_t w[8] = {a[u].x, a[u].y, a[u].z, a[u].w, b[u].x, b[u].y, b[u].z, b[u].w};
+        const uint32_t gw[8] = {ga.x, ga.y, ga.z, ga.w, gb2.x, gb2.y, gb2.z, gb2.w};
+        float v[16];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          v[2 * i] = normed(__uint_as_float(w[i] << 16), inv[u], __uint_as_float(gw[i] << 16));
+          v[2 * i + 1] = normed(__uint_as_float(w[i] & 0xFFFF0000u), inv[u], __uint_as_float(gw[i] & 0xFFFF0000u));
+        }
+        uint32_t codes[2];
+        sfb = encode_block16(v, gs, six_gs, codes);
+        *reinterpret_cast<uint2 *>(q + r * (K / 2) + c * 8) = make_uint2(codes[0], codes[1]);
+      }
+      if (sf_layout == NVFP4_SF_LINEAR) {
+        if (live) sf[r * kb + c] = static_cast<uint8_t>(sfb);
+      } else {
+        uint32_t word = sfb << ((lane & 3) * 8);
+        word |= __shfl_xor_sync(0xffffffffu, word, 1);
+        word |= __shfl_xor_sync(0xffffffffu, word, 2);
+        if (valid && (lane & 3) == 0)
+          *reinterpret_cast<uint32_t *>(sf + sf_word_offset(r, c >> 2, kb >> 2)) = word;
+      }
     }
-    uint32_t codes[2];
-    sfb = encode_block16(v, gs, six_gs, codes);
-    *reinterpret_cast<uint2 *>(q + r * (K / 2) + c * 8) = make_uint2(codes[0], codes[1]);
-  }
-  if (sf_layout == NVFP4_SF_LINEAR) {
-    if (live) sf[r * kb + c] = static_cast<uint8_t>(sfb);
-  } else {
-    const int lane = threadIdx.x & 31;
-    uint32_t word = sfb << ((lane & 3) * 8);
-    word |= __shfl_xor_sync(0xffffffffu, word, 1);
-    word |= __shfl_xor_sync(0xffffffffu, word, 2);
-    if (valid && (lane & 3) == 0)
-      *reinterpret_cast<uint32_t *>(sf + sf_word_offset(r, c >> 2, kb >> 2)) = word;
   }
 }
 
@@ -162,7 +219,8 @@ cudaError_t launch_rmsnorm_quantize(const void *x, int64_t M, int64_t K, int64_t
                                     cudaStream_t s) {
   const int64_t rows_total = sf_layout == NVFP4_SF_LINEAR ? M : ((M + 127) / 128) * 128;
   const int64_t items = rows_total * (K / 16);
-  const int64_t blocks = items > 0 ? (items + kNormThreads - 1) / kNormThreads : 1;
+  int64_t blocks = items > 0 ? (items + kNormThreads - 1) / kNormThreads : 1;
+  if (blocks > stream_grid_cap()) blocks = stream_grid_cap();
   return launch_pdl(rmsnorm_quantize_kernel, dim3(static_cast<unsigned>(blocks)), dim3(kNormThreads), 0, s,
                     static_cast<const uint16_t *>(x), M, K, ldx, static_cast<const uint16_t *>(gamma), inv_rms,
                     partials, nparts, gs_static, gs_out, q, sf, sf_layout, rows_total);

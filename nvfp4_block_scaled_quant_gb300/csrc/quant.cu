@@ -57,9 +57,44 @@ __global__ void __launch_bounds__(kAmaxThreads) amax_partials_kernel(const uint1
   if (threadIdx.x == 0) partials[blockIdx.x] = m;
 }
 
-// One thread per 16-element block of a (M, K) bf16 tensor.  Swizzled output
-// also covers the padding rows up to a multiple of 128 (scale 0, no codes).
-__global__ void __launch_bounds__(kQuantThreads) quantize_kernel(
+// Encode one 16-element block (two 16-byte halves a, b of bf16 pairs) and store its codes;
+// returns the E4M3 scale byte.
+__device__ __forceinline__ uint32_t encode_and_store(uint4 a, uint4 b, float gs, float six_gs, uint8_t *qdst) {
+  const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+  float v[16];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    v[2 * i] = __uint_as_float(w[i] << 16);
+    v[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+  }
+  uint32_t codes[2];
+  const uint32_t sfb = encode_block16(v, gs, six_gs, codes);
+  *reinterpret_cast<uint2 *>(qdst) = make_uint2(codes[0], codes[1]);
+  return sfb;
+}
+
+// Store the scale byte of block (r, c): one byte (row-major layout) or, in the swizzled
+// layout, one 32-bit word per four consecutive blocks of a row, gathered from lanes 4i..4i+3
+// (all 32 lanes must call this together).
+__device__ __forceinline__ void store_scale(uint8_t *sf, int sf_layout, bool valid, bool live, int64_t r, int64_t c,
+                                            int64_t kb, uint32_t sfb) {
+  if (sf_layout == NVFP4_SF_LINEAR) {
+    if (live) sf[r * kb + c] = static_cast<uint8_t>(sfb);
+  } else {
+    const int lane = threadIdx.x & 31;
+    uint32_t word = sfb << ((lane & 3) * 8);
+    word |= __shfl_xor_sync(0xffffffffu, word, 1);
+    word |= __shfl_xor_sync(0xffffffffu, word, 2);
+    if (valid && (lane & 3) == 0) *reinterpret_cast<uint32_t *>(sf + sf_word_offset(r, c >> 2, kb >> 2)) = word;
+  }
+}
+
+// 16-element blocks of a (M, K) bf16 tensor, consecutive threads on consecutive blocks of a
+// row (so lanes 4i..4i+3 share one swizzled scale word; K % 64 == 0).  A fixed grid walks all
+// blocks with kQuantUnroll blocks' loads in flight per thread, and each CTA derives gs once.
+// The swizzled output also covers the padding rows up to a multiple of 128 (scale 0, no codes).
+constexpr int kQuantUnroll = 2;
+__global__ void __launch_bounds__(kQuantThreads, kStreamCtasPerSm) quantize_kernel(
     const uint16_t *__restrict__ x, int64_t M, int64_t K, int64_t ldx,
     const uint32_t *__restrict__ partials, int nparts, const float *__restrict__ gs_static,
     float *__restrict__ gs_out, uint8_t *__restrict__ q, uint8_t *__restrict__ sf,
@@ -68,37 +103,42 @@ __global__ void __launch_bounds__(kQuantThreads) quantize_kernel(
   pdl_wait();
   pdl_trigger();
   const int64_t kb = K / 16;
-  const int64_t gb = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-  const bool valid = gb < rows_total * kb;
-  const int64_t r = valid ? gb / kb : 0;
-  const int64_t c = valid ? gb - r * kb : 0;
-  const bool live = valid && r < M;
-  // the block's 16 elements are loaded first: their latency overlaps the gs reduction
-  uint4 a = make_uint4(0u, 0u, 0u, 0u), b = a;
-  if (live) {
-    const uint4 *src = reinterpret_cast<const uint4 *>(x + r * ldx + c * 16);
-    a = __ldg(src);
-    b = __ldg(src + 1);
-  }
+  const int64_t total = rows_total * kb;
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  const int lane = threadIdx.x & 31;
+  const int64_t wbase0 = static_cast<int64_t>(blockIdx.x) * blockDim.x + (threadIdx.x & ~31);
+  // the first blocks' loads are issued before the gs reduction, which their latency overlaps
+  uint4 a[kQuantUnroll], b[kQuantUnroll];
+  auto load = [&](int64_t wb) {
+#pragma unroll
+    for (int u = 0; u < kQuantUnroll; ++u) {
+      const int64_t g = wb + u * stride + lane;
+      a[u] = b[u] = make_uint4(0u, 0u, 0u, 0u);
+      if (g < total) {
+        const int64_t r = g / kb, c = g - r * kb;
+        if (r < M) {
+          const uint4 *src = reinterpret_cast<const uint4 *>(x + r * ldx + c * 16);
+          a[u] = __ldg(src);
+          b[u] = __ldg(src + 1);
+        }
+      }
+    }
+  };
+  load(wbase0);
   float gs = 0.f;
   if (nparts == 0) {
-    // Small input: every block with live rows reduces the whole of x itself (one launch
-    // fewer); blocks of padding rows only write zero scales and need no gs.  Block 0
-    // always reduces, so gs_out is written (0 when M == 0).  The condition is uniform
-    // over the block, so the reduction's barriers are safe.
-    if (blockIdx.x == 0 || static_cast<int64_t>(blockIdx.x) * blockDim.x / kb < M) {
-      uint32_t m = 0;
-      const int64_t chunks = K / 8;
-      for (int64_t i = threadIdx.x; i < M * chunks; i += blockDim.x) {
-        const int64_t rr = i / chunks;
-        const uint4 v = __ldg(reinterpret_cast<const uint4 *>(x + rr * ldx) + (i - rr * chunks));
-        m = max(m, max(max(max_abs_bf16x2(v.x), max_abs_bf16x2(v.y)),
-                       max(max_abs_bf16x2(v.z), max_abs_bf16x2(v.w))));
-      }
-      m = block_reduce_max(m, scratch);
-      gs = __fdiv_rn(__uint_as_float(m << 16), 2688.0f);
-      if (blockIdx.x == 0 && threadIdx.x == 0) *gs_out = gs;
+    // Small input (at most kInlineAmaxElems elements): every block reduces the whole of x
+    // itself, one launch fewer.  Block 0 writes gs (0 when M == 0).
+    uint32_t m = 0;
+    const int64_t chunks = K / 8;
+    for (int64_t i = threadIdx.x; i < M * chunks; i += blockDim.x) {
+      const int64_t rr = i / chunks;
+      const uint4 v = __ldg(reinterpret_cast<const uint4 *>(x + rr * ldx) + (i - rr * chunks));
+      m = max(m, max(max(max_abs_bf16x2(v.x), max_abs_bf16x2(v.y)), max(max_abs_bf16x2(v.z), max_abs_bf16x2(v.w))));
     }
+    m = block_reduce_max(m, scratch);
+    gs = __fdiv_rn(__uint_as_float(m << 16), 2688.0f);
+    if (blockIdx.x == 0 && threadIdx.x == 0) *gs_out = gs;
   } else if (partials) {
     gs = gs_from_partials(partials, nparts, scratch);
     if (blockIdx.x == 0 && threadIdx.x == 0) *gs_out = gs;
@@ -106,29 +146,18 @@ __global__ void __launch_bounds__(kQuantThreads) quantize_kernel(
     gs = *gs_static;
   }
   const float six_gs = __fmul_rn(6.0f, gs);
-  uint32_t sfb = 0;
-  if (live) {
-    const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
-    float v[16];
+  for (int64_t wb = wbase0; wb < total; wb += kQuantUnroll * stride) {  // uniform over the warp
+    if (wb != wbase0) load(wb);
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      v[2 * i] = __uint_as_float(w[i] << 16);
-      v[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+    for (int u = 0; u < kQuantUnroll; ++u) {
+      const int64_t g = wb + u * stride + lane;
+      const bool valid = g < total;
+      const int64_t r = valid ? g / kb : 0, c = valid ? g - r * kb : 0;
+      const bool live = valid && r < M;
+      uint32_t sfb = 0;
+      if (live) sfb = encode_and_store(a[u], b[u], gs, six_gs, q + r * (K / 2) + c * 8);
+      store_scale(sf, sf_layout, valid, live, r, c, kb, sfb);
     }
-    uint32_t codes[2];
-    sfb = encode_block16(v, gs, six_gs, codes);
-    *reinterpret_cast<uint2 *>(q + r * (K / 2) + c * 8) = make_uint2(codes[0], codes[1]);
-  }
-  if (sf_layout == NVFP4_SF_LINEAR) {
-    if (live) sf[r * kb + c] = static_cast<uint8_t>(sfb);
-  } else {
-    // lanes 4i..4i+3 hold the scale columns 4c'..4c'+3 of one row (kb % 4 == 0)
-    const int lane = threadIdx.x & 31;
-    uint32_t word = sfb << ((lane & 3) * 8);
-    word |= __shfl_xor_sync(0xffffffffu, word, 1);
-    word |= __shfl_xor_sync(0xffffffffu, word, 2);
-    if (valid && (lane & 3) == 0)
-      *reinterpret_cast<uint32_t *>(sf + sf_word_offset(r, c >> 2, kb >> 2)) = word;
   }
 }
 
@@ -186,13 +215,26 @@ cudaError_t launch_amax_partials(const void *x, int64_t M, int64_t K, int64_t ld
                     static_cast<const uint16_t *>(x), M, K, ldx, partials);
 }
 
+int stream_grid_cap() {
+  static int cached[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 1024;
+  if (cached[dev] == 0) {
+    int sms = 0;
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    cached[dev] = (sms > 0 ? sms : 128) * kStreamCtasPerSm;
+  }
+  return cached[dev];
+}
+
 cudaError_t launch_quantize(const void *x, int64_t M, int64_t K, int64_t ldx,
                             const uint32_t *partials, int nparts, const float *gs_static,
                             float *gs_out, uint8_t *q, uint8_t *sf, int sf_layout,
                             cudaStream_t s) {
   const int64_t rows_total = sf_layout == NVFP4_SF_LINEAR ? M : ((M + 127) / 128) * 128;
   const int64_t items = rows_total * (K / 16);
-  const int64_t blocks = items > 0 ? (items + kQuantThreads - 1) / kQuantThreads : 1;
+  int64_t blocks = items > 0 ? (items + kQuantThreads - 1) / kQuantThreads : 1;
+  if (blocks > stream_grid_cap()) blocks = stream_grid_cap();
   return launch_pdl(quantize_kernel, dim3(static_cast<unsigned>(blocks)), dim3(kQuantThreads), 0, s,
                     static_cast<const uint16_t *>(x), M, K, ldx, partials, nparts, gs_static, gs_out, q, sf,
                     sf_layout, rows_total);

@@ -268,32 +268,45 @@ __global__ void __launch_bounds__(kRtThreads, 1)
   if (warp == 1) tmem_dealloc(tmem_base, kRtTile);
 }
 
-// One warp per token: the logits are the sum of the K splits' partials (in split order), then
-// a softmax over E (<= 1024) logits, then top-k by repeated warp arg-max (larger probability
-// first, lower expert id on ties), weights renormalised over the k chosen.  logits (optional)
-// receives the summed logits.
-__global__ void router_topk_kernel(const float *__restrict__ partial, int splits, int64_t T, int64_t E, int topk,
-                                   int32_t *__restrict__ ids, float *__restrict__ weights,
-                                   float *__restrict__ logits) {
+// One CTA per token.  Its threads sum the K splits' partial logits of their experts (each
+// expert's partials in split order, so the logits are the same from call to call) into shared
+// memory; warp 0 then takes the softmax over E (<= 1024) logits and the top-k by repeated warp
+// arg-max (larger probability first, lower expert id on ties), weights renormalised over the
+// k chosen.  logits (optional) receives the summed logits.
+constexpr int kTopkThreads = 256;
+template <int kPer>  // experts per lane: E <= 32 * kPer
+__global__ void __launch_bounds__(kTopkThreads) router_topk_kernel(const float *__restrict__ partial, int splits,
+                                                                   int64_t T, int64_t E, int topk,
+                                                                   int32_t *__restrict__ ids,
+                                                                   float *__restrict__ weights,
+                                                                   float *__restrict__ logits) {
+  __shared__ float s_logit[kMaxExperts];
   pdl_wait();
   pdl_trigger();
-  const int lane = threadIdx.x & 31;
-  const int64_t t = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
-  if (t >= T) return;
-  constexpr int kPer = kMaxExperts / 32;
+  const int64_t t = blockIdx.x;
+  for (int64_t e = threadIdx.x; e < E; e += blockDim.x) {
+    const float *p = partial + t * E + e;
+    const int64_t sstride = T * E;
+    float v = 0.f;
+    int sp = 0;
+    for (; sp + 4 <= splits; sp += 4) {  // four loads in flight, summed in split order
+      const float a = __ldg(p + sp * sstride), b = __ldg(p + (sp + 1) * sstride), c = __ldg(p + (sp + 2) * sstride),
+                  d = __ldg(p + (sp + 3) * sstride);
+      v = __fadd_rn(__fadd_rn(__fadd_rn(__fadd_rn(v, a), b), c), d);
+    }
+    for (; sp < splits; ++sp) v = __fadd_rn(v, __ldg(p + sp * sstride));
+    s_logit[e] = v;
+    if (logits != nullptr) logits[t * E + e] = v;
+  }
+  __syncthreads();
+  if (threadIdx.x >= 32) return;
+  const int lane = threadIdx.x;
   float p[kPer];
   float mx = -INFINITY;
 #pragma unroll
   for (int i = 0; i < kPer; ++i) {
     const int64_t e = lane + 32 * i;
-    if (e < E) {
-      float v = 0.f;
-      for (int sp = 0; sp < splits; ++sp) v = __fadd_rn(v, __ldg(partial + (sp * T + t) * E + e));
-      if (logits != nullptr) logits[t * E + e] = v;
-      p[i] = v;
-    } else {
-      p[i] = -INFINITY;
-    }
+    p[i] = e < E ? s_logit[e] : -INFINITY;
     mx = fmaxf(mx, p[i]);
   }
 #pragma unroll
@@ -392,8 +405,10 @@ cudaError_t launch_router(const CUtensorMap &tm_x, const CUtensorMap &tm_w, int6
                              tm_x, tm_w, static_cast<int>(T), static_cast<int>(E), static_cast<int>(H), splits, per,
                              partial, err);
   if (e != cudaSuccess) return e;
-  const int64_t blocks = (T + 7) / 8;
-  return launch_pdl(router_topk_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, s,
+  auto kernel = E <= 128 ? router_topk_kernel<4>
+                         : (E <= 256 ? router_topk_kernel<8> : (E <= 512 ? router_topk_kernel<16> : router_topk_kernel<32>));
+  static_assert(32 * 32 >= kMaxExperts, "experts per lane");
+  return launch_pdl(kernel, dim3(static_cast<unsigned>(T)), dim3(kTopkThreads), 0, s,
                     static_cast<const float *>(partial), splits, T, E, topk, ids, weights, logits);
 }
 
