@@ -55,7 +55,7 @@
 extern "C" {
 #endif
 
-#define NVFP4_ABI_VERSION 5
+#define NVFP4_ABI_VERSION 6
 
 /* Exported symbols: the library builds with hidden visibility by default. */
 #if defined(NVFP4_BUILD) && defined(__GNUC__)
@@ -146,11 +146,17 @@ NVFP4_API nvfp4_status nvfp4_rmsnorm_quantize(const void *x, int64_t M, int64_t 
 /* ------------------------------------------------------------ weight prepare
  * Checkpoint-layout weights of G groups (experts): codes w (G, N, K/2) and
  * row-major E4M3 scales sf (G, N, K/16) used as stored, no transpose (page 2: the
- * checkpoint-layout fix, N-major codes and untransposed scales).  Writes w_out (G, N, K/2) and sf_out
- * (G blocks of nvfp4_sf_bytes(N, K)).  NVFP4_PREP_W13_INTERLEAVE reorders the
- * rows of a fused gate/up projection so that every 128-row tile holds 64 gate
- * rows followed by the 64 matching up rows (needs N % 128 == 0).  Run once at
- * load time; w and w_out must not overlap. */
+ * checkpoint-layout fix, N-major codes and untransposed scales).  Writes w_out
+ * (nvfp4_prepared_weight_bytes(G, N, K) bytes) and sf_out (G blocks of
+ * nvfp4_sf_bytes(N, K)).  The prepared codes are tile-major: for group g, 128-row tile t
+ * and 128-byte column slab s of the K/2 code bytes, block ((g * N/128 + t) * S + s),
+ * S = ceil(K/256), holds the tile's 128 rows x 128 bytes contiguously (row r at byte
+ * 128 r of the 16 KiB block); slab bytes past K/2 are zero codes.  A GEMM stage reads one
+ * such block.  NVFP4_PREP_W13_INTERLEAVE reorders the rows of a fused gate/up projection so
+ * that every 128-row tile holds 64 gate rows followed by the 64 matching up rows.
+ * K % 64 == 0, N % 128 == 0.  Run once at load time; w and w_out must not overlap.
+ * Every w / w13 / w2 / sh_* weight argument below is such a prepared buffer. */
+NVFP4_API size_t nvfp4_prepared_weight_bytes(int64_t G, int64_t N, int64_t K);
 NVFP4_API nvfp4_status nvfp4_prepare_weights(const uint8_t *w, const uint8_t *sf, int64_t G, int64_t N,
                                    int64_t K, int flags, uint8_t *w_out, uint8_t *sf_out,
                                    void *stream);

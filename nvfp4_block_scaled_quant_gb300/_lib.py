@@ -37,7 +37,7 @@ DEVERR_INTERNAL = 4
 LINEAR_NOALLOC_MAX_BYTES = 4 << 20
 
 
-ABI_VERSION = 5  # NVFP4_ABI_VERSION of the header these signatures follow
+ABI_VERSION = 6  # NVFP4_ABI_VERSION of the header these signatures follow
 
 
 class MoeWsLayout(Structure):
@@ -57,6 +57,7 @@ _SIGNATURES = {
     "nvfp4_quantize_workspace_bytes": (c_size_t, [I64, I64]),
     "nvfp4_quantize_act": (c_int, [P, I64, I64, I64, c_int, P, P, P, c_int, P, c_size_t, P]),
     "nvfp4_prepare_weights": (c_int, [P, P, I64, I64, I64, c_int, P, P, P]),
+    "nvfp4_prepared_weight_bytes": (c_size_t, [I64, I64, I64]),
     "nvfp4_rmsnorm_quantize_workspace_bytes": (c_size_t, [I64, I64]),
     "nvfp4_rmsnorm": (c_int, [P, I64, I64, I64, P, c_float, P, P]),
     "nvfp4_rmsnorm_quantize": (c_int, [P, I64, I64, I64, P, c_float, c_int, P, P, P, c_int, P, P, c_size_t, P]),

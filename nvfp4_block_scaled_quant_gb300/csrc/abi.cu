@@ -129,6 +129,13 @@ nvfp4_status make_map(const char *fn, CUtensorMap *m, const void *base, int64_t 
   return NVFP4_OK;
 }
 
+// Prepared (tile-major) weights of rows x K: blocks of 128 rows x 128 bytes, read through a
+// map of 128-byte rows with 128-row boxes.
+nvfp4_status make_weight_map(const char *fn, CUtensorMap *m, const void *w, int64_t rows, int64_t K) {
+  const int64_t slabs = (K / 2 + 127) / 128;
+  return make_map(fn, m, w, 128, rows * slabs, 128, 128);
+}
+
 size_t align256(size_t v) { return (v + 255) & ~static_cast<size_t>(255); }
 int64_t round_up(int64_t v, int64_t a) { return (v + a - 1) / a * a; }
 
@@ -263,9 +270,9 @@ nvfp4_status moe_gemm_impl(const char *fn, DeviceInfo *d, Epi epi, int64_t T, in
   CUtensorMap ta, tb, tbs;
   nvfp4_status st = make_map(fn, &ta, at<uint8_t>(ws, w13 ? L.xq : L.hq), K / 2, L.rows_capacity, K / 2, kABoxRows);
   if (st != NVFP4_OK) return st;
-  if ((st = make_map(fn, &tb, w, K / 2, E * N, K / 2, kBlockN)) != NVFP4_OK) return st;
+  if ((st = make_weight_map(fn, &tb, w, E * N, K)) != NVFP4_OK) return st;
   if (has_shared) {
-    if ((st = make_map(fn, &tbs, sh_w, K / 2, N, K / 2, kBlockN)) != NVFP4_OK) return st;
+    if ((st = make_weight_map(fn, &tbs, sh_w, N, K)) != NVFP4_OK) return st;
   } else {
     tbs = tb;
   }
@@ -454,6 +461,11 @@ nvfp4_status nvfp4_rmsnorm_quantize(const void *x, int64_t M, int64_t K, int64_t
   return NVFP4_OK;
 }
 
+size_t nvfp4_prepared_weight_bytes(int64_t G, int64_t N, int64_t K) {
+  if (G <= 0 || N <= 0 || K <= 0 || K % 64 || N % 128) return 0;
+  return static_cast<size_t>(G) * static_cast<size_t>(N) * static_cast<size_t>((K / 2 + 127) / 128) * 128u;
+}
+
 nvfp4_status nvfp4_prepare_weights(const uint8_t *w, const uint8_t *sf, int64_t G, int64_t N, int64_t K, int flags,
                                    uint8_t *w_out, uint8_t *sf_out, void *stream) {
   NV_REQUIRE(w && sf && w_out && sf_out, NVFP4_ERR_INVALID_ARG, "NULL pointer argument");
@@ -490,7 +502,7 @@ static nvfp4_status gemm_dense(const char *fn, DeviceInfo *d, const uint8_t *xq,
   CUtensorMap ta, tb;
   nvfp4_status st = make_map(fn, &ta, xq, G * K / 2, M, G * K / 2, pair_clusters > 0 ? 128 : kABoxRows);
   if (st != NVFP4_OK) return st;
-  if ((st = make_map(fn, &tb, w, K / 2, G * N, K / 2, kBlockN)) != NVFP4_OK) return st;
+  if ((st = make_weight_map(fn, &tb, w, G * N, K)) != NVFP4_OK) return st;
   GemmArgs a;
   std::memset(&a, 0, sizeof(a));
   a.G = static_cast<int>(G);
@@ -529,7 +541,7 @@ static nvfp4_status linear_fused(const char *fn, DeviceInfo *d, const void *x, i
                                  int64_t N, const uint8_t *w, const uint8_t *w_sf, const float *ws2, bool dyn,
                                  float *gs, void *y, cudaStream_t s) {
   CUtensorMap tb;
-  nvfp4_status st = make_map(fn, &tb, w, K / 2, G * N, K / 2, kBlockN);
+  nvfp4_status st = make_weight_map(fn, &tb, w, G * N, K);
   if (st != NVFP4_OK) return st;
   GemmArgs a;
   std::memset(&a, 0, sizeof(a));

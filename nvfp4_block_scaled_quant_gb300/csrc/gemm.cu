@@ -263,7 +263,7 @@ __global__ void __launch_bounds__(kGemmThreads, kQuantA ? 1 : kCtasPerSm)
           for (int s = 0; s < early; ++s) {
             const int kv = min(4, k_steps - 4 * s);
             mbar_expect_tx(&full[s], kTileBytesB + kv * kSfBytesPerKStep);
-            tma_load_2d(sB + s * kTileBytesB, mb, s * (kStageK / 2), b_row0, &full[s], pol_w);
+            tma_load_2d(sB + s * kTileBytesB, mb, 0, (b_row0 / kBlockN * k_stages + s) * kBlockN, &full[s], pol_w);
             bulk_load(sSFB + s * kSfBytesStage, sfb + static_cast<size_t>(s) * kSfBytesStage,
                       kv * kSfBytesPerKStep, &full[s], pol_w);
           }
@@ -314,7 +314,8 @@ __global__ void __launch_bounds__(kGemmThreads, kQuantA ? 1 : kCtasPerSm)
                       kv * kSfBytesPerKStep, &full[stage], pol_a);
           }
           if (!b_done) {
-            tma_load_2d(sB + stage * kTileBytesB, mb, ks * (kStageK / 2), b_row0, &full[stage],
+            // the tile-major weights: block (tile, stage) is 128 rows of 128 bytes, contiguous
+            tma_load_2d(sB + stage * kTileBytesB, mb, 0, (b_row0 / kBlockN * k_stages + ks) * kBlockN, &full[stage],
                         pol_w);
             bulk_load(sSFB + stage * kSfBytesStage, sfb + static_cast<size_t>(ks) * kSfBytesStage,
                       kv * kSfBytesPerKStep, &full[stage], pol_w);

@@ -148,7 +148,8 @@ __global__ void __launch_bounds__(kPThreads, 1)
           mbar_arrive_expect_tx(&full[stage], bytes);
           // rows of A beyond M read as zeros (out-of-range box rows); their outputs are dropped
           tma_load_2d(sA + stage * kPTileA, &tmA, ks * (kStageK / 2), a_row, &full[stage], pol_a);
-          tma_load_2d(sB + stage * kPTileB, &tmB, ks * (kStageK / 2), b_row, &full[stage], pol_b);
+          // tile-major weights: block (128-row tile, stage) is contiguous
+          tma_load_2d(sB + stage * kPTileB, &tmB, 0, (b_row / kPHalf * k_stages + ks) * kPHalf, &full[stage], pol_b);
           if (sfa_live)
             bulk_load(sSFA + stage * kSfBytesStage, sfa + static_cast<size_t>(ks) * kSfBytesStage,
                       kv * kSfBytesPerKStep, &full[stage], pol_a);

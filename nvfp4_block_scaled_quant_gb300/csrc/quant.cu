@@ -161,9 +161,11 @@ __global__ void __launch_bounds__(kQuantThreads, kStreamCtasPerSm) quantize_kern
   }
 }
 
-// Prepared weight layout.  Codes: 16-byte chunks, row permuted for the w13
-// interleave.  Scales: one 32-bit word (4 scales) per thread, written in the
-// swizzled layout.
+// Prepared weight layout.  Codes are tile-major: for each group, 128-row tile and 128-byte
+// column slab of K (256 FP4 elements), the tile's 128 rows x 128 bytes sit in one contiguous
+// 16 KiB block (row r of the tile at 128 r), rows permuted for the w13 interleave and slabs
+// past K/2 bytes filled with zero codes; a GEMM stage then reads one contiguous block.
+// Scales: one 32-bit word (4 scales) per thread, written in the swizzled layout.
 __device__ __forceinline__ int64_t interleave_src_row(int64_t n, int64_t N, int flags) {
   if (!(flags & NVFP4_PREP_W13_INTERLEAVE)) return n;
   const int64_t tile = n >> 7, j = n & 127;
@@ -175,19 +177,25 @@ __global__ void prepare_kernel(const uint8_t *__restrict__ w, const uint8_t *__r
                                uint8_t *__restrict__ w_out, uint8_t *__restrict__ sf_out) {
   pdl_wait();
   pdl_trigger();
-  const int64_t row_chunks = K / 32;              // 16-byte chunks per packed row
-  const int64_t code_items = G * N * row_chunks;
+  const int64_t row_bytes = K / 2;                // a multiple of 32 (K % 64 == 0)
+  const int64_t slabs = (row_bytes + 127) / 128;  // 128-byte column slabs per row
+  const int64_t tiles = N / 128;
+  const int64_t code_items = G * tiles * slabs * 1024;  // 16-byte chunks of the tile-major blocks
   const int64_t words_per_group = N * K / 64;     // 4 scales per word
   const int64_t total = code_items + G * words_per_group;
   const int64_t kb = K / 16, kc4 = K / 64;
   for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
        i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
     if (i < code_items) {
-      const int64_t row = i / row_chunks, ch = i - row * row_chunks;
-      const int64_t g = row / N, n = row - g * N;
-      const int64_t src = g * N + interleave_src_row(n, N, flags);
-      reinterpret_cast<uint4 *>(w_out + row * (K / 2))[ch] =
-          __ldg(reinterpret_cast<const uint4 *>(w + src * (K / 2)) + ch);
+      const int64_t blk = i >> 10, within = i & 1023;  // block (group, tile, slab); 16-byte chunk
+      const int64_t r = within >> 3, c16 = within & 7;
+      const int64_t tile = blk / slabs, s = blk - tile * slabs;
+      const int64_t g = tile / tiles, nt = tile - g * tiles;
+      const int64_t src = g * N + interleave_src_row(nt * 128 + r, N, flags);
+      const int64_t byte = s * 128 + c16 * 16;
+      const uint4 v = byte < row_bytes ? __ldg(reinterpret_cast<const uint4 *>(w + src * row_bytes + byte))
+                                       : make_uint4(0u, 0u, 0u, 0u);
+      reinterpret_cast<uint4 *>(w_out)[i] = v;
     } else {
       const int64_t j = i - code_items;
       const int64_t g = j / words_per_group, wi = j - g * words_per_group;

@@ -97,10 +97,11 @@ def rmsnorm_quantize(x: torch.Tensor, gamma: torch.Tensor, eps: float = 1e-6, gs
 
 def prepare_weights(w: torch.Tensor, sf: torch.Tensor, N: int, K: int, interleave_w13: bool = False,
                     stream=None) -> Tuple[torch.Tensor, torch.Tensor]:
-    """Checkpoint codes (G, N, K/2) + row-major scales (G, N, K/16) -> prepared codes + swizzled scales."""
+    """Checkpoint codes (G, N, K/2) + row-major scales (G, N, K/16) -> prepared (tile-major) codes
+    + swizzled scales."""
     _cuda(w, sf)
     G = w.numel() // (N * K // 2)
-    w_out = torch.empty_like(w)
+    w_out = _u8(int(lib().nvfp4_prepared_weight_bytes(G, N, K)), device=w.device)
     sf_out = _u8(G * sf_bytes(N, K), device=w.device)
     call("nvfp4_prepare_weights", w.data_ptr(), sf.data_ptr(), G, N, K,
          _lib.PREP_W13_INTERLEAVE if interleave_w13 else _lib.PREP_PLAIN, w_out.data_ptr(), sf_out.data_ptr(),

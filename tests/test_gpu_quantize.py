@@ -117,6 +117,12 @@ def test_prepare_weights_layout():
                             for n in range(N)])
         else:
             src = np.arange(N)
+        # tile-major codes: block (g, tile, slab) = 128 rows x 128 bytes, the slab past K/2 zero
+        slabs = (K // 2 + 127) // 128
+        assert wo.size == G * N * slabs * 128
+        blocks = wo.reshape(G, N // 128, slabs, 128, 128)
+        rows = blocks.transpose(0, 1, 3, 2, 4).reshape(G, N, slabs * 128)
+        np.testing.assert_array_equal(rows[:, :, K // 2:], 0)
         for g in range(G):
-            np.testing.assert_array_equal(wo[g], w[g][src])
+            np.testing.assert_array_equal(rows[g, :, : K // 2], w[g][src])
             np.testing.assert_array_equal(O.unswizzle_sf(sfo[g], N, K), sf[g][src])
