@@ -258,10 +258,28 @@ nvfp4_status moe_dispatch_impl(const char *fn, DeviceInfo *d, const void *x, int
   return NVFP4_OK;
 }
 
+// One-token w13 (nvfp4_moe_forward at T = 1): the w13 CTAs quantise x themselves and take
+// their schedule from the top-k ids, so no dispatch launch runs and the weights stream while
+// the routing kernel is still working.
+struct Tok1 {
+  const void *x;
+  const int32_t *ids;
+  bool dynamic;
+  float *a1_gs;
+};
+
+bool tok1_applies(int64_t T, int64_t H, int topk) { return T == 1 && topk <= kTok1MaxTopk && H <= kTok1MaxK; }
+
+// Weight stages of a GEMM's first tile prefetched into L2 beyond its ring before the
+// previous launch of the chain completes (w13, w2).
+constexpr int kEarlyL2W13 = 0;
+constexpr int kEarlyL2W2 = 4;
+
 nvfp4_status moe_gemm_impl(const char *fn, DeviceInfo *d, Epi epi, int64_t T, int64_t H, int64_t I, int64_t E,
                            int topk, const uint8_t *w, const uint8_t *w_sf, const float *w_ws2,
                            const uint8_t *sh_w, const uint8_t *sh_sf, const float *sh_ws2, const float *gs_a,
-                           const float *gs_out, const float *topk_w, float *h_debug, void *ws, cudaStream_t s) {
+                           const float *gs_out, const float *topk_w, float *h_debug, void *ws, cudaStream_t s,
+                           const Tok1 *tok1 = nullptr) {
   const int has_shared = sh_w != nullptr;
   const nvfp4_moe_ws_layout L = moe_layout(T, H, I, E, topk, has_shared);
   if (T == 0) return NVFP4_OK;
@@ -297,6 +315,7 @@ nvfp4_status moe_gemm_impl(const char *fn, DeviceInfo *d, Epi epi, int64_t T, in
   a.gs_out = gs_out;
   a.err = d->flags;
   a.early_b = 1;  // dispatch (or w13) precedes this launch; routing and weights are older
+  a.early_l2 = w13 ? kEarlyL2W13 : kEarlyL2W2;
   if (w13) {
     a.out = at<uint8_t>(ws, L.hq);
     a.out_sf = at<uint8_t>(ws, L.hsf);
@@ -308,6 +327,18 @@ nvfp4_status moe_gemm_impl(const char *fn, DeviceInfo *d, Epi epi, int64_t T, in
     a.sorted_idx = at<int>(ws, L.sorted_idx);
     a.topk_w = topk_w;
     a.topk = topk;
+  }
+  if (tok1 != nullptr) {
+    a.qa_x = tok1->x;
+    a.qa_ld = H;
+    a.qa_gs_static = tok1->dynamic ? nullptr : tok1->a1_gs;
+    a.qa_gs_out = tok1->dynamic ? tok1->a1_gs : nullptr;
+    a.tok1_ids = tok1->ids;
+    a.tok1_E = static_cast<int>(E);
+    a.topk = topk;
+    a.early_b = 0;  // nothing is read before the wait but the ids and the weights
+    NV_CUDA(launch_gemm_tok1(tb, tbs, a, d->sms * kCtasPerSm, s), "one-token w13 launch");
+    return NVFP4_OK;
   }
   // The routing cut the groups into tiles of moe_tile_rows(T) rows: 32-row tiles fit one
   // A box each, so the ring with 4 small stages applies.
@@ -913,12 +944,26 @@ nvfp4_status nvfp4_moe_forward(const void *x, int64_t T, int64_t H, int64_t I, i
   DeviceInfo *d;
   if ((st = device_info(__func__, &d)) != NVFP4_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if ((st = moe_dispatch_impl(__func__, d, x, T, H, I, E, topk, topk_ids, has_shared, a1_gs_mode, a1_gs, ws, s)) !=
-      NVFP4_OK)
-    return st;
-  if ((st = moe_gemm_impl(__func__, d, Epi::kW13, T, H, I, E, topk, w13, w13_sf, w13_ws2, sh_w13, sh_w13_sf, sh_ws2,
-                          a1_gs, a2_gs, nullptr, nullptr, ws, s)) != NVFP4_OK)
-    return st;
+  if (tok1_applies(T, H, topk)) {
+    // routing and the zeroing of y_acc only; the w13 CTAs reduce the amax and quantise
+    const nvfp4_moe_ws_layout L = moe_layout(T, H, I, E, topk, has_shared);
+    RouteBufs rb = route_bufs(ws, L);
+    rb.tile_shift = moe_tile_shift(T);
+    NV_CUDA(launch_route_amax(topk_ids, 1, topk, static_cast<int>(E), has_shared, rb, nullptr, H, nullptr, 0,
+                              at<float>(ws, L.y_acc), d->flags, s),
+            "route kernel launch");
+    const Tok1 tok1{x, topk_ids, a1_gs_mode == NVFP4_GS_DYNAMIC, a1_gs};
+    if ((st = moe_gemm_impl(__func__, d, Epi::kW13, T, H, I, E, topk, w13, w13_sf, w13_ws2, sh_w13, sh_w13_sf,
+                            sh_ws2, a1_gs, a2_gs, nullptr, nullptr, ws, s, &tok1)) != NVFP4_OK)
+      return st;
+  } else {
+    if ((st = moe_dispatch_impl(__func__, d, x, T, H, I, E, topk, topk_ids, has_shared, a1_gs_mode, a1_gs, ws,
+                                s)) != NVFP4_OK)
+      return st;
+    if ((st = moe_gemm_impl(__func__, d, Epi::kW13, T, H, I, E, topk, w13, w13_sf, w13_ws2, sh_w13, sh_w13_sf,
+                            sh_ws2, a1_gs, a2_gs, nullptr, nullptr, ws, s)) != NVFP4_OK)
+      return st;
+  }
   if ((st = moe_gemm_impl(__func__, d, Epi::kW2, T, H, I, E, topk, w2, w2_sf, w2_ws2, sh_w2, sh_w2_sf, sh_ws2, a2_gs,
                           nullptr, topk_w, nullptr, ws, s)) != NVFP4_OK)
     return st;

@@ -123,6 +123,19 @@ __device__ __forceinline__ void bulk_load(void *smem_dst, const void *gmem_src, 
       : "memory");
 }
 
+// L2 prefetch of one box of a tensor map (innermost coordinate 16-byte aligned) and of a
+// contiguous range (16-byte aligned, a multiple of 16 bytes); neither waits for the data.
+__device__ __forceinline__ void tma_prefetch_l2_2d(const CUtensorMap *map, int32_t x, int32_t y) {
+  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(x), "r"(y)
+               : "memory");
+}
+
+__device__ __forceinline__ void bulk_prefetch_l2(const void *src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
 __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap *map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
@@ -399,6 +412,25 @@ __device__ __forceinline__ uint32_t encode_block16(const float (&v)[16], float g
   codes[0] = w[0];
   codes[1] = w[1];
   return sf;
+}
+
+// The same encoding with one 16-element block spread over four consecutive lanes
+// (lanes 4b..4b+3 of the warp; every lane of the warp calls it): each lane holds
+// four of the block's elements in v, in order.  The block amax is exchanged with
+// shuffles and every lane derives the scale the same way encode_block16 does.
+// Returns this lane's two code bytes (its first element in the low nibble of the
+// low byte); *sf receives the block's E4M3 scale byte.
+__device__ __forceinline__ uint32_t encode_block16_x4(float4 v, float gs, float six_gs, uint32_t *sf) {
+  float amax = fmaxf(fmaxf(fmaxf(fmaxf(0.f, fabsf(v.x)), fabsf(v.y)), fabsf(v.z)), fabsf(v.w));
+  amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+  amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+  const float s = (six_gs == 0.f) ? 0.f : __fdiv_rn(amax, six_gs);
+  *sf = f32_to_ue4m3(s);
+  const float d = __fmul_rn(ue4m3_to_f32(*sf), gs);
+  const float r = __frcp_rn(d);
+  if (d == 0.f || isinf(r)) return 0u;
+  return e2m1x2_signed(__fmul_rn(v.x, r), __fmul_rn(v.y, r)) |
+         (e2m1x2_signed(__fmul_rn(v.z, r), __fmul_rn(v.w, r)) << 8);
 }
 
 // Byte offset of the 32-bit word holding scales (row r, columns 4c'..4c'+3) in

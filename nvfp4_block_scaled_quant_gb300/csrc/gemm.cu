@@ -156,12 +156,89 @@ __device__ float quantize_resident_a(const GemmArgs &a, int g, uint8_t *sA, uint
   return gs;
 }
 
+// One-token MoE w13 (T = 1): the four epilogue warps (tid 0..127, named barrier 1) take gs
+// (dynamic: fl32(amax / 2688) over the token's K elements; static: read; CTA 0 writes a
+// dynamic one out), encode the row with the activation quantiser's arithmetic and write its
+// codes into all eight rows of the resident atom of every K stage (the atom of stage s is the
+// 1 KB at s * 1024; 16-byte chunk c of row r sits at chunk c ^ r) and the row's scale bytes,
+// one per 16 elements in K order, into sfa (four per 64-element K step: one 32-bit word).
+__device__ float quantize_token_a(const GemmArgs &a, uint8_t *sA, uint8_t *sfa, uint32_t *scratch, int tid) {
+  const int64_t K = a.K;
+  const uint16_t *x = static_cast<const uint16_t *>(a.qa_x);
+  const int warp = tid >> 5, lane = tid & 31;
+  float gs;
+  if (a.qa_gs_static == nullptr) {
+    uint32_t m = 0;
+    for (int64_t c = tid; c < K / 8; c += 128) {
+      const uint4 v = __ldg(reinterpret_cast<const uint4 *>(x) + c);
+      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int k = 0; k < 4; ++k) m = max(m, max(w[k] & 0x7FFFu, (w[k] >> 16) & 0x7FFFu));
+    }
+#pragma unroll
+    for (int o = 16; o; o >>= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, o));
+    if (lane == 0) scratch[warp] = m;
+    named_barrier_sync(1, 128);
+    m = max(max(scratch[0], scratch[1]), max(scratch[2], scratch[3]));
+    gs = __fdiv_rn(__uint_as_float(m << 16), 2688.0f);
+  } else {
+    gs = __ldg(a.qa_gs_static);
+  }
+  if (blockIdx.x == 0 && tid == 0 && a.qa_gs_out != nullptr) *a.qa_gs_out = gs;
+  const float six_gs = __fmul_rn(6.0f, gs);
+  for (int64_t c = tid; c < K / 16; c += 128) {  // 16-element block c of the row
+    const uint4 *src = reinterpret_cast<const uint4 *>(x + c * 16);
+    const uint4 p = __ldg(src), q = __ldg(src + 1);
+    const uint32_t w[8] = {p.x, p.y, p.z, p.w, q.x, q.y, q.z, q.w};
+    float v[16];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      v[2 * k] = __uint_as_float(w[k] << 16);
+      v[2 * k + 1] = __uint_as_float(w[k] & 0xFFFF0000u);
+    }
+    uint32_t codes[2];
+    const uint32_t sfb = encode_block16(v, gs, six_gs, codes);
+    const int st = static_cast<int>(c >> 4), j = static_cast<int>(c & 15);
+#pragma unroll
+    for (int r = 0; r < 8; ++r)
+      *reinterpret_cast<uint2 *>(sA + st * 1024 + r * 128 + (((j >> 1) ^ r) * 16) + (j & 1) * 8) =
+          make_uint2(codes[0], codes[1]);
+    sfa[c] = static_cast<uint8_t>(sfb);
+  }
+  fence_proxy_async_shared();  // the MMAs read the atoms through the async proxy
+  named_barrier_sync(1, 128);
+  return gs;
+}
+
+// One-token MoE w13: the schedule the routing kernel writes, derived from the token's top-k
+// ids by warp 0 (every lane calls this; topk <= 32).  The groups are the distinct valid ids
+// in increasing order, each one 32-row tile of as many rows as the id occurs (padded
+// segments of 128 rows: group i starts at row 128 i), then the shared group with the one
+// token.  Entry i = (group, m tile 0, rows, first row); sched[15].x = the group count.
+__device__ void tok1_schedule(const GemmArgs &a, int4 *sched, int lane) {
+  int id = lane < a.topk ? __ldg(a.tok1_ids + lane) : -1;
+  if (id < 0 || id >= a.tok1_E) id = -1;  // dropped, as the routing kernel drops it
+  const unsigned same = __match_any_sync(0xffffffffu, id);
+  const bool leader = id >= 0 && __ffs(same) - 1 == lane;
+  const unsigned lead = __ballot_sync(0xffffffffu, leader);
+  int rank = 0;  // distinct valid ids below this one
+  for (unsigned m = lead; m; m &= m - 1) rank += __shfl_sync(0xffffffffu, id, __ffs(m) - 1) < id;
+  if (leader) sched[rank] = make_int4(id, 0, __popc(same), kBlockM * rank);
+  const int nd = __popc(lead);
+  if (lane == 0) {
+    if (a.shared_group >= 0) sched[nd] = make_int4(a.shared_group, 0, 1, kBlockM * nd);
+    sched[15] = make_int4(nd + (a.shared_group >= 0 ? 1 : 0), 0, 0, 0);
+  }
+}
+
 template <int kEpi, bool kSmallA, bool kQuantA>
-__global__ void __launch_bounds__(kGemmThreads, kQuantA ? 1 : kCtasPerSm)
+__global__ void __launch_bounds__(kGemmThreads, (kQuantA && kEpi != static_cast<int>(Epi::kW13)) ? 1 : kCtasPerSm)
     nvfp4_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                       const __grid_constant__ CUtensorMap tmB,
                       const __grid_constant__ CUtensorMap tmBs, const GemmArgs args) {
-  using R = Ring<kSmallA, kQuantA>;
+  // kQuantA with the W13 epilogue: the one-token MoE w13 (resident token atoms, schedule from ids)
+  constexpr bool kTok1 = kQuantA && kEpi == static_cast<int>(Epi::kW13);
+  using R = Ring<kSmallA, kQuantA, kTok1>;
   constexpr int S = R::kStagesR;    // stages in the ring
   constexpr int kAB = R::kABytes;   // A slot per stage (kQuantA: per K stage, resident)
   extern __shared__ uint8_t smem_raw[];
@@ -170,16 +247,20 @@ __global__ void __launch_bounds__(kGemmThreads, kQuantA ? 1 : kCtasPerSm)
   uint8_t *sA = smem;
   uint8_t *sB = sA + R::kASlots * kAB;
   uint8_t *sSFA = sB + S * kTileBytesB;
-  uint8_t *sSFB = sSFA + R::kASlots * kSfBytesStage;
+  uint8_t *sSFB = sSFA + R::kSfaBytes;
   uint64_t *full = reinterpret_cast<uint64_t *>(sSFB + S * kSfBytesStage);
   uint64_t *empty = full + S;
   uint64_t *tfull = empty + S;
   uint64_t *tempty = tfull + 2;
   uint64_t *sf_ready = tempty + 2;
   uint64_t *drain = sf_ready + S;
-  uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(drain + 1);
+  uint64_t *h_full = drain + 1;   // small-A W13: the tile's h is in h_s
+  uint64_t *h_empty = drain + 2;  // small-A W13: the four epilogue warps have read h_s
+  uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(drain + 3);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_holder + 1);
   uint32_t *q_scratch = reinterpret_cast<uint32_t *>(tmem_holder + 2);  // kQuantA: 5 words
+  float *h_s = reinterpret_cast<float *>(reinterpret_cast<uint8_t *>(full) + kGemmBarrierBytes);  // R::kHBytes
+  int4 *sched = reinterpret_cast<int4 *>(reinterpret_cast<uint8_t *>(h_s) + R::kHBytes);  // kTok1
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
@@ -194,6 +275,8 @@ __global__ void __launch_bounds__(kGemmThreads, kQuantA ? 1 : kCtasPerSm)
       mbar_init(&tempty[i], 4);
     }
     mbar_init(drain, 1);
+    mbar_init(h_full, 1);
+    mbar_init(h_empty, 4);
     *abort_flag = 0;
     fence_barrier_init();
     fence_proxy_async_shared();
@@ -207,6 +290,9 @@ __global__ void __launch_bounds__(kGemmThreads, kQuantA ? 1 : kCtasPerSm)
     tmem_alloc(tmem_holder, R::kTmemColsR);
     tmem_relinquish();
   }
+  if constexpr (kTok1) {
+    if (warp == 0) tok1_schedule(args, sched, lane);
+  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -214,16 +300,20 @@ __global__ void __launch_bounds__(kGemmThreads, kQuantA ? 1 : kCtasPerSm)
   // Everything above overlaps the previous kernel.  Its outputs (the A operand, the
   // activation scale) are read only after pdl_wait; with early_b the producer first
   // streams the weights of its first stages, which the calling chain wrote earlier.
-  if (!args.early_b || threadIdx.x != 0) {
+  // kTok1 reads nothing the previous kernel (the routing) writes: one idle lane waits for it
+  // below, so that the next launch (and this grid's completion) still follow it.
+  if (!kTok1 && (!args.early_b || threadIdx.x != 0)) {
     pdl_wait();
     pdl_trigger();
   }
+  auto entry = [&](int mtg) { return kTok1 ? sched[mtg] : tile_entry(args, mtg); };
 
   const int n_tiles = args.N / kBlockN;
   const int k_steps = args.K / kUmmaK;
   const int k_stages = (k_steps + 3) / 4;
-  const int total_mtiles = args.counts ? __ldg(args.tile_offsets + args.G)
-                                       : args.G * ((args.dense_M + kBlockM - 1) / kBlockM);
+  const int total_mtiles = kTok1 ? sched[15].x
+                           : args.counts ? __ldg(args.tile_offsets + args.G)
+                                         : args.G * ((args.dense_M + kBlockM - 1) / kBlockM);
   const int total_tiles = total_mtiles * n_tiles;
   // The tiles of a launch cost the same, so the CTAs taking part are trimmed to
   // ceil(tiles / waves): every wave, the last included, is (nearly) full instead of
@@ -253,7 +343,7 @@ __global__ void __launch_bounds__(kGemmThreads, kQuantA ? 1 : kCtasPerSm)
       int early = 0;
       if (args.early_b) {
         if (first < total_tiles) {
-          const Tile t = make_tile(tile_entry(args, first / n_tiles), first, n_tiles);
+          const Tile t = make_tile(entry(first / n_tiles), first, n_tiles);
           const CUtensorMap *mb;
           int b_row0;
           const uint8_t *sfb;
@@ -267,6 +357,12 @@ __global__ void __launch_bounds__(kGemmThreads, kQuantA ? 1 : kCtasPerSm)
             bulk_load(sSFB + s * kSfBytesStage, sfb + static_cast<size_t>(s) * kSfBytesStage,
                       kv * kSfBytesPerKStep, &full[s], pol_w);
           }
+          // the next stages of the tile into L2, while the previous kernel finishes
+          const int l2_end = min(k_stages, early + args.early_l2);
+          for (int s = early; s < l2_end; ++s) {
+            tma_prefetch_l2_2d(mb, 0, (b_row0 / kBlockN * k_stages + s) * kBlockN);
+            bulk_prefetch_l2(sfb + static_cast<size_t>(s) * kSfBytesStage, min(4, k_steps - 4 * s) * kSfBytesPerKStep);
+          }
         }
         pdl_wait();
         pdl_trigger();
@@ -276,10 +372,10 @@ __global__ void __launch_bounds__(kGemmThreads, kQuantA ? 1 : kCtasPerSm)
       uint32_t issued = 0;  // bit s: stage s has a load in flight with parity bit (s+8)
       int n_issued = 0;     // stages issued so far (the first `early` already hold their B)
       bool ok = true;
-      int4 next = first < total_tiles ? tile_entry(args, first / n_tiles) : make_int4(0, 0, 0, 0);
+      int4 next = first < total_tiles ? entry(first / n_tiles) : make_int4(0, 0, 0, 0);
       for (int idx = first; ok && idx < total_tiles; idx += grid) {
         const Tile t = make_tile(next, idx, n_tiles);
-        if (idx + grid < total_tiles) next = tile_entry(args, (idx + grid) / n_tiles);
+        if (idx + grid < total_tiles) next = entry((idx + grid) / n_tiles);
         const CUtensorMap *mb;
         int b_row0;
         const uint8_t *sfb;
@@ -336,6 +432,17 @@ __global__ void __launch_bounds__(kGemmThreads, kQuantA ? 1 : kCtasPerSm)
           if (issued & (1u << s))
             mbar_wait_bounded(&full[s], (issued >> (s + 8)) & 1u, &never, nullptr, 100000000ull);
       }
+    } else if (kTok1 && lane == 1) {
+      // The routing kernel has finished once this returns; its schedule must be the one
+      // this CTA derived from the ids.
+      pdl_wait();
+      pdl_trigger();
+      bool same = __ldg(args.tile_offsets + args.G) == total_mtiles;
+      for (int i = 0; same && i < total_mtiles; ++i) {
+        const int4 r = __ldg(args.tile_table + i), e = sched[i];
+        same = r.x == e.x && r.y == e.y && r.z == e.z && r.w == e.w;
+      }
+      if (!same) raise_device_error(args.err, NVFP4_DEVERR_INTERNAL);
     }
   } else if (warp == 1) {
     if (lane == 0) {
@@ -396,9 +503,11 @@ __global__ void __launch_bounds__(kGemmThreads, kQuantA ? 1 : kCtasPerSm)
     const int quarter = warp & 3;  // TMEM lanes [32*quarter, 32*quarter + 32)
     const int m = quarter * 32 + lane;
     float gs_scalar = 0.f;
-    if constexpr (kQuantA) {
+    if constexpr (kTok1) {
+      gs_scalar = quantize_token_a(args, sA, sSFA, q_scratch, threadIdx.x - 2 * 32);
+    } else if constexpr (kQuantA) {
       // one tile per CTA (the launch guarantees it): its group's K columns
-      const int g = first < total_tiles ? tile_entry(args, first / n_tiles).x : 0;
+      const int g = first < total_tiles ? entry(first / n_tiles).x : 0;
       gs_scalar = quantize_resident_a(args, g, sA, sSFA, q_scratch, threadIdx.x - 2 * 32);
     } else if constexpr (kEpi != static_cast<int>(Epi::kW2)) {
       gs_scalar = __ldg(args.gs_a);
@@ -413,10 +522,10 @@ __global__ void __launch_bounds__(kGemmThreads, kQuantA ? 1 : kCtasPerSm)
     int sstage = 0;
     uint32_t sphase = 0;
     int it = 0;
-    int4 next = first < total_tiles ? tile_entry(args, first / n_tiles) : make_int4(0, 0, 0, 0);
+    int4 next = first < total_tiles ? entry(first / n_tiles) : make_int4(0, 0, 0, 0);
     for (int idx = first; idx < total_tiles; idx += grid, ++it) {
       const Tile t = make_tile(next, idx, n_tiles);
-      if (idx + grid < total_tiles) next = tile_entry(args, (idx + grid) / n_tiles);
+      if (idx + grid < total_tiles) next = entry((idx + grid) / n_tiles);
       const int acc = kAccBufs == 2 ? (it & 1) : 0;
       const uint32_t acc_phase = kAccBufs == 2 ? ((it >> 1) & 1) : (it & 1);
       // Per-tile epilogue scalars, loaded before this tile's main loop so that their
@@ -433,7 +542,7 @@ __global__ void __launch_bounds__(kGemmThreads, kQuantA ? 1 : kCtasPerSm)
       const bool row_ok = m < t.rows;
       // MoE small-A tiles are 32 rows high and may start 32 j rows into a scale block
       // (dense and uniform-group tiles start at row 0)
-      constexpr bool kRotA = kSmallA && kEpi != static_cast<int>(Epi::kLinear);
+      constexpr bool kRotA = kSmallA && !kTok1 && kEpi != static_cast<int>(Epi::kLinear);
       const int sfa_rot = kRotA ? (t.a_row0 / kABoxRows) & 3 : 0;
       bool ok = true;
       for (int ks = 0; ks < k_stages; ++ks) {
@@ -446,8 +555,11 @@ __global__ void __launch_bounds__(kGemmThreads, kQuantA ? 1 : kCtasPerSm)
         uint32_t ra[16], rb[16];
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-          const uint4 wa = j < kv ? *reinterpret_cast<const uint4 *>(pa + j * kSfBytesPerKStep)
-                                  : make_uint4(0u, 0u, 0u, 0u);
+          // kTok1: A rows 0..7 are the token (its scale word of the K step), the rest zero
+          const uint4 wa = kTok1 ? make_uint4(j < kv && lane < 8 ? reinterpret_cast<const uint32_t *>(sSFA)[4 * ks + j]
+                                                                 : 0u, 0u, 0u, 0u)
+                           : j < kv ? *reinterpret_cast<const uint4 *>(pa + j * kSfBytesPerKStep)
+                                    : make_uint4(0u, 0u, 0u, 0u);
           const uint4 wb = j < kv ? *reinterpret_cast<const uint4 *>(pb + j * kSfBytesPerKStep)
                                   : make_uint4(0u, 0u, 0u, 0u);
           ra[4 * j] = wa.x, ra[4 * j + 1] = wa.y, ra[4 * j + 2] = wa.z, ra[4 * j + 3] = wa.w;
@@ -509,7 +621,76 @@ __global__ void __launch_bounds__(kGemmThreads, kQuantA ? 1 : kCtasPerSm)
         if (lane == 0) mbar_arrive(&tempty[acc]);
       };
 
-      if (!warp_live) {
+      constexpr bool kTeamH = kSmallA && kEpi == static_cast<int>(Epi::kW13);
+      if constexpr (kTeamH) {
+        // The tile's rows sit in lane quarter 0: its warp computes h into h_s and hands
+        // the accumulator back; then all four warps re-quantise h, four lanes per block.
+        const float gs2 = g_aux;
+        const float six_gs2 = __fmul_rn(6.0f, gs2);
+        const int I = args.out_ld * 2;
+        if (quarter == 0) {
+          ok = mbar_wait_bounded(h_empty, (it & 1) ^ 1, abort_flag, args.err, kPipelineTimeoutNs);
+          ok = __all_sync(0xffffffffu, ok);
+          if (!ok) break;
+          const float alpha = gs_scalar * ws2;
+          float *hrow = h_s + m * kHRowFloats;
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            uint32_t rg[16], ru[16];
+            tmem_ld16(tbase + c * 16, rg);
+            tmem_ld16(tbase + kBlockN / 2 + c * 16, ru);
+            tmem_ld_wait();
+            if (c == 3) release();
+            float h[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+              h[i] = silu_mul(__uint_as_float(rg[i]) * alpha, __uint_as_float(ru[i]) * alpha);
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+              reinterpret_cast<float4 *>(hrow + c * 16)[i] = make_float4(h[4 * i], h[4 * i + 1], h[4 * i + 2], h[4 * i + 3]);
+            if (args.h_debug != nullptr && row_ok) {
+              float4 *hd = reinterpret_cast<float4 *>(args.h_debug + (t.a_row0 + m) * I + t.nt * 64 + c * 16);
+#pragma unroll
+              for (int i = 0; i < 4; ++i)
+                hd[i] = make_float4(h[4 * i], h[4 * i + 1], h[4 * i + 2], h[4 * i + 3]);
+            }
+          }
+          __syncwarp();
+          if (lane == 0) mbar_arrive(h_full);
+        } else {
+          release();
+        }
+        ok = mbar_wait_bounded(h_full, it & 1, abort_flag, args.err, kPipelineTimeoutNs);
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) break;
+        // Thread e of the 128 takes the 16-bit piece j = e % 16 (elements 4j..4j+3) of row
+        // r0 + e / 16: the four lanes of a block share its amax, sixteen lanes make a row's
+        // 32 code bytes and its scale word.
+        const int e = static_cast<int>(threadIdx.x) - 64;
+        const int j = e & 15;
+        uint8_t *out = static_cast<uint8_t *>(args.out);
+        const int trows = min(t.rows, kABoxRows);  // a tile breaking the small-A promise raised an error
+        for (int r0 = 0; r0 < trows; r0 += 8) {
+          const int row = r0 + (e >> 4);
+          const bool act = row < trows;
+          const float4 v = act ? *reinterpret_cast<const float4 *>(h_s + row * kHRowFloats + 4 * j)
+                               : make_float4(0.f, 0.f, 0.f, 0.f);
+          uint32_t sfb;
+          const uint32_t bits = encode_block16_x4(v, gs2, six_gs2, &sfb);
+          const uint32_t hi = __shfl_down_sync(0xffffffffu, bits, 1);
+          uint32_t sfw = sfb << (8 * (j >> 2));
+          sfw |= __shfl_xor_sync(0xffffffffu, sfw, 4);
+          sfw |= __shfl_xor_sync(0xffffffffu, sfw, 8);
+          if (act) {
+            const int64_t p = t.a_row0 + row;
+            if ((j & 1) == 0)
+              *reinterpret_cast<uint32_t *>(out + p * args.out_ld + t.nt * 32 + 2 * j) = bits | (hi << 16);
+            if (j == 0) *reinterpret_cast<uint32_t *>(args.out_sf + sf_word_offset(p, t.nt, I / 64)) = sfw;
+          }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(h_empty);
+      } else if (!warp_live) {
         release();
       } else if constexpr (kEpi == static_cast<int>(Epi::kLinear)) {
         const float alpha = gs_scalar * ws2;
@@ -549,31 +730,38 @@ __global__ void __launch_bounds__(kGemmThreads, kQuantA ? 1 : kCtasPerSm)
         const float six_gs2 = __fmul_rn(6.0f, gs2);
         const int64_t p = t.a_row0 + m;
         const int I = args.out_ld * 2;
-        uint32_t codes[8];
-        uint32_t sfw = 0;
-#pragma unroll 1
+        // h of this thread's row; the accumulator is handed back once it has been read
+        float h[4][16];
+#pragma unroll
         for (int c = 0; c < 4; ++c) {
           uint32_t rg[16], ru[16];
           tmem_ld16(tbase + c * 16, rg);
           tmem_ld16(tbase + kBlockN / 2 + c * 16, ru);
           tmem_ld_wait();
-          float h[16];
+          if (c == 3) release();
 #pragma unroll
           for (int i = 0; i < 16; ++i)
-            h[i] = silu_mul(__uint_as_float(rg[i]) * alpha, __uint_as_float(ru[i]) * alpha);
-          if (args.h_debug != nullptr && row_ok) {
+            h[c][i] = silu_mul(__uint_as_float(rg[i]) * alpha, __uint_as_float(ru[i]) * alpha);
+        }
+        if (args.h_debug != nullptr && row_ok) {
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
             float4 *hd = reinterpret_cast<float4 *>(args.h_debug + p * I + t.nt * 64 + c * 16);
 #pragma unroll
             for (int i = 0; i < 4; ++i)
-              hd[i] = make_float4(h[4 * i], h[4 * i + 1], h[4 * i + 2], h[4 * i + 3]);
+              hd[i] = make_float4(h[c][4 * i], h[c][4 * i + 1], h[c][4 * i + 2], h[c][4 * i + 3]);
           }
+        }
+        uint32_t codes[8];
+        uint32_t sfw = 0;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
           uint32_t cw[2];
-          const uint32_t sfb = encode_block16(h, gs2, six_gs2, cw);
+          const uint32_t sfb = encode_block16(h[c], gs2, six_gs2, cw);
           codes[2 * c] = cw[0];
           codes[2 * c + 1] = cw[1];
           sfw |= sfb << (8 * c);
         }
-        release();
         if (row_ok) {
           // 32 code bytes of this row and tile; the workspace is 256-byte aligned and
           // rows are I/2 (a multiple of 32) bytes apart
@@ -637,7 +825,7 @@ __global__ void wait_timeout_probe_kernel(uint64_t timeout_ns, uint32_t *err) {
 template <int kEpi, bool kSmallA, bool kQuantA = false>
 cudaError_t launch_gemm_t(const CUtensorMap &ta, const CUtensorMap &tb, const CUtensorMap &tbs,
                           const GemmArgs &args, int grid, bool one_per_sm, cudaStream_t s) {
-  using R = Ring<kSmallA, kQuantA>;
+  using R = Ring<kSmallA, kQuantA, kQuantA && kEpi == static_cast<int>(Epi::kW13)>;
   static bool attr_done[64] = {false};
   int dev = 0;
   cudaGetDevice(&dev);
@@ -679,6 +867,11 @@ cudaError_t launch_gemm(Epi epi, const CUtensorMap &ta, const CUtensorMap &tb,
 
 cudaError_t launch_gemm_quant_a(const CUtensorMap &tb, const GemmArgs &args, int grid, cudaStream_t s) {
   return launch_gemm_t<static_cast<int>(Epi::kLinear), true, true>(tb, tb, tb, args, grid, true, s);
+}
+
+cudaError_t launch_gemm_tok1(const CUtensorMap &tb, const CUtensorMap &tbs, const GemmArgs &args, int grid,
+                             cudaStream_t s) {
+  return launch_gemm_t<static_cast<int>(Epi::kW13), true, true>(tb, tb, tbs, args, grid, false, s);
 }
 
 cudaError_t launch_wait_timeout_probe(uint32_t timeout_us, uint32_t *err, cudaStream_t s) {

@@ -40,7 +40,7 @@ constexpr uint32_t kTmemSfCols = 32;                 // per stage: 16 SFA + 16 S
 constexpr uint32_t kTmemCols = 256;                  // per CTA: 128 accumulator + 96 scale columns
 static_assert(kCtasPerSm * kTmemCols <= 512, "two CTAs share the SM's 512 TMEM columns");
 
-// full, empty, sf_ready per stage; two tfull/tempty; drain; TMEM address; abort flag
+// full, empty, sf_ready per stage; two tfull/tempty; drain; h_full/h_empty; TMEM address; abort flag
 constexpr size_t kGemmBarrierBytes = 256;
 
 // The stage ring in shared memory.  The regular ring holds kStages stages with a
@@ -56,24 +56,45 @@ constexpr int kQuantMaxK = 4096;
 constexpr int64_t kQuantMaxElems = 16384;
 constexpr int kQuantStages = 6;
 
-template <bool kSmallA, bool kQuantA = false>
+// Small-A MoE tiles keep their (at most 32) rows in the first TMEM lane quarter, so one
+// warp reads the whole accumulator.  It leaves the tile's h = SiLU(gate) * up in shared
+// memory (rows of kHRowFloats fp32, padded so that row-strided float4 accesses cover all
+// banks) and the four epilogue warps re-quantise it together.
+constexpr int kHRowFloats = 68;
+
+// One-token MoE calls (T = 1, top-k <= kTok1MaxTopk, H <= kTok1MaxK): every group's A is
+// the same token row, so the w13 CTAs quantise it themselves into one resident 8-row
+// swizzle atom per K stage (the row repeated: a token that lists an expert more than once
+// fills that many rows) and take their tile schedule from the top-k ids.  They start
+// streaming weights as soon as the routing kernel has started.
+constexpr int kTok1MaxK = 7168;
+constexpr int kTok1MaxTopk = 8;
+constexpr int kTok1SchedBytes = 256;  // group entries (int4) + the group count
+
+template <bool kSmallA, bool kQuantA = false, bool kTok1 = false>
 struct Ring {
-  static constexpr int kStagesR = kQuantA ? kQuantStages : (kSmallA ? 4 : kStages);
-  static constexpr int kABytes = kSmallA ? kABoxRows * kStageK / 2 : kTileBytesA;
-  static constexpr int kASlots = kQuantA ? kQuantMaxK / kStageK : kStagesR;  // A and SFA slots
-  static constexpr uint32_t kTmemColsR = kQuantA ? 512 : kTmemCols;
-  static constexpr size_t kSmem = 1024 /* alignment slack */ +
-                                  static_cast<size_t>(kASlots) * (kABytes + kSfBytesStage) +
+  static constexpr int kStagesR = kTok1 ? 4 : (kQuantA ? kQuantStages : (kSmallA ? 4 : kStages));
+  static constexpr int kABytes = kTok1 ? 1024 : (kSmallA ? kABoxRows * kStageK / 2 : kTileBytesA);
+  static constexpr int kASlots =
+      kTok1 ? kTok1MaxK / kStageK : (kQuantA ? kQuantMaxK / kStageK : kStagesR);  // A slots
+  // SFA: one 2 KB block per A slot, or (kTok1) the token row's four scale words per K stage
+  static constexpr int kSfaBytes = kTok1 ? 512 : kASlots * kSfBytesStage;
+  static constexpr uint32_t kTmemColsR = (kQuantA && !kTok1) ? 512 : kTmemCols;
+  static constexpr int kHBytes = kSmallA && (!kQuantA || kTok1) ? kABoxRows * kHRowFloats * 4 : 0;  // h of a tile
+  static constexpr int kSchedBytes = kTok1 ? kTok1SchedBytes : 0;
+  static constexpr size_t kSmem = 1024 /* alignment slack */ + static_cast<size_t>(kASlots) * kABytes + kSfaBytes +
                                   static_cast<size_t>(kStagesR) * (kTileBytesB + kSfBytesStage) +
-                                  kGemmBarrierBytes;
+                                  kGemmBarrierBytes + kHBytes + kSchedBytes;
   // Requested (not used) by launches that want one CTA per SM: two of these do not fit.
-  static constexpr size_t kSmemSolo = kQuantA ? kSmem : 2 * kSmem;
+  static constexpr size_t kSmemSolo = (kQuantA && !kTok1) ? kSmem : 2 * kSmem;
   static_assert(!kQuantA || kSmallA, "the resident A holds one 32-row box per K stage");
   static_assert(kTmemAccCols + kStagesR * kTmemSfCols <= kTmemColsR, "TMEM budget");
-  static_assert((3 * kStagesR + 5) * 8 + 8 + 24 <= kGemmBarrierBytes, "barrier region and scratch");
+  static_assert((3 * kStagesR + 7) * 8 + 8 + 24 <= kGemmBarrierBytes, "barrier region and scratch");
   static_assert(kSmemSolo <= 232448, "per-block shared memory limit");
-  static_assert(kQuantA || 2 * (kSmem + 1024) <= 233472, "two CTAs per SM");
+  static_assert((kQuantA && !kTok1) || 2 * (kSmem + 1024) <= 233472, "two CTAs per SM");
   static_assert(kABytes % 1024 == 0, "128-byte swizzle atoms stay 1024-byte aligned");
+  static_assert(kSfaBytes % 512 == 0, "the B ring stays 512-byte aligned");
+  static_assert(!kTok1 || (kTok1MaxK / 16) <= kSfaBytes, "one scale byte per 16 elements of the token row");
 };
 
 enum class Epi : int { kLinear = 0, kW13 = 1, kW2 = 2 };
@@ -125,7 +146,15 @@ struct GemmArgs {
   int64_t qa_ld;
   const float *qa_gs_static;
   float *qa_gs_out;
+  // kTok1 (one-token MoE w13): the top-k ids of the token (the routing kernel reads the
+  // same array) and the number of routed experts E; the groups are the distinct valid ids
+  // in increasing order, then the shared group.
+  const int32_t *tok1_ids;
+  int tok1_E;
+  // early_b: stages of the first tile's weights prefetched into L2 beyond the ring
+  int early_l2;
 };
+
 
 // Launch with programmatic dependent launch allowed: the kernel may start while the
 // previous kernel on the stream is finishing.  Every kernel of the library therefore
@@ -222,6 +251,10 @@ cudaError_t launch_gemm(Epi epi, const CUtensorMap &ta, const CUtensorMap &tb,
 // Dense or fixed-group linear with the activation quantisation fused (kQuantA): 1 <= M <= 32,
 // K <= kQuantMaxK, grid = tiles <= SM count (one tile per CTA).
 cudaError_t launch_gemm_quant_a(const CUtensorMap &tb, const GemmArgs &args, int grid, cudaStream_t s);
+// One-token MoE w13 (T = 1): the CTAs quantise the token (args.qa_*) and derive the tile
+// schedule from args.tok1_ids; two CTAs per SM.
+cudaError_t launch_gemm_tok1(const CUtensorMap &tb, const CUtensorMap &tbs, const GemmArgs &args, int grid,
+                             cudaStream_t s);
 // Dense GEMM on CTA pairs (256 x 256 tiles, tcgen05 cta_group::2): N % 256 == 0, A read
 // through a tensor map with 128-row boxes.  gemm_pair_max_clusters: clusters of 2 that fit
 // on the current device at once (0 if the query fails).

@@ -18,7 +18,7 @@ import numpy as np
 import pytest
 import torch
 
-from nvfp4_block_scaled_quant_gb300 import model, ops, workloads
+from nvfp4_block_scaled_quant_gb300 import _lib, model, ops, workloads
 from oracle import nvfp4_oracle as O
 from tests.helpers import assert_parity, bf16_to_np, oracle_expert_fn, oracle_pool
 
@@ -129,6 +129,9 @@ def run_moe_check(x, ids, w, W: ops.MoEWeights, oe, tokens, shared: bool, strict
     assert code_agree >= 0.999 and sf_agree >= 0.999, (code_agree, sf_agree)
     row_match = np.all(hq_gpu == hq_ref, axis=1) & np.all(hsf_gpu == hsf_ref, axis=1)
 
+    hq_split = hq[torch.from_numpy(rows).to(DEV)].cpu().numpy()  # the stage-by-stage w13's rows
+    hsf_split = hsf_gpu.copy()
+
     # ---------------------------------------------------------------- (d) on the oracle's operands
     hq_host = hq.cpu().numpy()
     hq_host[rows] = O.pack_codes(hq_ref)
@@ -147,6 +150,10 @@ def run_moe_check(x, ids, w, W: ops.MoEWeights, oe, tokens, shared: bool, strict
     torch.cuda.synchronize()
     assert ops.device_error() == (0, 0)
     assert g.item() == float(ref.xq.gs)
+    # the forward's w13 (at T = 1 the one-token kernel, which quantises x itself and takes its
+    # schedule from the ids) leaves the same re-quantised rows as the stage-by-stage launches
+    np.testing.assert_array_equal(hq[torch.from_numpy(rows).to(DEV)].cpu().numpy(), hq_split)
+    np.testing.assert_array_equal(hsf_t.cpu().numpy()[hsf_off[rows, : I // 16]], hsf_split)
     yf = bf16_to_np(y)[tokens]
     assert np.isfinite(bf16_to_np(y)).all()
     slot_tok = np.array([tokens.index(t) for t, _ in slots])
@@ -286,6 +293,57 @@ def segment_rows(ids: np.ndarray, e: int) -> np.ndarray:
     """Tokens of expert e's routed rows in segment order (the routing is stable by flat index)."""
     k = ids.shape[1]
     return np.nonzero(ids.reshape(-1) == e)[0] // k
+
+
+@pytest.mark.parametrize("ids_row,shared", [([3, 3, 1, 3, 0, 1, 2, 3], True), ([5, 2, 7, 5, 0, 6, 1, 4], False),
+                                            ([6, 6, 6, 6, 6, 6, 6, 6], True)])
+def test_moe_one_token_repeated_ids(ids_row, shared):
+    """One token (the one-token w13: x quantised in the GEMM CTAs, schedule from the ids) with an
+    expert listed up to eight times: that group's tile holds as many copies of the token."""
+    H, I, E, k = 384, 128, 8, 8  # H = 384: the last K stage holds two of its four K steps
+    base = 141
+    W = model.make_moe_weights(E, H, I, base, DEV, shared=shared)
+    oe = oracle_expert_fn(base, H, I, DEV)
+    x = workloads.activations(1, H, seed=142, device="cpu", outliers=True)
+    ids = torch.tensor([ids_row], dtype=torch.int32)
+    w = torch.softmax(torch.randn(1, k, generator=torch.Generator().manual_seed(143)), -1).contiguous()
+    run_moe_check(x, ids, w, W, oe, [0], shared)
+
+
+def test_moe_one_token_static_gs_and_bad_id():
+    """One token: a static a1 scale equal to the dynamic one gives the same re-quantised rows; an
+    out-of-range id is dropped (the routing flags it) and the w13 schedule drops it too."""
+    H, I, E, k = 512, 128, 8, 4
+    W = model.make_moe_weights(E, H, I, 151, DEV, shared=True)
+    x = workloads.activations(1, H, seed=152, device=DEV)
+    ids = torch.tensor([[4, 1, 6, 2]], dtype=torch.int32, device=DEV)
+    w = torch.full((1, k), 0.25, device=DEV)
+    a2 = torch.full((E + 1,), 0.01, device=DEV)
+    L = ops.moe_workspace_layout(1, H, I, E, k, True)
+    ws = torch.zeros(L.total, dtype=torch.uint8, device=DEV)
+    hq = _region(ws, L.hq, L.rows_capacity * I // 2, torch.uint8)
+    y_dyn, g = ops.moe_forward(x, ids, w, W, a2, workspace=ws)
+    torch.cuda.synchronize()
+    assert ops.device_error() == (0, 0)
+    hq_dyn = hq.clone()
+    hq.zero_()
+    y_st, _ = ops.moe_forward(x, ids, w, W, a2, a1_gs=g.clone(), workspace=ws)
+    torch.cuda.synchronize()
+    assert ops.device_error() == (0, 0)
+    assert torch.equal(hq, hq_dyn)
+    assert torch.allclose(y_st.float(), y_dyn.float(), rtol=1e-2, atol=1e-3)
+    ids_bad = ids.clone()
+    ids_bad[0, 2] = 9
+    ops.device_error()
+    y_bad, _ = ops.moe_forward(x, ids_bad, w, W, a2, workspace=ws)
+    st, flags = ops.device_error()
+    assert st == _lib.ERR_DEVICE_FAULT and flags == _lib.DEVERR_BAD_EXPERT_ID
+    w_drop = w.clone()
+    w_drop[0, 2] = 0.0
+    y_drop, _ = ops.moe_forward(x, ids, w_drop, W, a2, workspace=ws)
+    torch.cuda.synchronize()
+    assert ops.device_error() == (0, 0)
+    assert torch.allclose(y_bad.float(), y_drop.float(), rtol=1e-2, atol=1e-3)
 
 
 def chunk_tokens(ids: np.ndarray, n: int, seed: int, R: int = 32) -> list:
