@@ -25,8 +25,9 @@
  *    a kernel may start while the previous kernel on the stream finishes, and
  *    reads its inputs only after that kernel completed.  The one exception is
  *    that the GEMMs of nvfp4_linear and of the MoE stages read the weights and
- *    the routing arrays one launch early.  Those must therefore be final before
- *    the call that opens the chain (nvfp4_linear, nvfp4_moe_forward or
+ *    the routing arrays one launch early (the one-token MoE forward also the
+ *    token x and its top-k ids and weights).  Those must therefore be final
+ *    before the call that opens the chain (nvfp4_linear, nvfp4_moe_forward or
  *    nvfp4_moe_dispatch) is enqueued, which ordinary stream order gives.
  *  - bf16 tensors are passed as void* to raw bf16 storage (row-major).
  *  - Scale-factor buffers in the "swizzled" tensor-core layout hold
@@ -277,7 +278,13 @@ NVFP4_API nvfp4_status nvfp4_moe_route(const int32_t *ids, int64_t T, int topk, 
  * above, *a1_gs written in dynamic mode) and a2_gs (E+1 entries, last = shared
  * expert) the static global scales of the re-quantised intermediate h
  * (warm-up calibrated, page 3: the warm-up calibration passage).
- * y (T, H) bf16; the output width is H (page 3: the MoE shape-rules passage).  H % 128 == 0, I % 64 == 0. */
+ * y (T, H) bf16; the output width is H (page 3: the MoE shape-rules passage).  H % 128 == 0, I % 64 == 0.
+ * nvfp4_moe_forward with one token (T = 1, topk <= 8, H <= 7168) runs as routing, one GEMM
+ * launch and the conversion of y: the GEMM CTAs quantise the token themselves, take their
+ * tiles from the ids and add each tile's share of the down projection (its 64 columns of
+ * the re-quantised h times that K step of w2) into the fp32 accumulator; the workspace's xq,
+ * xsf and amax_partials are then left untouched.  The re-quantised h rows (hq, hsf) are the
+ * ones the stage-by-stage calls produce; y agrees within fp32 summation order. */
 typedef struct nvfp4_moe_ws_layout {
   /* byte offsets into the workspace */
   size_t counts;        /* int32 [G]        rows per group (G = E + has_shared)     */

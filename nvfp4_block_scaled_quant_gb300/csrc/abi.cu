@@ -112,16 +112,17 @@ nvfp4_status get_encoder(const char *fn, EncodeTiledFn *out) {
 // 2-D byte tensor (rows x row_bytes, row stride ld_bytes) read in boxes of
 // 128 bytes x box_rows with the 128-byte swizzle.
 nvfp4_status make_map(const char *fn, CUtensorMap *m, const void *base, int64_t row_bytes,
-                      int64_t rows, int64_t ld_bytes, int box_rows) {
+                      int64_t rows, int64_t ld_bytes, int box_rows, int box_bytes = 128,
+                      CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B) {
   EncodeTiledFn encode;
   nvfp4_status st = get_encoder(fn, &encode);
   if (st != NVFP4_OK) return st;
   const cuuint64_t dims[2] = {static_cast<cuuint64_t>(row_bytes), static_cast<cuuint64_t>(rows)};
   const cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld_bytes)};
-  const cuuint32_t box[2] = {128u, static_cast<cuuint32_t>(box_rows)};
+  const cuuint32_t box[2] = {static_cast<cuuint32_t>(box_bytes), static_cast<cuuint32_t>(box_rows)};
   const cuuint32_t estr[2] = {1u, 1u};
   CUresult r = encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(base), dims, strides, box, estr,
-                      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                      CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
                       CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS)
     return fail(NVFP4_ERR_CUDA, fn, "cuTensorMapEncodeTiled failed (%d) for %lld x %lld bytes", static_cast<int>(r),
@@ -134,6 +135,13 @@ nvfp4_status make_map(const char *fn, CUtensorMap *m, const void *base, int64_t 
 nvfp4_status make_weight_map(const char *fn, CUtensorMap *m, const void *w, int64_t rows, int64_t K) {
   const int64_t slabs = (K / 2 + 127) / 128;
   return make_map(fn, m, w, 128, rows * slabs, 128, 128);
+}
+
+// The same weights read one 64-element K step at a time: boxes of 128 rows x 32 bytes at
+// x = 32 (k % 4) of slab k / 4, 32-byte swizzle (the one-token kernel's w2 slices).
+nvfp4_status make_weight_slice_map(const char *fn, CUtensorMap *m, const void *w, int64_t rows, int64_t K) {
+  const int64_t slabs = (K / 2 + 127) / 128;
+  return make_map(fn, m, w, 128, rows * slabs, 128, 128, 32, CU_TENSOR_MAP_SWIZZLE_32B);
 }
 
 size_t align256(size_t v) { return (v + 255) & ~static_cast<size_t>(255); }
@@ -266,6 +274,10 @@ struct Tok1 {
   const int32_t *ids;
   bool dynamic;
   float *a1_gs;
+  // the down projection, fused into the same launch (split K over I): w2 codes, scales and
+  // weight scales, the shared expert's, the routing weights
+  const uint8_t *w2, *w2_sf, *sh_w2, *sh_w2_sf;
+  const float *w2_ws2, *sh_ws2, *topk_w;
 };
 
 bool tok1_applies(int64_t T, int64_t H, int topk) { return T == 1 && topk <= kTok1MaxTopk && H <= kTok1MaxK; }
@@ -337,7 +349,22 @@ nvfp4_status moe_gemm_impl(const char *fn, DeviceInfo *d, Epi epi, int64_t T, in
     a.tok1_E = static_cast<int>(E);
     a.topk = topk;
     a.early_b = 0;  // nothing is read before the wait but the ids and the weights
-    NV_CUDA(launch_gemm_tok1(tb, tbs, a, d->sms * kCtasPerSm, s), "one-token w13 launch");
+    CUtensorMap t2, t2s;
+    if ((st = make_weight_slice_map(fn, &t2, tok1->w2, E * H, I)) != NVFP4_OK) return st;
+    if (has_shared) {
+      if ((st = make_weight_slice_map(fn, &t2s, tok1->sh_w2, H, I)) != NVFP4_OK) return st;
+    } else {
+      t2s = t2;
+    }
+    a.p2_N = static_cast<int>(H);
+    a.p2_K = static_cast<int>(I);
+    a.p2_acc = at<float>(ws, L.y_acc);
+    a.p2_sf = tok1->w2_sf;
+    a.p2_sf_shared = tok1->sh_w2_sf;
+    a.p2_ws2 = tok1->w2_ws2;
+    a.p2_ws2_shared = tok1->sh_ws2 ? tok1->sh_ws2 + 1 : nullptr;
+    a.p2_topk_w = tok1->topk_w;
+    NV_CUDA(launch_gemm_tok1(tb, tbs, t2, t2s, a, d->sms * kCtasPerSm, s), "one-token MoE launch");
     return NVFP4_OK;
   }
   // The routing cut the groups into tiles of moe_tile_rows(T) rows: 32-row tiles fit one
@@ -952,7 +979,8 @@ nvfp4_status nvfp4_moe_forward(const void *x, int64_t T, int64_t H, int64_t I, i
     NV_CUDA(launch_route_amax(topk_ids, 1, topk, static_cast<int>(E), has_shared, rb, nullptr, H, nullptr, 0,
                               at<float>(ws, L.y_acc), d->flags, s),
             "route kernel launch");
-    const Tok1 tok1{x, topk_ids, a1_gs_mode == NVFP4_GS_DYNAMIC, a1_gs};
+    const Tok1 tok1{x,   topk_ids, a1_gs_mode == NVFP4_GS_DYNAMIC, a1_gs, w2, w2_sf, sh_w2, sh_w2_sf,
+                    w2_ws2, sh_ws2, topk_w};
     if ((st = moe_gemm_impl(__func__, d, Epi::kW13, T, H, I, E, topk, w13, w13_sf, w13_ws2, sh_w13, sh_w13_sf,
                             sh_ws2, a1_gs, a2_gs, nullptr, nullptr, ws, s, &tok1)) != NVFP4_OK)
       return st;
@@ -964,7 +992,9 @@ nvfp4_status nvfp4_moe_forward(const void *x, int64_t T, int64_t H, int64_t I, i
                             sh_ws2, a1_gs, a2_gs, nullptr, nullptr, ws, s)) != NVFP4_OK)
       return st;
   }
-  if ((st = moe_gemm_impl(__func__, d, Epi::kW2, T, H, I, E, topk, w2, w2_sf, w2_ws2, sh_w2, sh_w2_sf, sh_ws2, a2_gs,
+  // (at T = 1 the one-token launch did the down projection too)
+  if (!tok1_applies(T, H, topk) &&
+      (st = moe_gemm_impl(__func__, d, Epi::kW2, T, H, I, E, topk, w2, w2_sf, w2_ws2, sh_w2, sh_w2_sf, sh_ws2, a2_gs,
                           nullptr, topk_w, nullptr, ws, s)) != NVFP4_OK)
     return st;
   if (T == 0) return NVFP4_OK;

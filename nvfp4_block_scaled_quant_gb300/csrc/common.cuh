@@ -194,7 +194,7 @@ __device__ __forceinline__ void tc_commit(uint64_t *bar) {
 
 // Shared-memory matrix descriptor (tcgen05 format): start address, leading and
 // stride byte offsets (all >> 4), fixed version bits 46..47 = 1, swizzle mode
-// in bits 61..63 (0 none, 2 = 128-byte swizzle).
+// in bits 61..63 (0 none, 2 = 128-byte swizzle, 6 = 32-byte swizzle).
 __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo_bytes,
                                               uint32_t sbo_bytes, uint32_t swizzle_mode) {
   uint64_t d = 0;
@@ -230,6 +230,13 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
         "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
       : "r"(taddr)
       : "memory");
+}
+
+// 32 lanes x 1 column: thread i receives lane (base lane + i).
+__device__ __forceinline__ uint32_t tmem_ld1(uint32_t taddr) {
+  uint32_t r;
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x1.b32 {%0}, [%1];" : "=r"(r) : "r"(taddr) : "memory");
+  return r;
 }
 
 __device__ __forceinline__ void tmem_ld_wait() {

@@ -78,6 +78,19 @@ __device__ __forceinline__ uint4 rotate_words(uint4 v, int j) {
 constexpr uint32_t kIdesc = (1u << 7) | (1u << 10) | ((uint32_t(kBlockN) >> 3) << 17) |
                             ((uint32_t(kBlockM) >> 4) << 24);
 
+// The one-token kernel's fused down projection: per stage kP2RowTiles w2 row tiles of 128
+// rows x one 64-element K step (32 bytes, 32-byte swizzle), each one MMA of M = 128 (w2 rows)
+// by N = kP2N (rows of the re-quantised h: the token's copies, at most kTok1MaxTopk) into its
+// own slot of one of two 64-column accumulator buffers, so that a stage's MMAs run while the
+// epilogue reads the previous stage's.
+constexpr int kP2RowTiles = 4;
+constexpr int kP2N = 16;
+constexpr int kP2TileBytes = kBlockN * 32;
+constexpr uint32_t kIdescP2 = (1u << 7) | (1u << 10) | ((uint32_t(kP2N) >> 3) << 17) | ((uint32_t(kBlockM) >> 4) << 24);
+static_assert(kP2RowTiles * kP2TileBytes <= kTileBytesB && kP2RowTiles * kSfBytesPerKStep <= kSfBytesStage,
+              "a fused-down-projection stage fits a ring slot");
+static_assert(2 * kP2RowTiles * kP2N <= kBlockN && kTok1MaxTopk <= kP2N, "two slot buffers fit the accumulator");
+
 // SiLU(g) * u with the fast exponential and divide (relative error ~1e-6; for g below
 // about -88, exp(-g) is +inf and the quotient is 0).
 __device__ __forceinline__ float silu_mul(float g, float u) {
@@ -235,7 +248,8 @@ template <int kEpi, bool kSmallA, bool kQuantA>
 __global__ void __launch_bounds__(kGemmThreads, (kQuantA && kEpi != static_cast<int>(Epi::kW13)) ? 1 : kCtasPerSm)
     nvfp4_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                       const __grid_constant__ CUtensorMap tmB,
-                      const __grid_constant__ CUtensorMap tmBs, const GemmArgs args) {
+                      const __grid_constant__ CUtensorMap tmBs,
+                      const __grid_constant__ CUtensorMap tmC, const GemmArgs args) {
   // kQuantA with the W13 epilogue: the one-token MoE w13 (resident token atoms, schedule from ids)
   constexpr bool kTok1 = kQuantA && kEpi == static_cast<int>(Epi::kW13);
   using R = Ring<kSmallA, kQuantA, kTok1>;
@@ -261,6 +275,12 @@ __global__ void __launch_bounds__(kGemmThreads, (kQuantA && kEpi != static_cast<
   uint32_t *q_scratch = reinterpret_cast<uint32_t *>(tmem_holder + 2);  // kQuantA: 5 words
   float *h_s = reinterpret_cast<float *>(reinterpret_cast<uint8_t *>(full) + kGemmBarrierBytes);  // R::kHBytes
   int4 *sched = reinterpret_cast<int4 *>(reinterpret_cast<uint8_t *>(h_s) + R::kHBytes);  // kTok1
+  uint8_t *p2_tile = reinterpret_cast<uint8_t *>(sched) + R::kSchedBytes;             // kTok1: h rows, B of the
+  uint32_t *p2_sfw = reinterpret_cast<uint32_t *>(p2_tile + 32 * 32);                 // fused w2; their scales
+  uint64_t *p2_full = reinterpret_cast<uint64_t *>(p2_sfw + 32);  // kTok1: a slot buffer holds MMA results
+  uint64_t *p2_empty = p2_full + 2;                               // kTok1: the epilogue has read a buffer
+  // (kTok1) the w2 codes of the fused down projection come through tmA (routed experts)
+  // and tmC (the shared expert)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
@@ -277,6 +297,12 @@ __global__ void __launch_bounds__(kGemmThreads, (kQuantA && kEpi != static_cast<
     mbar_init(drain, 1);
     mbar_init(h_full, 1);
     mbar_init(h_empty, 4);
+    if constexpr (kTok1) {
+      for (int i = 0; i < 2; ++i) {
+        mbar_init(&p2_full[i], 1);
+        mbar_init(&p2_empty[i], 4);
+      }
+    }
     *abort_flag = 0;
     fence_barrier_init();
     fence_proxy_async_shared();
@@ -285,6 +311,7 @@ __global__ void __launch_bounds__(kGemmThreads, (kQuantA && kEpi != static_cast<
     prefetch_tensormap(&tmA);
     prefetch_tensormap(&tmB);
     if (args.shared_group >= 0) prefetch_tensormap(&tmBs);
+    if (kTok1 && args.p2_acc != nullptr && args.shared_group >= 0) prefetch_tensormap(&tmC);
   }
   if (warp == 1) {
     tmem_alloc(tmem_holder, R::kTmemColsR);
@@ -423,6 +450,42 @@ __global__ void __launch_bounds__(kGemmThreads, (kQuantA && kEpi != static_cast<
             phase ^= 1;
           }
         }
+        if constexpr (kTok1) {
+          // The fused down projection of this tile: its h columns 64 nt .. 64 nt + 63 are K step
+          // nt of w2; every w2 row tile of the group contributes 128 rows x 32 bytes.
+          if (ok && args.p2_acc != nullptr) {
+            const int n_rt = args.p2_N / kBlockN;
+            const int kst2 = args.p2_K / kUmmaK, ks2 = (kst2 + 3) / 4;
+            const bool sh = t.g == args.shared_group;
+            const CUtensorMap *m2 = sh ? &tmC : &tmA;
+            const int rt0 = sh ? 0 : t.g * n_rt;
+            const int slab = t.nt >> 2, x2 = (t.nt & 3) * 32;
+            const uint8_t *sf2 = (sh ? args.p2_sf_shared
+                                     : args.p2_sf + static_cast<size_t>(t.g) * args.p2_N * (args.p2_K / 16)) +
+                                 static_cast<size_t>(t.nt) * kSfBytesPerKStep;
+            for (int p = 0; p * kP2RowTiles < n_rt; ++p) {
+              const int nq = min(kP2RowTiles, n_rt - p * kP2RowTiles);
+              if (!mbar_wait_bounded(&empty[stage], phase ^ 1, abort_flag, args.err, kPipelineTimeoutNs)) {
+                ok = false;
+                break;
+              }
+              mbar_arrive_expect_tx(&full[stage], nq * (kP2TileBytes + kSfBytesPerKStep));
+              for (int q = 0; q < nq; ++q) {
+                const int rt = p * kP2RowTiles + q;
+                tma_load_2d(sB + stage * kTileBytesB + q * kP2TileBytes, m2, x2, ((rt0 + rt) * ks2 + slab) * kBlockN,
+                            &full[stage], pol_stream);
+                bulk_load(sSFB + stage * kSfBytesStage + q * kSfBytesPerKStep,
+                          sf2 + static_cast<size_t>(rt) * kst2 * kSfBytesPerKStep, kSfBytesPerKStep, &full[stage],
+                          pol_stream);
+              }
+              issued = (issued & ~(0x101u << stage)) | (1u << stage) | (phase << (stage + 8));
+              if (++stage == S) {
+                stage = 0;
+                phase ^= 1;
+              }
+            }
+          }
+        }
       }
       if (!ok) {
         // let the copies already in flight land before the CTA leaves (this wait
@@ -452,6 +515,7 @@ __global__ void __launch_bounds__(kGemmThreads, (kQuantA && kEpi != static_cast<
       int it = 0;
       bool ok = true;
       const uint32_t sA0 = smem_u32(sA), sB0 = smem_u32(sB);
+      int p2n = 0;  // kTok1: down-projection stages so far (slot buffer p2n & 1)
       for (int idx = first; ok && idx < total_tiles; idx += grid, ++it) {
         const int acc = kAccBufs == 2 ? (it & 1) : 0;
         const uint32_t acc_phase = kAccBufs == 2 ? ((it >> 1) & 1) : (it & 1);
@@ -492,6 +556,39 @@ __global__ void __launch_bounds__(kGemmThreads, (kQuantA && kEpi != static_cast<
         }
         if (!ok) break;
         tc_commit(&tfull[acc]);
+        if constexpr (kTok1) {
+          if (args.p2_acc != nullptr) {
+            const int n_rt = args.p2_N / kBlockN;
+            const uint64_t bdesc2 = smem_desc(smem_u32(p2_tile), 16, 256, 6);
+            // the down projection takes the accumulator columns as one more use: its slot
+            // buffers overlap the w13 accumulator, which the W13 epilogue must have read
+            ++it;
+            ok = mbar_wait_bounded(&tempty[0], (it & 1) ^ 1, abort_flag, args.err, kPipelineTimeoutNs);
+            for (int p = 0; ok && p * kP2RowTiles < n_rt; ++p, ++p2n) {
+              const int nq = min(kP2RowTiles, n_rt - p * kP2RowTiles);
+              const int b = p2n & 1;
+              if (!mbar_wait_bounded(&p2_empty[b], ((p2n >> 1) & 1) ^ 1, abort_flag, args.err, kPipelineTimeoutNs) ||
+                  !mbar_wait_bounded(&full[stage], phase, abort_flag, args.err, kPipelineTimeoutNs) ||
+                  !mbar_wait_bounded(&sf_ready[stage], phase, abort_flag, args.err, kPipelineTimeoutNs)) {
+                ok = false;
+                break;
+              }
+              tc_fence_after();
+              const uint32_t sf_col = tmem_base + kTmemAccCols + stage * kTmemSfCols;
+              for (int q = 0; q < nq; ++q)
+                tc_mma_nvf4(tmem_base + b * (kP2RowTiles * kP2N) + q * kP2N,
+                            smem_desc(sB0 + stage * kTileBytesB + q * kP2TileBytes, 16, 256, 6), bdesc2, kIdescP2,
+                            sf_col + 4 * q, sf_col + 16, 0u);
+              tc_commit(&empty[stage]);
+              tc_commit(&p2_full[b]);
+              if (++stage == S) {
+                stage = 0;
+                phase ^= 1;
+              }
+            }
+            if (!ok) break;
+          }
+        }
       }
       // every MMA this thread issued has completed before TMEM is released
       volatile int never = 0;
@@ -521,7 +618,10 @@ __global__ void __launch_bounds__(kGemmThreads, (kQuantA && kEpi != static_cast<
     const int sf_off = lane * 16;
     int sstage = 0;
     uint32_t sphase = 0;
-    int it = 0;
+    int it = 0;   // uses of the accumulator columns (a tile, then kTok1's down-projection stages)
+    int ht = 0;   // tiles through h_s (small-A W13)
+    bool p2_ordered = false;  // kTok1: the routing kernel (which zeroes the fp32 output) has finished
+    int p2n = 0;              // kTok1: down-projection stages so far (slot buffer p2n & 1)
     int4 next = first < total_tiles ? entry(first / n_tiles) : make_int4(0, 0, 0, 0);
     for (int idx = first; idx < total_tiles; idx += grid, ++it) {
       const Tile t = make_tile(next, idx, n_tiles);
@@ -629,13 +729,42 @@ __global__ void __launch_bounds__(kGemmThreads, (kQuantA && kEpi != static_cast<
         const float six_gs2 = __fmul_rn(6.0f, gs2);
         const int I = args.out_ld * 2;
         if (quarter == 0) {
-          ok = mbar_wait_bounded(h_empty, (it & 1) ^ 1, abort_flag, args.err, kPipelineTimeoutNs);
+          ok = mbar_wait_bounded(h_empty, (ht & 1) ^ 1, abort_flag, args.err, kPipelineTimeoutNs);
           ok = __all_sync(0xffffffffu, ok);
           if (!ok) break;
           const float alpha = gs_scalar * ws2;
           float *hrow = h_s + m * kHRowFloats;
+          if constexpr (kTok1) {
+            // Every row of a one-token tile is the token: lane 0's accumulator row (gate columns
+            // 0..63, up columns 64..127) goes through shared memory (rows 1.. of h_s) to the 32
+            // lanes, two h columns each, into row 0 of h_s.
+            float *raw = h_s + kHRowFloats;
 #pragma unroll
-          for (int c = 0; c < 4; ++c) {
+            for (int c = 0; c < 8; ++c) {
+              uint32_t r[16];
+              tmem_ld16(tbase + c * 16, r);
+              tmem_ld_wait();
+              if (c == 7) release();
+              if (lane == 0) {
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+                  reinterpret_cast<float4 *>(raw + c * 16)[i] =
+                      make_float4(__uint_as_float(r[4 * i]), __uint_as_float(r[4 * i + 1]),
+                                  __uint_as_float(r[4 * i + 2]), __uint_as_float(r[4 * i + 3]));
+              }
+            }
+            __syncwarp();
+            const float2 g2 = *reinterpret_cast<const float2 *>(raw + 2 * lane);
+            const float2 u2 = *reinterpret_cast<const float2 *>(raw + kBlockN / 2 + 2 * lane);
+            const float2 hh = make_float2(silu_mul(g2.x * alpha, u2.x * alpha), silu_mul(g2.y * alpha, u2.y * alpha));
+            __syncwarp();
+            *reinterpret_cast<float2 *>(h_s + 2 * lane) = hh;
+            if (args.h_debug != nullptr)
+              for (int r = 0; r < t.rows; ++r)
+                *reinterpret_cast<float2 *>(args.h_debug + (t.a_row0 + r) * I + t.nt * 64 + 2 * lane) = hh;
+          }
+#pragma unroll
+          for (int c = 0; c < (kTok1 ? 0 : 4); ++c) {
             uint32_t rg[16], ru[16];
             tmem_ld16(tbase + c * 16, rg);
             tmem_ld16(tbase + kBlockN / 2 + c * 16, ru);
@@ -660,7 +789,7 @@ __global__ void __launch_bounds__(kGemmThreads, (kQuantA && kEpi != static_cast<
         } else {
           release();
         }
-        ok = mbar_wait_bounded(h_full, it & 1, abort_flag, args.err, kPipelineTimeoutNs);
+        ok = mbar_wait_bounded(h_full, ht & 1, abort_flag, args.err, kPipelineTimeoutNs);
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) break;
         // Thread e of the 128 takes the 16-bit piece j = e % 16 (elements 4j..4j+3) of row
@@ -673,7 +802,8 @@ __global__ void __launch_bounds__(kGemmThreads, (kQuantA && kEpi != static_cast<
         for (int r0 = 0; r0 < trows; r0 += 8) {
           const int row = r0 + (e >> 4);
           const bool act = row < trows;
-          const float4 v = act ? *reinterpret_cast<const float4 *>(h_s + row * kHRowFloats + 4 * j)
+          // (kTok1: every row is the token, whose h is row 0)
+          const float4 v = act ? *reinterpret_cast<const float4 *>(h_s + (kTok1 ? 0 : row) * kHRowFloats + 4 * j)
                                : make_float4(0.f, 0.f, 0.f, 0.f);
           uint32_t sfb;
           const uint32_t bits = encode_block16_x4(v, gs2, six_gs2, &sfb);
@@ -686,10 +816,118 @@ __global__ void __launch_bounds__(kGemmThreads, (kQuantA && kEpi != static_cast<
             if ((j & 1) == 0)
               *reinterpret_cast<uint32_t *>(out + p * args.out_ld + t.nt * 32 + 2 * j) = bits | (hi << 16);
             if (j == 0) *reinterpret_cast<uint32_t *>(args.out_sf + sf_word_offset(p, t.nt, I / 64)) = sfw;
+            if constexpr (kTok1) {
+              // the same row as the fused down projection's B operand: 32 bytes, 32-byte swizzle
+              // (16-byte chunk c of row r at chunk c ^ ((r >> 2) & 1))
+              if ((j & 1) == 0)
+                *reinterpret_cast<uint32_t *>(p2_tile + row * 32 + ((((j >> 3) ^ (row >> 2)) & 1) << 4) + ((2 * j) & 15)) =
+                    bits | (hi << 16);
+              if (j == 0) p2_sfw[row] = sfw;
+            }
           }
         }
+        if constexpr (kTok1) fence_proxy_async_shared();  // the MMAs read p2_tile through the async proxy
         __syncwarp();
         if (lane == 0) mbar_arrive(h_empty);
+        if constexpr (kTok1) {
+          // every warp's rows of p2_tile and p2_sfw are written once this tile's h_empty phase completes
+          if (args.p2_acc != nullptr) {
+            ok = mbar_wait_bounded(h_empty, ht & 1, abort_flag, args.err, kPipelineTimeoutNs);
+            ok = __all_sync(0xffffffffu, ok);
+            if (!ok) break;
+          }
+        }
+        ++ht;
+        if constexpr (kTok1) {
+          // The fused down projection of the tile (see the producer): stage the w2 scale blocks
+          // (A) and the h rows' scales (B), then add the MMA results of the token's column.
+          if (args.p2_acc != nullptr) {
+            if (!p2_ordered) {
+              pdl_wait();
+              p2_ordered = true;
+            }
+            const int n_rt = args.p2_N / kBlockN;
+            float wsum = 1.f;  // the group's routing weight: the shared group takes the token once
+            if (!sh) {
+              wsum = 0.f;
+              for (int f = 0; f < args.topk; ++f)
+                if (__ldg(args.tok1_ids + f) == t.g) wsum += __ldg(args.p2_topk_w + f);
+            }
+            const float alpha2 = gs2 * (sh ? __ldg(args.p2_ws2_shared) : __ldg(args.p2_ws2 + t.g)) * wsum;
+            const uint32_t hq_sfw = lane < trows ? p2_sfw[lane] : 0u;
+            const uint64_t pol_y = policy_evict_last();
+            ++it;  // the down projection's use of the accumulator columns (see the MMA)
+            const int P = (n_rt + kP2RowTiles - 1) / kP2RowTiles;
+            // stage p's scales: the w2 scale blocks (A of the MMA, four columns each) and the
+            // h rows' scale words (B, lanes 0..15 of column 16)
+            auto stage_sf = [&](int p) -> bool {
+              const int nq = min(kP2RowTiles, n_rt - p * kP2RowTiles);
+              bool fine = mbar_wait_bounded(&full[sstage], sphase, abort_flag, args.err, kPipelineTimeoutNs);
+              fine = __all_sync(0xffffffffu, fine);
+              if (!fine) return false;
+              uint32_t ra[16], rb[16];
+#pragma unroll
+              for (int q = 0; q < 4; ++q) {
+                const uint4 wa = q < nq ? *reinterpret_cast<const uint4 *>(sSFB + sstage * kSfBytesStage +
+                                                                          q * kSfBytesPerKStep + sf_off)
+                                        : make_uint4(0u, 0u, 0u, 0u);
+                ra[4 * q] = wa.x, ra[4 * q + 1] = wa.y, ra[4 * q + 2] = wa.z, ra[4 * q + 3] = wa.w;
+              }
+#pragma unroll
+              for (int i = 0; i < 16; ++i) rb[i] = 0u;
+              rb[0] = hq_sfw;
+              tmem_st16(sf_lane + sstage * kTmemSfCols, ra);
+              tmem_st16(sf_lane + sstage * kTmemSfCols + 16, rb);
+              tmem_st_wait();
+              tc_fence_before();
+              __syncwarp();
+              if (lane == 0) mbar_arrive(&sf_ready[sstage]);
+              if (++sstage == S) {
+                sstage = 0;
+                sphase ^= 1;
+              }
+              return true;
+            };
+            ok = stage_sf(0) && (P < 2 || stage_sf(1));
+            const uint32_t tq = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16);
+            for (int p = 0; ok && p < P; ++p, ++p2n) {
+              const int nq = min(kP2RowTiles, n_rt - p * kP2RowTiles);
+              const int b = p2n & 1;
+              ok = mbar_wait_bounded(&p2_full[b], (p2n >> 1) & 1, abort_flag, args.err, kPipelineTimeoutNs);
+              ok = __all_sync(0xffffffffu, ok);
+              if (!ok) break;
+              tc_fence_after();
+              uint32_t v[kP2RowTiles];
+#pragma unroll
+              for (int q = 0; q < kP2RowTiles; ++q)
+                v[q] = q < nq ? tmem_ld1(tq + b * (kP2RowTiles * kP2N) + q * kP2N) : 0u;
+              tmem_ld_wait();
+              tc_fence_before();
+              __syncwarp();
+              if (lane == 0) mbar_arrive(&p2_empty[b]);
+              // w2 row 32 quarter + lane of row tile 4 p + q is output column 128 (4 p + q) + 32 quarter + lane
+#pragma unroll
+              for (int q = 0; q < kP2RowTiles; ++q) {
+                if (q < nq) {
+                  const float y0 = __uint_as_float(v[q]) * alpha2;
+                  const float y1 = __shfl_down_sync(0xffffffffu, y0, 1);
+                  const float y2 = __shfl_down_sync(0xffffffffu, y0, 2);
+                  const float y3 = __shfl_down_sync(0xffffffffu, y0, 3);
+                  if ((lane & 3) == 0)
+                    red_add_v4(reinterpret_cast<float4 *>(args.p2_acc + (p * kP2RowTiles + q) * kBlockN + quarter * 32 +
+                                                          lane),
+                               y0, y1, y2, y3, pol_y);
+                }
+              }
+              if (p + 2 < P) ok = stage_sf(p + 2);
+            }
+            if (!ok) break;
+            // the accumulator columns are free for the next tile's w13
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&tempty[0]);
+          }
+        }
       } else if (!warp_live) {
         release();
       } else if constexpr (kEpi == static_cast<int>(Epi::kLinear)) {
@@ -824,7 +1062,8 @@ __global__ void wait_timeout_probe_kernel(uint64_t timeout_ns, uint32_t *err) {
 
 template <int kEpi, bool kSmallA, bool kQuantA = false>
 cudaError_t launch_gemm_t(const CUtensorMap &ta, const CUtensorMap &tb, const CUtensorMap &tbs,
-                          const GemmArgs &args, int grid, bool one_per_sm, cudaStream_t s) {
+                          const GemmArgs &args, int grid, bool one_per_sm, cudaStream_t s,
+                          const CUtensorMap *tc = nullptr) {
   using R = Ring<kSmallA, kQuantA, kQuantA && kEpi == static_cast<int>(Epi::kW13)>;
   static bool attr_done[64] = {false};
   int dev = 0;
@@ -839,7 +1078,7 @@ cudaError_t launch_gemm_t(const CUtensorMap &ta, const CUtensorMap &tb, const CU
   // A grid no larger than the SM count asks for enough shared memory to keep one CTA per
   // SM, so its tiles spread over as many SMs as there are tiles.
   return launch_pdl(nvfp4_gemm_kernel<kEpi, kSmallA, kQuantA>, dim3(grid), dim3(kGemmThreads),
-                    one_per_sm ? R::kSmemSolo : R::kSmem, s, ta, tb, tbs, args);
+                    one_per_sm ? R::kSmemSolo : R::kSmem, s, ta, tb, tbs, tc ? *tc : tb, args);
 }
 
 template <int kEpi>
@@ -869,9 +1108,9 @@ cudaError_t launch_gemm_quant_a(const CUtensorMap &tb, const GemmArgs &args, int
   return launch_gemm_t<static_cast<int>(Epi::kLinear), true, true>(tb, tb, tb, args, grid, true, s);
 }
 
-cudaError_t launch_gemm_tok1(const CUtensorMap &tb, const CUtensorMap &tbs, const GemmArgs &args, int grid,
-                             cudaStream_t s) {
-  return launch_gemm_t<static_cast<int>(Epi::kW13), true, true>(tb, tb, tbs, args, grid, false, s);
+cudaError_t launch_gemm_tok1(const CUtensorMap &tb, const CUtensorMap &tbs, const CUtensorMap &t2,
+                             const CUtensorMap &t2s, const GemmArgs &args, int grid, cudaStream_t s) {
+  return launch_gemm_t<static_cast<int>(Epi::kW13), true, true>(t2, tb, tbs, args, grid, false, s, &t2s);
 }
 
 cudaError_t launch_wait_timeout_probe(uint32_t timeout_us, uint32_t *err, cudaStream_t s) {

@@ -82,9 +82,12 @@ struct Ring {
   static constexpr uint32_t kTmemColsR = (kQuantA && !kTok1) ? 512 : kTmemCols;
   static constexpr int kHBytes = kSmallA && (!kQuantA || kTok1) ? kABoxRows * kHRowFloats * 4 : 0;  // h of a tile
   static constexpr int kSchedBytes = kTok1 ? kTok1SchedBytes : 0;
+  // kTok1: the re-quantised h of a tile as the fused down projection's B operand (32 rows of
+  // 32 bytes, 32-byte swizzle) and its rows' scale words
+  static constexpr int kP2Bytes = kTok1 ? 32 * 32 + 32 * 4 + 4 * 8 : 0;  // + p2_full[2], p2_empty[2]
   static constexpr size_t kSmem = 1024 /* alignment slack */ + static_cast<size_t>(kASlots) * kABytes + kSfaBytes +
                                   static_cast<size_t>(kStagesR) * (kTileBytesB + kSfBytesStage) +
-                                  kGemmBarrierBytes + kHBytes + kSchedBytes;
+                                  kGemmBarrierBytes + kHBytes + kSchedBytes + kP2Bytes;
   // Requested (not used) by launches that want one CTA per SM: two of these do not fit.
   static constexpr size_t kSmemSolo = (kQuantA && !kTok1) ? kSmem : 2 * kSmem;
   static_assert(!kQuantA || kSmallA, "the resident A holds one 32-row box per K stage");
@@ -153,6 +156,20 @@ struct GemmArgs {
   int tok1_E;
   // early_b: stages of the first tile's weights prefetched into L2 beyond the ring
   int early_l2;
+  // One-token w13 with the down projection fused (p2_acc set; p2_N = H, p2_K = I): after a
+  // w13 tile (h columns 64 nt .. 64 nt + 63 of group g) the CTA multiplies its re-quantised
+  // h by that 64-wide K step of all H rows of the group's w2 (split K over I; the w2 codes
+  // through the slice maps, p2_sf / p2_sf_shared their scales, p2_ws2 / p2_ws2_shared the
+  // weight scales) and adds the products, times the group's routing weight (tok1_ids,
+  // p2_topk_w; 1 for the shared group) and the static scale of h, into p2_acc (H fp32).
+  float *p2_acc;
+  int p2_N;
+  int p2_K;
+  const uint8_t *p2_sf;
+  const uint8_t *p2_sf_shared;
+  const float *p2_ws2;
+  const float *p2_ws2_shared;
+  const float *p2_topk_w;
 };
 
 
@@ -253,8 +270,8 @@ cudaError_t launch_gemm(Epi epi, const CUtensorMap &ta, const CUtensorMap &tb,
 cudaError_t launch_gemm_quant_a(const CUtensorMap &tb, const GemmArgs &args, int grid, cudaStream_t s);
 // One-token MoE w13 (T = 1): the CTAs quantise the token (args.qa_*) and derive the tile
 // schedule from args.tok1_ids; two CTAs per SM.
-cudaError_t launch_gemm_tok1(const CUtensorMap &tb, const CUtensorMap &tbs, const GemmArgs &args, int grid,
-                             cudaStream_t s);
+cudaError_t launch_gemm_tok1(const CUtensorMap &tb, const CUtensorMap &tbs, const CUtensorMap &t2,
+                             const CUtensorMap &t2s, const GemmArgs &args, int grid, cudaStream_t s);
 // Dense GEMM on CTA pairs (256 x 256 tiles, tcgen05 cta_group::2): N % 256 == 0, A read
 // through a tensor map with 128-row boxes.  gemm_pair_max_clusters: clusters of 2 that fit
 // on the current device at once (0 if the query fails).
