@@ -614,7 +614,7 @@ static nvfp4_status linear_fused(const char *fn, DeviceInfo *d, const void *x, i
   a.out_ld = static_cast<int>(G * N);
   a.out_group_cols = static_cast<int>(N);
   a.err = d->flags;
-  a.early_b = 0;  // the launch just before this one may have written W
+  a.early_b = 1;  // the weights are older than the previous launch (prepare_weights does not trigger early)
   a.qa_x = x;
   a.qa_ld = G * K;
   a.qa_gs_static = dyn ? nullptr : gs;

@@ -33,7 +33,9 @@ __device__ __forceinline__ void raise_device_error(uint32_t *err, uint32_t flag)
 // Programmatic dependent launch: wait for the previous grid on the stream to complete
 // (and its writes to be visible); allow the next grid to start launching.  Every kernel
 // of the library triggers only after its own wait returned, so when a library kernel
-// starts, every grid two or more launches back on the stream has completed.
+// starts, every grid two or more launches back on the stream has completed.  The weight
+// preparation kernel does not trigger at all: the launch after it starts once it has
+// completed, so weights are final for any library kernel that reads them early.
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 

@@ -26,6 +26,8 @@
 //            permuted rows of the w2 input                 (gate/up projection)
 //   kW2      y_acc[t] += topk_w * gs2_e * ws2_e * D        (down projection,
 //            top-k weighted scatter-add in fp32)
+#include <type_traits>
+
 #include "common.cuh"
 
 namespace nvfp4 {
@@ -117,21 +119,32 @@ __device__ float quantize_resident_a(const GemmArgs &a, int g, uint8_t *sA, uint
   float gs;
   if (a.qa_gs_static == nullptr) {
     uint32_t m = 0;
-    const int64_t chunks = ld / 8, n = M * chunks;
-    for (int64_t i0 = tid; i0 < n; i0 += 8 * 128) {  // eight 16-byte loads in flight per thread
-      uint4 v[8];
+    // the M x ld inputs are contiguous (row stride ld): U 16-byte loads in flight per thread,
+    // 32 when x is large enough that 8 would take several round trips (the 8 x 4096 inputs
+    // of a grouped o-projection token take one)
+    const int n = static_cast<int>(M * (ld / 8));
+    const uint4 *xv = reinterpret_cast<const uint4 *>(x);
+    auto reduce = [&](auto U) {
+      constexpr int kU = decltype(U)::value;
+      for (int i0 = tid; i0 < n; i0 += kU * 128) {
+        uint4 v[kU];
 #pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        const int64_t i = i0 + u * 128, r = i / chunks;
-        v[u] = i < n ? __ldg(reinterpret_cast<const uint4 *>(x + r * ld) + (i - r * chunks)) : make_uint4(0, 0, 0, 0);
+        for (int u = 0; u < kU; ++u) {
+          const int i = i0 + u * 128;
+          v[u] = i < n ? __ldg(xv + i) : make_uint4(0, 0, 0, 0);
+        }
+#pragma unroll
+        for (int u = 0; u < kU; ++u) {
+          const uint32_t w[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+#pragma unroll
+          for (int k = 0; k < 4; ++k) m = max(m, max(w[k] & 0x7FFFu, (w[k] >> 16) & 0x7FFFu));
+        }
       }
-#pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        const uint32_t w[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
-#pragma unroll
-        for (int k = 0; k < 4; ++k) m = max(m, max(w[k] & 0x7FFFu, (w[k] >> 16) & 0x7FFFu));
-      }
-    }
+    };
+    if (n > 8 * 128)
+      reduce(std::integral_constant<int, 32>());
+    else
+      reduce(std::integral_constant<int, 8>());
 #pragma unroll
     for (int o = 16; o; o >>= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, o));
     if (lane == 0) scratch[warp] = m;
@@ -145,8 +158,8 @@ __device__ float quantize_resident_a(const GemmArgs &a, int g, uint8_t *sA, uint
   const float six_gs = __fmul_rn(6.0f, gs);
   const int64_t kb = K / 16;
 #pragma unroll 2
-  for (int64_t i = tid; i < M * kb; i += 128) {
-    const int64_t r = i / kb, c = i - r * kb;  // row, 16-element block of the group
+  for (int i = tid; i < static_cast<int>(M * kb); i += 128) {
+    const int r = i / static_cast<int>(kb), c = i - r * static_cast<int>(kb);  // row, 16-element block of the group
     const uint4 *src = reinterpret_cast<const uint4 *>(x + r * ld + static_cast<int64_t>(g) * K + c * 16);
     const uint4 p = __ldg(src), q = __ldg(src + 1);
     const uint32_t w[8] = {p.x, p.y, p.z, p.w, q.x, q.y, q.z, q.w};
@@ -740,17 +753,20 @@ __global__ void __launch_bounds__(kGemmThreads, (kQuantA && kEpi != static_cast<
             // lanes, two h columns each, into row 0 of h_s.
             float *raw = h_s + kHRowFloats;
 #pragma unroll
-            for (int c = 0; c < 8; ++c) {
-              uint32_t r[16];
-              tmem_ld16(tbase + c * 16, r);
+            for (int c0 = 0; c0 < 8; c0 += 4) {
+              uint32_t r[4][16];
+#pragma unroll
+              for (int q = 0; q < 4; ++q) tmem_ld16(tbase + (c0 + q) * 16, r[q]);
               tmem_ld_wait();
-              if (c == 7) release();
+              if (c0 == 4) release();
               if (lane == 0) {
 #pragma unroll
-                for (int i = 0; i < 4; ++i)
-                  reinterpret_cast<float4 *>(raw + c * 16)[i] =
-                      make_float4(__uint_as_float(r[4 * i]), __uint_as_float(r[4 * i + 1]),
-                                  __uint_as_float(r[4 * i + 2]), __uint_as_float(r[4 * i + 3]));
+                for (int q = 0; q < 4; ++q)
+#pragma unroll
+                  for (int i = 0; i < 4; ++i)
+                    reinterpret_cast<float4 *>(raw + (c0 + q) * 16)[i] =
+                        make_float4(__uint_as_float(r[q][4 * i]), __uint_as_float(r[q][4 * i + 1]),
+                                    __uint_as_float(r[q][4 * i + 2]), __uint_as_float(r[q][4 * i + 3]));
               }
             }
             __syncwarp();
@@ -937,28 +953,34 @@ __global__ void __launch_bounds__(kGemmThreads, (kQuantA && kEpi != static_cast<
         __nv_bfloat16 *y = static_cast<__nv_bfloat16 *>(args.out) +
                            row * static_cast<int64_t>(args.out_ld) +
                            static_cast<int64_t>(t.g) * args.out_group_cols + t.nt * kBlockN;
+        // four TMEM loads in flight per wait
 #pragma unroll 1
-        for (int c = 0; c < kBlockN / 16; ++c) {
-          uint32_t r[16];
-          tmem_ld16(tbase + c * 16, r);
-          tmem_ld_wait();
-          if (c == kBlockN / 16 - 1) release();
-          if (row_ok) {
-            uint32_t packed[8];
+        for (int c0 = 0; c0 < kBlockN / 16; c0 += 4) {
+          uint32_t r[4][16];
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-              const __nv_bfloat162 v = __floats2bfloat162_rn(
-                  __uint_as_float(r[2 * i]) * alpha, __uint_as_float(r[2 * i + 1]) * alpha);
-              packed[i] = *reinterpret_cast<const uint32_t *>(&v);
-            }
-            // 32 bytes per row and chunk: one 256-bit store when the output is 32-byte
-            // aligned (row strides and column offsets are multiples of 256 bytes)
-            if (out32) {
-              st_global_v8(y + c * 16, packed);
-            } else {
-              uint4 *dst = reinterpret_cast<uint4 *>(y + c * 16);
-              dst[0] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
-              dst[1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
+          for (int q = 0; q < 4; ++q) tmem_ld16(tbase + (c0 + q) * 16, r[q]);
+          tmem_ld_wait();
+          if (c0 + 4 == kBlockN / 16) release();
+          if (row_ok) {
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              const int c = c0 + q;
+              uint32_t packed[8];
+#pragma unroll
+              for (int i = 0; i < 8; ++i) {
+                const __nv_bfloat162 v = __floats2bfloat162_rn(
+                    __uint_as_float(r[q][2 * i]) * alpha, __uint_as_float(r[q][2 * i + 1]) * alpha);
+                packed[i] = *reinterpret_cast<const uint32_t *>(&v);
+              }
+              // 32 bytes per row and chunk: one 256-bit store when the output is 32-byte
+              // aligned (row strides and column offsets are multiples of 256 bytes)
+              if (out32) {
+                st_global_v8(y + c * 16, packed);
+              } else {
+                uint4 *dst = reinterpret_cast<uint4 *>(y + c * 16);
+                dst[0] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+                dst[1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
+              }
             }
           }
         }

@@ -175,8 +175,10 @@ __device__ __forceinline__ int64_t interleave_src_row(int64_t n, int64_t N, int 
 __global__ void prepare_kernel(const uint8_t *__restrict__ w, const uint8_t *__restrict__ sf,
                                int64_t G, int64_t N, int64_t K, int flags,
                                uint8_t *__restrict__ w_out, uint8_t *__restrict__ sf_out) {
+  // No early trigger: the launch after this one may read the prepared weights before its
+  // own wait (the GEMMs stream their first weight stages early), so it starts only once
+  // this grid has completed.
   pdl_wait();
-  pdl_trigger();
   const int64_t row_bytes = K / 2;                // a multiple of 32 (K % 64 == 0)
   const int64_t slabs = (row_bytes + 127) / 128;  // 128-byte column slabs per row
   const int64_t tiles = N / 128;
