@@ -389,6 +389,7 @@ def run_native(args, rank: int, world: int, local_rank: int):
 
 def run_secondary(state, args):
     """Decode steps and the dense linear / GEMM workloads, one line each in 'secondary'."""
+    import numpy as np
     import torch
 
     from nvfp4_block_scaled_quant_gb300 import model, ops, workloads
@@ -477,7 +478,43 @@ def run_secondary(state, args):
                 "tflops": acct["flops"] / (ms / 1e3) / 1e12,
                 "tensor_frac_fp4": acct["flops"] / (ms / 1e3) / 1e12 / fp4_peak, "groups": acct["groups"],
                 "note": "one call over the same 4096 tokens as the 32-chunk step"})
-    del wsw, xd, idd, wd, yw
+    # The same call's hot-expert tiles alone: groups of >= 1000 rows (the popular experts and the
+    # shared expert).  Every other slot of the routing gets an out-of-range id, which the routing
+    # drops (it raises the bad-id flag, read and cleared here), so the GEMMs run exactly the hot
+    # groups' tiles; w13 and w2 are timed with events around their launches.
+    idn = ids.numpy()
+    counts = np.bincount(idn.reshape(-1), minlength=cfg.E)
+    hot = counts >= 1000
+    ids_hot = np.where(hot[idn], idn, cfg.E).astype(np.int32)
+    rows_hot = int(counts[hot].sum()) + cfg.T
+    idh = torch.from_numpy(ids_hot).to(dev)
+    a1 = torch.empty(1, dtype=torch.float32, device=dev)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+    t13 = t2 = 0.0
+    for rep in range(6):
+        ops.moe_dispatch(xd, idh, W, a1, True, wsw)
+        ev[0].record()
+        ops.moe_w13(cfg.T, cfg.topk, W, a1, a2, wsw)
+        ev[1].record()
+        ops.moe_w2(cfg.T, cfg.topk, wd, W, a2, wsw)
+        ev[2].record()
+        ev[2].synchronize()
+        if rep >= 2:
+            t13 += ev[0].elapsed_time(ev[1]) / 4
+            t2 += ev[1].elapsed_time(ev[2]) / 4
+    flag = ops.device_error()
+    f13 = 2.0 * rows_hot * 2 * cfg.I * cfg.H
+    f2 = 2.0 * rows_hot * cfg.H * cfg.I
+    out.append({"workload": "prefill_whole_hot_expert_tiles_rows_ge_1000", "groups": int(hot.sum()) + 1,
+                "rows": rows_hot, "w13_ms": t13, "w2_ms": t2,
+                "w13_tflops": f13 / (t13 / 1e3) / 1e12, "w2_tflops": f2 / (t2 / 1e3) / 1e12,
+                "tflops": (f13 + f2) / ((t13 + t2) / 1e3) / 1e12,
+                "tensor_frac_fp4": (f13 + f2) / ((t13 + t2) / 1e3) / 1e12 / fp4_peak,
+                "w13_tensor_frac_fp4": f13 / (t13 / 1e3) / 1e12 / fp4_peak,
+                "bad_id_flag_expected": list(flag),
+                "note": "the 4096-token call's groups with >= 1000 rows and the shared expert, the other slots "
+                        "dropped; 128-row m tiles on the one-SM grouped GEMM; CUDA events around each launch"})
+    del wsw, xd, idd, wd, yw, idh
     # dense linear K=1536 N=16384: 14 MB of weights fit in L2, so rotate 16 weight copies (> L2)
     K, N = 1536, 16384
     dws = [model.make_dense_weight(N, K, seed=50 + i, device=dev) for i in range(16)]

@@ -405,9 +405,13 @@ def test_moe_prefill_whole_4096_hot_experts(big_weights, oracle_map):
     run_moe_check(x, ids, w, W, oe, tokens, True, mapper=oracle_map, calib_tokens=tokens[:2])
 
 
-def test_moe_forward_cuda_graph_replay():
-    """nvfp4_moe_forward captured in a CUDA graph and replayed matches eager execution."""
-    cfg = workloads.TINY_SHARED
+@pytest.mark.parametrize("T", [16, 1])
+def test_moe_forward_cuda_graph_replay(T):
+    """nvfp4_moe_forward captured in a CUDA graph and replayed matches eager execution; new inputs
+    and routings written into the captured buffers flow through the replay (T = 1: the one-token
+    launch, which reads the ids before its dependency wait)."""
+    base = workloads.TINY_SHARED
+    cfg = workloads.MoEConfig(base.name, T, base.H, base.I, base.E, base.topk, True, base.routing, False)
     W = model.make_moe_weights(cfg.E, cfg.H, cfg.I, 108, DEV, shared=True)
     ws = ops.moe_workspace(cfg.T, cfg.H, cfg.I, cfg.E, cfg.topk, True, DEV)
     a2 = torch.full((cfg.E + 1,), 0.004, device=DEV)
@@ -435,6 +439,9 @@ def test_moe_forward_cuda_graph_replay():
     np.testing.assert_allclose(bf16_to_np(y), bf16_to_np(eager), rtol=1e-2, atol=1e-3 * float(eager.float().abs().max()))
     # new inputs in the captured buffers flow through the replay
     x.copy_(workloads.activations(cfg.T, cfg.H, seed=3, device=DEV))
+    ids2, w2 = workloads.routing(cfg, seed=4, device=DEV)
+    ids.copy_(ids2)
+    w.copy_(w2)
     g.replay()
     y2 = y.clone()
     ops.moe_forward(x, ids, w, W, a2, workspace=ws, out=y)
