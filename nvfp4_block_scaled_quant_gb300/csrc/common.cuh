@@ -388,12 +388,11 @@ __device__ __forceinline__ uint32_t f32_to_ue4m3(float s) {
 
 // Two fp32 values -> one byte of E2M1 codes, v0 in the low nibble, each code
 // rounded to nearest-even on |v| with saturation at 6 and the sign bit of v
-// kept (so a negative value that rounds to zero gives code 0x8).
+// kept (so a negative value that rounds to zero gives code 0x8).  The hardware
+// conversion keeps the sign of a value that rounds to zero; the bit-exact
+// quantiser tests hold it to that (-0.0, -0.1, negative midpoints).
 __device__ __forceinline__ uint32_t e2m1x2_signed(float v0, float v1) {
-  const uint32_t mag = static_cast<uint32_t>(
-      __nv_cvt_float2_to_fp4x2(make_float2(fabsf(v0), fabsf(v1)), __NV_E2M1, cudaRoundNearest));
-  const uint32_t s0 = __float_as_uint(v0) >> 31, s1 = __float_as_uint(v1) >> 31;
-  return mag | (s0 << 3) | (s1 << 7);
+  return static_cast<uint32_t>(__nv_cvt_float2_to_fp4x2(make_float2(v0, v1), __NV_E2M1, cudaRoundNearest));
 }
 
 // Encode one 16-element block with global multiplier gs (six_gs = fl32(6 * gs)).
@@ -441,6 +440,24 @@ __device__ __forceinline__ uint32_t encode_block16_x4(float4 v, float gs, float 
   return e2m1x2_signed(__fmul_rn(v.x, r), __fmul_rn(v.y, r)) |
          (e2m1x2_signed(__fmul_rn(v.z, r), __fmul_rn(v.w, r)) << 8);
 }
+
+// Row and column of a flat block index g = r * kb + c, advanced by a fixed step with no
+// division in the loop (the step's own quotient and remainder are computed once).
+struct RowCol {
+  int64_t r, c;
+  __device__ __forceinline__ void init(int64_t g, int64_t kb) {
+    r = g / kb;
+    c = g - r * kb;
+  }
+  __device__ __forceinline__ void advance(int64_t step_r, int64_t step_c, int64_t kb) {
+    c += step_c;
+    r += step_r;
+    if (c >= kb) {
+      c -= kb;
+      ++r;
+    }
+  }
+};
 
 // Byte offset of the 32-bit word holding scales (row r, columns 4c'..4c'+3) in
 // the swizzled layout, for a buffer whose rows carry K elements (kc4 = K / 64

@@ -139,6 +139,12 @@ __global__ void __launch_bounds__(kNormThreads, kStreamCtasPerSm) rmsnorm_quanti
   const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
   const int lane = threadIdx.x & 31;
   const int64_t wbase0 = static_cast<int64_t>(blockIdx.x) * blockDim.x + (threadIdx.x & ~31);
+  // (row, block) of each of this thread's kNormUnroll blocks, advanced without division
+  const int64_t step = kNormUnroll * stride;
+  const int64_t step_r = step / kb, step_c = step - step_r * kb;
+  RowCol pos[kNormUnroll];
+#pragma unroll
+  for (int u = 0; u < kNormUnroll; ++u) pos[u].init(wbase0 + u * stride + lane, kb);
   uint4 a[kNormUnroll], b[kNormUnroll];
   float inv[kNormUnroll];
   auto load = [&](int64_t wb) {
@@ -147,14 +153,11 @@ __global__ void __launch_bounds__(kNormThreads, kStreamCtasPerSm) rmsnorm_quanti
       const int64_t g = wb + u * stride + lane;
       a[u] = b[u] = make_uint4(0u, 0u, 0u, 0u);
       inv[u] = 0.f;
-      if (g < total) {
-        const int64_t r = g / kb, c = g - r * kb;
-        if (r < M) {
-          const uint4 *src = reinterpret_cast<const uint4 *>(x + r * ldx + c * 16);
-          a[u] = __ldg(src);
-          b[u] = __ldg(src + 1);
-          inv[u] = __ldg(inv_rms + r);
-        }
+      if (g < total && pos[u].r < M) {
+        const uint4 *src = reinterpret_cast<const uint4 *>(x + pos[u].r * ldx + pos[u].c * 16);
+        a[u] = __ldg(src);
+        b[u] = __ldg(src + 1);
+        inv[u] = __ldg(inv_rms + pos[u].r);
       }
     }
   };
@@ -167,13 +170,14 @@ __global__ void __launch_bounds__(kNormThreads, kStreamCtasPerSm) rmsnorm_quanti
     gs = *gs_static;
   }
   const float six_gs = __fmul_rn(6.0f, gs);
-  for (int64_t wb = wbase0; wb < total; wb += kNormUnroll * stride) {  // uniform over the warp
+  for (int64_t wb = wbase0; wb < total; wb += step) {  // uniform over the warp
     if (wb != wbase0) load(wb);
 #pragma unroll
     for (int u = 0; u < kNormUnroll; ++u) {
       const int64_t g = wb + u * stride + lane;
       const bool valid = g < total;
-      const int64_t r = valid ? g / kb : 0, c = valid ? g - r * kb : 0;
+      const int64_t r = pos[u].r, c = pos[u].c;
+      pos[u].advance(step_r, step_c, kb);
       const bool live = valid && r < M;
       uint32_t sfb = 0;
       if (live) {

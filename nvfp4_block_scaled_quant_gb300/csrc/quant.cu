@@ -107,6 +107,12 @@ __global__ void __launch_bounds__(kQuantThreads, kStreamCtasPerSm) quantize_kern
   const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
   const int lane = threadIdx.x & 31;
   const int64_t wbase0 = static_cast<int64_t>(blockIdx.x) * blockDim.x + (threadIdx.x & ~31);
+  // (row, block) of each of this thread's kQuantUnroll blocks, advanced without division
+  const int64_t step = kQuantUnroll * stride;
+  const int64_t step_r = step / kb, step_c = step - step_r * kb;
+  RowCol pos[kQuantUnroll];
+#pragma unroll
+  for (int u = 0; u < kQuantUnroll; ++u) pos[u].init(wbase0 + u * stride + lane, kb);
   // the first blocks' loads are issued before the gs reduction, which their latency overlaps
   uint4 a[kQuantUnroll], b[kQuantUnroll];
   auto load = [&](int64_t wb) {
@@ -114,13 +120,10 @@ __global__ void __launch_bounds__(kQuantThreads, kStreamCtasPerSm) quantize_kern
     for (int u = 0; u < kQuantUnroll; ++u) {
       const int64_t g = wb + u * stride + lane;
       a[u] = b[u] = make_uint4(0u, 0u, 0u, 0u);
-      if (g < total) {
-        const int64_t r = g / kb, c = g - r * kb;
-        if (r < M) {
-          const uint4 *src = reinterpret_cast<const uint4 *>(x + r * ldx + c * 16);
-          a[u] = __ldg(src);
-          b[u] = __ldg(src + 1);
-        }
+      if (g < total && pos[u].r < M) {
+        const uint4 *src = reinterpret_cast<const uint4 *>(x + pos[u].r * ldx + pos[u].c * 16);
+        a[u] = __ldg(src);
+        b[u] = __ldg(src + 1);
       }
     }
   };
@@ -131,9 +134,11 @@ __global__ void __launch_bounds__(kQuantThreads, kStreamCtasPerSm) quantize_kern
     // itself, one launch fewer.  Block 0 writes gs (0 when M == 0).
     uint32_t m = 0;
     const int64_t chunks = K / 8;
-    for (int64_t i = threadIdx.x; i < M * chunks; i += blockDim.x) {
-      const int64_t rr = i / chunks;
-      const uint4 v = __ldg(reinterpret_cast<const uint4 *>(x + rr * ldx) + (i - rr * chunks));
+    RowCol ix;
+    ix.init(threadIdx.x, chunks);
+    const int64_t sr = blockDim.x / chunks, sc = blockDim.x - sr * chunks;
+    for (int64_t i = threadIdx.x; i < M * chunks; i += blockDim.x, ix.advance(sr, sc, chunks)) {
+      const uint4 v = __ldg(reinterpret_cast<const uint4 *>(x + ix.r * ldx) + ix.c);
       m = max(m, max(max(max_abs_bf16x2(v.x), max_abs_bf16x2(v.y)), max(max_abs_bf16x2(v.z), max_abs_bf16x2(v.w))));
     }
     m = block_reduce_max(m, scratch);
@@ -146,17 +151,18 @@ __global__ void __launch_bounds__(kQuantThreads, kStreamCtasPerSm) quantize_kern
     gs = *gs_static;
   }
   const float six_gs = __fmul_rn(6.0f, gs);
-  for (int64_t wb = wbase0; wb < total; wb += kQuantUnroll * stride) {  // uniform over the warp
+  for (int64_t wb = wbase0; wb < total; wb += step) {  // uniform over the warp
     if (wb != wbase0) load(wb);
 #pragma unroll
     for (int u = 0; u < kQuantUnroll; ++u) {
       const int64_t g = wb + u * stride + lane;
       const bool valid = g < total;
-      const int64_t r = valid ? g / kb : 0, c = valid ? g - r * kb : 0;
+      const int64_t r = pos[u].r, c = pos[u].c;
       const bool live = valid && r < M;
       uint32_t sfb = 0;
       if (live) sfb = encode_and_store(a[u], b[u], gs, six_gs, q + r * (K / 2) + c * 8);
       store_scale(sf, sf_layout, valid, live, r, c, kb, sfb);
+      pos[u].advance(step_r, step_c, kb);
     }
   }
 }

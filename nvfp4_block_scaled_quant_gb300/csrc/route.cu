@@ -362,7 +362,8 @@ __global__ void __launch_bounds__(kDispatchThreads, 1) dispatch_quant_kernel(
   const int64_t kb = H / 16;
   const int64_t gb = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   const bool valid = gb < static_cast<int64_t>(T) * kb;
-  const int64_t t = valid ? gb / kb : 0;
+  // (32-bit division while the index fits)
+  const int64_t t = !valid ? 0 : (gb <= 0x7FFFFFFF ? static_cast<int64_t>(static_cast<uint32_t>(gb) / static_cast<uint32_t>(kb)) : gb / kb);
   const int64_t c = valid ? gb - t * kb : 0;
   // The block's 16 elements and the token's destination rows are loaded first, so
   // their latency overlaps the gs reduction.
