@@ -395,14 +395,11 @@ __device__ __forceinline__ uint32_t e2m1x2_signed(float v0, float v1) {
   return static_cast<uint32_t>(__nv_cvt_float2_to_fp4x2(make_float2(v0, v1), __NV_E2M1, cudaRoundNearest));
 }
 
-// Encode one 16-element block with global multiplier gs (six_gs = fl32(6 * gs)).
-// Returns the E4M3 scale byte; codes[0..1] receive the 8 code bytes (element 0
-// in the low nibble of byte 0).
-__device__ __forceinline__ uint32_t encode_block16(const float (&v)[16], float gs, float six_gs,
-                                                   uint32_t (&codes)[2]) {
-  float amax = 0.f;
-#pragma unroll
-  for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(v[i]));
+// Encode one 16-element block whose largest magnitude is amax, with global multiplier gs
+// (six_gs = fl32(6 * gs)).  Returns the E4M3 scale byte; codes[0..1] receive the 8 code
+// bytes (element 0 in the low nibble of byte 0).
+__device__ __forceinline__ uint32_t encode_block16_amax(const float (&v)[16], float amax, float gs, float six_gs,
+                                                        uint32_t (&codes)[2]) {
   const float s = (six_gs == 0.f) ? 0.f : __fdiv_rn(amax, six_gs);
   const uint32_t sf = f32_to_ue4m3(s);
   const float d = __fmul_rn(ue4m3_to_f32(sf), gs);
@@ -420,6 +417,39 @@ __device__ __forceinline__ uint32_t encode_block16(const float (&v)[16], float g
   codes[0] = w[0];
   codes[1] = w[1];
   return sf;
+}
+
+// Encode one 16-element block with global multiplier gs (six_gs = fl32(6 * gs)).
+// Returns the E4M3 scale byte; codes[0..1] receive the 8 code bytes (element 0
+// in the low nibble of byte 0).
+__device__ __forceinline__ uint32_t encode_block16(const float (&v)[16], float gs, float six_gs,
+                                                   uint32_t (&codes)[2]) {
+  float amax = 0.f;
+#pragma unroll
+  for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(v[i]));
+  return encode_block16_amax(v, amax, gs, six_gs, codes);
+}
+
+// The largest magnitude of 16 bf16 values packed two per word, as fp32: |bf16| orders like
+// its unsigned bits once the sign is cleared, so two halves are compared per instruction.
+__device__ __forceinline__ float amax_bf16x16(const uint32_t (&w)[8]) {
+  uint32_t m = w[0] & 0x7FFF7FFFu;
+#pragma unroll
+  for (int i = 1; i < 8; ++i) m = __vmaxu2(m, w[i] & 0x7FFF7FFFu);
+  return __uint_as_float(max(m & 0xFFFFu, m >> 16) << 16);
+}
+
+// bf16 block (two 16-byte halves of bf16 pairs, element 0 in the low half of the first word)
+// -> codes and scale byte, as encode_block16 on the unpacked values.
+__device__ __forceinline__ uint32_t encode_block16_bf16(const uint32_t (&w)[8], float gs, float six_gs,
+                                                        uint32_t (&codes)[2]) {
+  float v[16];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    v[2 * i] = __uint_as_float(w[i] << 16);
+    v[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+  }
+  return encode_block16_amax(v, amax_bf16x16(w), gs, six_gs, codes);
 }
 
 // The same encoding with one 16-element block spread over four consecutive lanes

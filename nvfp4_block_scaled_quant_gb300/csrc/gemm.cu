@@ -163,14 +163,8 @@ __device__ float quantize_resident_a(const GemmArgs &a, int g, uint8_t *sA, uint
     const uint4 *src = reinterpret_cast<const uint4 *>(x + r * ld + static_cast<int64_t>(g) * K + c * 16);
     const uint4 p = __ldg(src), q = __ldg(src + 1);
     const uint32_t w[8] = {p.x, p.y, p.z, p.w, q.x, q.y, q.z, q.w};
-    float v[16];
-#pragma unroll
-    for (int k = 0; k < 8; ++k) {
-      v[2 * k] = __uint_as_float(w[k] << 16);
-      v[2 * k + 1] = __uint_as_float(w[k] & 0xFFFF0000u);
-    }
     uint32_t codes[2];
-    const uint32_t sfb = encode_block16(v, gs, six_gs, codes);
+    const uint32_t sfb = encode_block16_bf16(w, gs, six_gs, codes);
     const int st = static_cast<int>(c >> 4), j = static_cast<int>(c & 15), rr = static_cast<int>(r);
     const int chunk = (j >> 1) ^ (rr & 7);
     *reinterpret_cast<uint2 *>(sA + st * (kABoxRows * kStageK / 2) + rr * 128 + chunk * 16 + (j & 1) * 8) =
@@ -216,14 +210,8 @@ __device__ float quantize_token_a(const GemmArgs &a, uint8_t *sA, uint8_t *sfa, 
     const uint4 *src = reinterpret_cast<const uint4 *>(x + c * 16);
     const uint4 p = __ldg(src), q = __ldg(src + 1);
     const uint32_t w[8] = {p.x, p.y, p.z, p.w, q.x, q.y, q.z, q.w};
-    float v[16];
-#pragma unroll
-    for (int k = 0; k < 8; ++k) {
-      v[2 * k] = __uint_as_float(w[k] << 16);
-      v[2 * k + 1] = __uint_as_float(w[k] & 0xFFFF0000u);
-    }
     uint32_t codes[2];
-    const uint32_t sfb = encode_block16(v, gs, six_gs, codes);
+    const uint32_t sfb = encode_block16_bf16(w, gs, six_gs, codes);
     const int st = static_cast<int>(c >> 4), j = static_cast<int>(c & 15);
 #pragma unroll
     for (int r = 0; r < 8; ++r)

@@ -61,14 +61,8 @@ __global__ void __launch_bounds__(kAmaxThreads) amax_partials_kernel(const uint1
 // returns the E4M3 scale byte.
 __device__ __forceinline__ uint32_t encode_and_store(uint4 a, uint4 b, float gs, float six_gs, uint8_t *qdst) {
   const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
-  float v[16];
-#pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    v[2 * i] = __uint_as_float(w[i] << 16);
-    v[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
-  }
   uint32_t codes[2];
-  const uint32_t sfb = encode_block16(v, gs, six_gs, codes);
+  const uint32_t sfb = encode_block16_bf16(w, gs, six_gs, codes);
   *reinterpret_cast<uint2 *>(qdst) = make_uint2(codes[0], codes[1]);
   return sfb;
 }

@@ -315,13 +315,7 @@ __device__ __forceinline__ void dispatch_store(const DispatchIn &in, bool valid,
   uint32_t codes[2] = {0u, 0u}, sfb = 0;
   if (valid) {
     const uint32_t w[8] = {in.a.x, in.a.y, in.a.z, in.a.w, in.b.x, in.b.y, in.b.z, in.b.w};
-    float v[16];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      v[2 * i] = __uint_as_float(w[i] << 16);
-      v[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
-    }
-    sfb = encode_block16(v, gs, six_gs, codes);
+    sfb = encode_block16_bf16(w, gs, six_gs, codes);
   }
   const int lane = threadIdx.x & 31;
   uint32_t word = sfb << ((lane & 3) * 8);
