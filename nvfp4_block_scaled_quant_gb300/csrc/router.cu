@@ -250,14 +250,16 @@ __global__ void __launch_bounds__(kRtThreads, 1)
         for (int q = 0; q < 16; ++q) r[q] = 0u;
       }
       if (t < T && c * 16 < e_live) {  // E % 16 == 0 is not required: the tail is written one by one
-        if (c * 16 + 16 <= e_live) {
+        // 16-byte stores need every row start 16-byte aligned: E % 4 == 0 (the buffer is 256-aligned)
+        if (c * 16 + 16 <= e_live && (E & 3) == 0) {
           float4 *d4 = reinterpret_cast<float4 *>(dst + c * 16);
 #pragma unroll
           for (int q = 0; q < 4; ++q)
             d4[q] = make_float4(__uint_as_float(r[4 * q]), __uint_as_float(r[4 * q + 1]), __uint_as_float(r[4 * q + 2]),
                                 __uint_as_float(r[4 * q + 3]));
         } else {
-          for (int q = 0; q < e_live - c * 16; ++q) dst[c * 16 + q] = __uint_as_float(r[q]);
+          const int n = min(16, e_live - c * 16);
+          for (int q = 0; q < n; ++q) dst[c * 16 + q] = __uint_as_float(r[q]);
         }
       }
     }
@@ -284,14 +286,14 @@ __global__ void __launch_bounds__(kTopkThreads) router_topk_kernel(const float *
   pdl_wait();
   pdl_trigger();
   const int64_t t = blockIdx.x;
+  const int64_t sstride = T * E;
   for (int64_t e = threadIdx.x; e < E; e += blockDim.x) {
     const float *p = partial + t * E + e;
-    const int64_t sstride = T * E;
     float v = 0.f;
     int sp = 0;
     for (; sp + 4 <= splits; sp += 4) {  // four loads in flight, summed in split order
-      const float a = __ldg(p + sp * sstride), b = __ldg(p + (sp + 1) * sstride), c = __ldg(p + (sp + 2) * sstride),
-                  d = __ldg(p + (sp + 3) * sstride);
+      const float a = __ldg(p + sp * sstride), b = __ldg(p + (sp + 1) * sstride),
+                  c = __ldg(p + (sp + 2) * sstride), d = __ldg(p + (sp + 3) * sstride);
       v = __fadd_rn(__fadd_rn(__fadd_rn(__fadd_rn(v, a), b), c), d);
     }
     for (; sp < splits; ++sp) v = __fadd_rn(v, __ldg(p + sp * sstride));

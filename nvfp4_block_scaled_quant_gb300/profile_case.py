@@ -4,6 +4,7 @@
     python -m nvfp4_block_scaled_quant_gb300.profile_case decode --T 1 --experts 384 --iters 8
     python -m nvfp4_block_scaled_quant_gb300.profile_case gemm --M 4096 --iters 3
     python -m nvfp4_block_scaled_quant_gb300.profile_case linear --M 32 --iters 3
+    python -m nvfp4_block_scaled_quant_gb300.profile_case grouped --M 1 --iters 3
     python -m nvfp4_block_scaled_quant_gb300.profile_case dispatch --T 128 --iters 3
     python -m nvfp4_block_scaled_quant_gb300.profile_case norm --M 128 --iters 3
     python -m nvfp4_block_scaled_quant_gb300.profile_case router --T 128 --iters 3
@@ -19,7 +20,8 @@ T = 128, the decode routing below, the 32 chunks at once for T = 4096; no expert
 weights are needed); ``norm`` the fused RMSNorm -> NVFP4 quantiser over hidden
 7168; ``router`` the router gate (384 experts, hidden 7168, top-8); ``quant``
 the activation quantiser over K = 7168 (M = 1024 .. 16384 are the large-GEMM
-sweep's activations).
+sweep's activations); ``linear`` the dense 1536 -> 16384 linear and ``grouped`` the
+fixed-group 8 x (4096 -> 1024) linear at ``--M`` tokens.
 """
 
 from __future__ import annotations
@@ -34,7 +36,7 @@ from . import build as B
 
 def main(argv=None):
     p = argparse.ArgumentParser()
-    p.add_argument("case", choices=["moe", "decode", "gemm", "linear", "dispatch", "norm", "router", "quant"])
+    p.add_argument("case", choices=["moe", "decode", "gemm", "linear", "grouped", "dispatch", "norm", "router", "quant"])
     p.add_argument("--T", type=int, default=1)
     p.add_argument("--experts", type=int, default=64)
     p.add_argument("--M", type=int, default=4096)
@@ -110,6 +112,12 @@ def main(argv=None):
         for i in range(a.iters):
             x = workloads.activations(a.M, 7168, seed=80 + i, device=dev)
             ops.quantize_act(x)
+    elif a.case == "grouped":
+        _, G, K, N = workloads.GROUPED_LINEAR.get(a.M, (a.M, 8, 4096, 1024))
+        gw = model.make_grouped_weight(G, N, K, seed=90, device=dev)
+        x = workloads.activations(a.M, G * K, seed=95, device=dev, outliers=True)
+        for _ in range(a.iters):
+            ops.grouped_linear(x, gw.w, gw.sf, gw.ws2, G, N)
     else:
         K, N = 1536, 16384
         dw = model.make_dense_weight(N, K, seed=50, device=dev)

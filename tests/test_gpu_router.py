@@ -80,3 +80,28 @@ def test_router_drives_moe_end_to_end():
     rid, rw, _ = O.router(x.float().numpy(), ref, k)
     res = O.moe_forward(x.float().numpy(), rid, rw.astype(np.float32), oe, E, a2, shared=oe(E))
     assert O.cosine(bf16_to_np(y), res.y) > 0.999
+
+
+def test_router_expert_count_not_multiple_of_4_and_unaligned_logits():
+    """E not a multiple of 4 (the logits kernel's rows of split partials are then not 16-byte
+    aligned, so it stores them one float at a time) against the oracle, and logits written to a
+    4-byte-aligned (not 16-byte-aligned) buffer equal the aligned ones bit for bit."""
+    from nvfp4_block_scaled_quant_gb300 import _lib
+    for E in (21, 24):
+        wg, ref = _gate(E, 512, 11)
+        x = workloads.activations(6, 512, seed=12, device="cpu")
+        ids, w, logits = ops.router(x.to(DEV), wg, 3, want_logits=True)
+        _check_router(x, wg, ref, 3)
+        T, H = x.shape
+        xd = x.to(DEV)
+        buf = torch.full((T * E + 4,), float("nan"), dtype=torch.float32, device=DEV)
+        ids2 = torch.empty(T, 3, dtype=torch.int32, device=DEV)
+        w2 = torch.empty(T, 3, dtype=torch.float32, device=DEV)
+        n = int(_lib.lib().nvfp4_router_workspace_bytes(T, E))
+        ws = torch.empty(max(n, 256), dtype=torch.uint8, device=DEV)
+        _lib.call("nvfp4_router", xd.data_ptr(), T, H, wg.data_ptr(), E, 3, ids2.data_ptr(), w2.data_ptr(),
+                  buf.data_ptr() + 4, ws.data_ptr(), ws.numel(), torch.cuda.current_stream().cuda_stream)
+        torch.cuda.synchronize()
+        assert torch.isnan(buf[0]) and torch.isnan(buf[T * E + 1:]).all()
+        assert torch.equal(buf[1:T * E + 1].view(T, E), logits)
+        assert torch.equal(ids2, ids) and torch.equal(w2, w)
