@@ -15,7 +15,12 @@
 //               lane quarter: A and B scales of rows 32q..32q+31), then the
 //               epilogue, one accumulator row per thread.
 // The two CTAs of an SM overlap each other's epilogues and keep two MMA
-// issuers busy (one accumulator buffer each).  Every wait is bounded (kPipelineTimeoutNs); a role that gives up
+// issuers busy (one accumulator buffer each).  The linears that quantise their own
+// activations (one CTA per SM, at most 32 tokens) swap the operands instead: the
+// weight tile is the MMA's 128 rows and the tokens its N, and warps 6..8 join warp 1
+// as MMA issuers, each taking every fourth K stage into its own 32-column
+// accumulator (one issuing thread is held ~100 ns per MMA; issuers in different
+// warps overlap).  Every wait is bounded (kPipelineTimeoutNs); a role that gives up
 // sets a shared abort flag, the others drain and the CTA frees TMEM and exits
 // with NVFP4_DEVERR_PIPELINE_TIMEOUT raised.
 //
@@ -79,6 +84,10 @@ __device__ __forceinline__ uint4 rotate_words(uint4 v, int j) {
 // instruction descriptor: E2M1 x E2M1, UE4M3 scales, K-major A and B, M=128, N=128
 constexpr uint32_t kIdesc = (1u << 7) | (1u << 10) | ((uint32_t(kBlockN) >> 3) << 17) |
                             ((uint32_t(kBlockM) >> 4) << 24);
+
+// Swapped-operand linears (weights M = 128, tokens N = 32)
+constexpr uint32_t kIdescSwap = (1u << 7) | (1u << 10) | ((uint32_t(kABoxRows) >> 3) << 17) |
+                                ((uint32_t(kBlockM) >> 4) << 24);
 
 // The one-token kernel's fused down projection: per stage kP2RowTiles w2 row tiles of 128
 // rows x one 64-element K step (32 bytes, 32-byte swizzle), each one MMA of M = 128 (w2 rows)
@@ -246,7 +255,8 @@ __device__ void tok1_schedule(const GemmArgs &a, int4 *sched, int lane) {
 }
 
 template <int kEpi, bool kSmallA, bool kQuantA>
-__global__ void __launch_bounds__(kGemmThreads, (kQuantA && kEpi != static_cast<int>(Epi::kW13)) ? 1 : kCtasPerSm)
+__global__ void __launch_bounds__(Ring<kSmallA, kQuantA, kQuantA && kEpi == static_cast<int>(Epi::kW13)>::kThreads,
+                                  (kQuantA && kEpi != static_cast<int>(Epi::kW13)) ? 1 : kCtasPerSm)
     nvfp4_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                       const __grid_constant__ CUtensorMap tmB,
                       const __grid_constant__ CUtensorMap tmBs,
@@ -292,10 +302,10 @@ __global__ void __launch_bounds__(kGemmThreads, (kQuantA && kEpi != static_cast<
       mbar_init(&sf_ready[s], 4);
     }
     for (int i = 0; i < 2; ++i) {
-      mbar_init(&tfull[i], 1);
+      mbar_init(&tfull[i], R::kIssuers);
       mbar_init(&tempty[i], 4);
     }
-    mbar_init(drain, 1);
+    mbar_init(drain, R::kIssuers);
     mbar_init(h_full, 1);
     mbar_init(h_empty, 4);
     if constexpr (kTok1) {
@@ -508,9 +518,11 @@ __global__ void __launch_bounds__(kGemmThreads, (kQuantA && kEpi != static_cast<
       }
       if (!same) raise_device_error(args.err, NVFP4_DEVERR_INTERNAL);
     }
-  } else if (warp == 1) {
+  } else if (warp == 1 || (R::kIssuers > 1 && warp >= 6)) {
     if (lane == 0) {
-      // ------------------------------------------------------------ MMA issuer
+      // ------------------------------------------------------------ MMA issuer(s)
+      // Issuer iss takes the K stages ks with ks % kIssuers == iss into its own accumulator.
+      const int iss = warp == 1 ? 0 : warp - 5;
       int stage = 0;
       uint32_t phase = 0;
       int it = 0;
@@ -526,9 +538,16 @@ __global__ void __launch_bounds__(kGemmThreads, (kQuantA && kEpi != static_cast<
           break;
         }
         tc_fence_after();
-        const uint32_t d_tmem = tmem_base + acc * kBlockN;
+        const uint32_t d_tmem = tmem_base + (R::kSwapAB ? iss * kABoxRows : acc * kBlockN);
         for (int ks = 0; ks < k_stages; ++ks) {
           const int kv = min(4, k_steps - 4 * ks);
+          if (R::kIssuers > 1 && ks % R::kIssuers != iss) {  // another issuer's stage
+            if (++stage == S) {
+              stage = 0;
+              phase ^= 1;
+            }
+            continue;
+          }
           if (!mbar_wait_bounded(&full[stage], phase, abort_flag, args.err,
                                  kPipelineTimeoutNs)) {
             ok = false;
@@ -541,13 +560,17 @@ __global__ void __launch_bounds__(kGemmThreads, (kQuantA && kEpi != static_cast<
             break;
           }
           tc_fence_after();
-          const uint32_t sf_col = tmem_base + kTmemAccCols + stage * kTmemSfCols;
+          const uint32_t sf_col = tmem_base + R::kAccColsR + stage * kTmemSfCols;
           const uint64_t adesc = smem_desc(sA0 + (kQuantA ? ks : stage) * kAB, 16, 1024, 2);
           const uint64_t bdesc = smem_desc(sB0 + stage * kTileBytesB, 16, 1024, 2);
           for (int j = 0; j < kv; ++j) {
             // +32 bytes of K per step inside the 128-byte swizzle row (descriptor units of 16 B)
-            tc_mma_nvf4(d_tmem, adesc + 2 * j, bdesc + 2 * j, kIdesc, sf_col + j * 4,
-                        sf_col + 16 + j * 4, (ks | j) != 0);
+            if constexpr (R::kSwapAB)  // weights x tokens: the scale blocks swap places too
+              tc_mma_nvf4(d_tmem, bdesc + 2 * j, adesc + 2 * j, kIdescSwap, sf_col + 16 + j * 4, sf_col + j * 4,
+                          ks != iss || j != 0);
+            else
+              tc_mma_nvf4(d_tmem, adesc + 2 * j, bdesc + 2 * j, kIdesc, sf_col + j * 4, sf_col + 16 + j * 4,
+                          ks != 0 || j != 0);
           }
           tc_commit(&empty[stage]);
           if (++stage == S) {
@@ -575,7 +598,7 @@ __global__ void __launch_bounds__(kGemmThreads, (kQuantA && kEpi != static_cast<
                 break;
               }
               tc_fence_after();
-              const uint32_t sf_col = tmem_base + kTmemAccCols + stage * kTmemSfCols;
+              const uint32_t sf_col = tmem_base + R::kAccColsR + stage * kTmemSfCols;
               for (int q = 0; q < nq; ++q)
                 tc_mma_nvf4(tmem_base + b * (kP2RowTiles * kP2N) + q * kP2N,
                             smem_desc(sB0 + stage * kTileBytesB + q * kP2TileBytes, 16, 256, 6), bdesc2, kIdescP2,
@@ -615,7 +638,7 @@ __global__ void __launch_bounds__(kGemmThreads, (kQuantA && kEpi != static_cast<
     // receives the same copy of the block: lane 32 q + r, column (scale address + c)
     // holds the word of row 32 c + r, the arrangement the MMA reads scales from.  This
     // warp writes its own quarter; lane r loads the 16 bytes at 16 r.
-    const uint32_t sf_lane = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + kTmemAccCols;
+    const uint32_t sf_lane = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + R::kAccColsR;
     const int sf_off = lane * 16;
     int sstage = 0;
     uint32_t sphase = 0;
@@ -713,7 +736,7 @@ __global__ void __launch_bounds__(kGemmThreads, (kQuantA && kEpi != static_cast<
                              static_cast<uint32_t>(acc * kBlockN);
       // A warp whose 32 accumulator rows are all padding (a group's last m tile) has
       // nothing to read or store; it only releases the accumulator.
-      const bool warp_live = quarter * 32 < t.rows;
+      const bool warp_live = R::kSwapAB || quarter * 32 < t.rows;
       // Each warp hands its accumulator lanes back to the MMA as soon as it has read
       // them, so the next tile's MMAs overlap this tile's global stores.
       auto release = [&]() {
@@ -934,6 +957,35 @@ __global__ void __launch_bounds__(kGemmThreads, (kQuantA && kEpi != static_cast<
         }
       } else if (!warp_live) {
         release();
+      } else if constexpr (kEpi == static_cast<int>(Epi::kLinear) && R::kSwapAB) {
+        // accumulator lane m is output feature 128 nt + m, column r token a_row0 + r; the
+        // issuers' accumulators (as many as there are K stages, up to kIssuers) add up
+        const float alpha = gs_scalar * ws2;
+        const int nacc = min(R::kIssuers, k_stages);
+        const int64_t ld = args.out_ld;
+        __nv_bfloat16 *y = static_cast<__nv_bfloat16 *>(args.out) + static_cast<int64_t>(t.a_row0) * ld +
+                           static_cast<int64_t>(t.g) * args.out_group_cols + t.nt * kBlockN + m;
+        if (t.rows <= 0) release();
+#pragma unroll 1
+        for (int c0 = 0; c0 < t.rows; c0 += 16) {
+          uint32_t r[R::kIssuers][16];
+#pragma unroll
+          for (int i = 0; i < R::kIssuers; ++i)
+            if (i < nacc) tmem_ld16(tbase + i * kABoxRows + c0, r[i]);
+          tmem_ld_wait();
+          if (c0 + 16 >= t.rows) release();
+          float v[16];
+#pragma unroll
+          for (int q = 0; q < 16; ++q) v[q] = __uint_as_float(r[0][q]);
+#pragma unroll
+          for (int i = 1; i < R::kIssuers; ++i)
+            if (i < nacc)
+#pragma unroll
+              for (int q = 0; q < 16; ++q) v[q] += __uint_as_float(r[i][q]);
+#pragma unroll
+          for (int q = 0; q < 16; ++q)
+            if (c0 + q < t.rows) y[(c0 + q) * ld] = __float2bfloat16_rn(v[q] * alpha);
+        }
       } else if constexpr (kEpi == static_cast<int>(Epi::kLinear)) {
         const float alpha = gs_scalar * ws2;
         const bool out32 = (reinterpret_cast<uintptr_t>(args.out) & 31u) == 0;
@@ -1087,7 +1139,7 @@ cudaError_t launch_gemm_t(const CUtensorMap &ta, const CUtensorMap &tb, const CU
   }
   // A grid no larger than the SM count asks for enough shared memory to keep one CTA per
   // SM, so its tiles spread over as many SMs as there are tiles.
-  return launch_pdl(nvfp4_gemm_kernel<kEpi, kSmallA, kQuantA>, dim3(grid), dim3(kGemmThreads),
+  return launch_pdl(nvfp4_gemm_kernel<kEpi, kSmallA, kQuantA>, dim3(grid), dim3(R::kThreads),
                     one_per_sm ? R::kSmemSolo : R::kSmem, s, ta, tb, tbs, tc ? *tc : tb, args);
 }
 

@@ -80,6 +80,16 @@ struct Ring {
   // SFA: one 2 KB block per A slot, or (kTok1) the token row's four scale words per K stage
   static constexpr int kSfaBytes = kTok1 ? 512 : kASlots * kSfBytesStage;
   static constexpr uint32_t kTmemColsR = (kQuantA && !kTok1) ? 512 : kTmemCols;
+  // MMA issuing threads.  One tcgen05.mma holds its issuing thread ~100 ns whatever its N,
+  // while issuers in different warps run side by side.  The one-tile-per-CTA linears
+  // (kQuantA) are chains of such issues: they swap the operands (the weight tile is the
+  // MMA's 128 rows, the at most 32 tokens its N), so that an accumulator is 32 columns, and
+  // four issuers take the K stages round-robin into an accumulator each; the epilogue adds
+  // them, every warp for 32 output features.
+  static constexpr bool kSwapAB = kQuantA && !kTok1;
+  static constexpr int kIssuers = kSwapAB ? 4 : 1;
+  static constexpr uint32_t kAccColsR = kSwapAB ? kIssuers * kABoxRows : kTmemAccCols;  // scale columns follow
+  static constexpr int kThreads = kGemmThreads + (kIssuers - 1) * 32;  // warps 6.. : the further issuers
   static constexpr int kHBytes = kSmallA && (!kQuantA || kTok1) ? kABoxRows * kHRowFloats * 4 : 0;  // h of a tile
   static constexpr int kSchedBytes = kTok1 ? kTok1SchedBytes : 0;
   // kTok1: the re-quantised h of a tile as the fused down projection's B operand (32 rows of
@@ -91,7 +101,7 @@ struct Ring {
   // Requested (not used) by launches that want one CTA per SM: two of these do not fit.
   static constexpr size_t kSmemSolo = (kQuantA && !kTok1) ? kSmem : 2 * kSmem;
   static_assert(!kQuantA || kSmallA, "the resident A holds one 32-row box per K stage");
-  static_assert(kTmemAccCols + kStagesR * kTmemSfCols <= kTmemColsR, "TMEM budget");
+  static_assert(kAccColsR + kStagesR * kTmemSfCols <= kTmemColsR, "TMEM budget");
   static_assert((3 * kStagesR + 7) * 8 + 8 + 24 <= kGemmBarrierBytes, "barrier region and scratch");
   static_assert(kSmemSolo <= 232448, "per-block shared memory limit");
   static_assert((kQuantA && !kTok1) || 2 * (kSmem + 1024) <= 233472, "two CTAs per SM");
