@@ -117,9 +117,9 @@ __device__ __forceinline__ void named_barrier_sync(int id, int threads) {
 // the static scale), then encode the K columns of group g (columns g*K .. g*K+K-1; g = 0
 // for a dense linear) with the activation quantiser's arithmetic into the resident A
 // boxes (one 32-row, 128-byte-swizzled 4 KB box per 256-element K stage: 16-byte chunk
-// c of row r sits at chunk c ^ (r & 7)) and their scale blocks (row r's four scales of a
-// 64-element K step at 16 r in that step's 512-byte block).  CTA 0 writes gs out; every
-// CTA returns the same gs.
+// c of row r sits at chunk c ^ (r & 7)) and their scale words (row r's four scales of a
+// 64-element K step at 4 r in that step's 128 bytes).  CTA 0 writes gs out; every CTA
+// returns the same gs.
 __device__ float quantize_resident_a(const GemmArgs &a, int g, uint8_t *sA, uint8_t *sSFA, uint32_t *scratch,
                                      int tid) {
   const int64_t M = a.dense_M, K = a.K, ld = a.qa_ld;
@@ -178,7 +178,7 @@ __device__ float quantize_resident_a(const GemmArgs &a, int g, uint8_t *sA, uint
     const int chunk = (j >> 1) ^ (rr & 7);
     *reinterpret_cast<uint2 *>(sA + st * (kABoxRows * kStageK / 2) + rr * 128 + chunk * 16 + (j & 1) * 8) =
         make_uint2(codes[0], codes[1]);
-    sSFA[st * kSfBytesStage + ((j >> 2) & 3) * kSfBytesPerKStep + rr * 16 + (j & 3)] = static_cast<uint8_t>(sfb);
+    sSFA[(st * 4 + ((j >> 2) & 3)) * 128 + rr * 4 + (j & 3)] = static_cast<uint8_t>(sfb);  // K step, row, block
   }
   fence_proxy_async_shared();  // the MMAs read the boxes through the async proxy
   named_barrier_sync(1, 128);
@@ -284,7 +284,7 @@ __global__ void __launch_bounds__(Ring<kSmallA, kQuantA, kQuantA && kEpi == stat
   uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(drain + 3);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_holder + 1);
   uint32_t *q_scratch = reinterpret_cast<uint32_t *>(tmem_holder + 2);  // kQuantA: 5 words
-  float *h_s = reinterpret_cast<float *>(reinterpret_cast<uint8_t *>(full) + kGemmBarrierBytes);  // R::kHBytes
+  float *h_s = reinterpret_cast<float *>(reinterpret_cast<uint8_t *>(full) + R::kBarBytes);  // R::kHBytes
   int4 *sched = reinterpret_cast<int4 *>(reinterpret_cast<uint8_t *>(h_s) + R::kHBytes);  // kTok1
   uint8_t *p2_tile = reinterpret_cast<uint8_t *>(sched) + R::kSchedBytes;             // kTok1: h rows, B of the
   uint32_t *p2_sfw = reinterpret_cast<uint32_t *>(p2_tile + 32 * 32);                 // fused w2; their scales
@@ -679,9 +679,12 @@ __global__ void __launch_bounds__(Ring<kSmallA, kQuantA, kQuantA && kEpi == stat
         uint32_t ra[16], rb[16];
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-          // kTok1: A rows 0..7 are the token (its scale word of the K step), the rest zero
+          // kTok1: A rows 0..7 are the token (its scale word of the K step), the rest zero;
+          // kQuantA: the scale word of row `lane` (rows 32.. of the block are not read: N <= 32)
           const uint4 wa = kTok1 ? make_uint4(j < kv && lane < 8 ? reinterpret_cast<const uint32_t *>(sSFA)[4 * ks + j]
                                                                  : 0u, 0u, 0u, 0u)
+                           : kQuantA ? make_uint4(j < kv ? reinterpret_cast<const uint32_t *>(sSFA)[(4 * ks + j) * 32 + lane]
+                                                         : 0u, 0u, 0u, 0u)
                            : j < kv ? *reinterpret_cast<const uint4 *>(pa + j * kSfBytesPerKStep)
                                     : make_uint4(0u, 0u, 0u, 0u);
           const uint4 wb = j < kv ? *reinterpret_cast<const uint4 *>(pb + j * kSfBytesPerKStep)

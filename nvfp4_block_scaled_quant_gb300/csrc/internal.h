@@ -54,7 +54,7 @@ constexpr size_t kGemmBarrierBytes = 256;
 constexpr int kQuantMaxK = 4096;
 // Every CTA quantises all of x: the fused path pays off while x is small.
 constexpr int64_t kQuantMaxElems = 16384;
-constexpr int kQuantStages = 6;
+constexpr int kQuantStages = 7;
 
 // Small-A MoE tiles keep their (at most 32) rows in the first TMEM lane quarter, so one
 // warp reads the whole accumulator.  It leaves the tile's h = SiLU(gate) * up in shared
@@ -77,8 +77,9 @@ struct Ring {
   static constexpr int kABytes = kTok1 ? 1024 : (kSmallA ? kABoxRows * kStageK / 2 : kTileBytesA);
   static constexpr int kASlots =
       kTok1 ? kTok1MaxK / kStageK : (kQuantA ? kQuantMaxK / kStageK : kStagesR);  // A slots
-  // SFA: one 2 KB block per A slot, or (kTok1) the token row's four scale words per K stage
-  static constexpr int kSfaBytes = kTok1 ? 512 : kASlots * kSfBytesStage;
+  // SFA: one 2 KB block per A slot; kQuantA: the (at most 32) rows' scale words only, 128 bytes
+  // per K step; kTok1: the token row's four scale words per K stage
+  static constexpr int kSfaBytes = kTok1 ? 512 : (kQuantA ? kASlots * 4 * 128 : kASlots * kSfBytesStage);
   static constexpr uint32_t kTmemColsR = (kQuantA && !kTok1) ? 512 : kTmemCols;
   // MMA issuing threads.  One tcgen05.mma holds its issuing thread ~100 ns whatever its N,
   // while issuers in different warps run side by side.  The one-tile-per-CTA linears
@@ -95,14 +96,15 @@ struct Ring {
   // kTok1: the re-quantised h of a tile as the fused down projection's B operand (32 rows of
   // 32 bytes, 32-byte swizzle) and its rows' scale words
   static constexpr int kP2Bytes = kTok1 ? 32 * 32 + 32 * 4 + 4 * 8 : 0;  // + p2_full[2], p2_empty[2]
+  static constexpr size_t kBarBytes = (3 * kStagesR + 7) * 8 + 8 + 24 <= kGemmBarrierBytes ? kGemmBarrierBytes : 512;
   static constexpr size_t kSmem = 1024 /* alignment slack */ + static_cast<size_t>(kASlots) * kABytes + kSfaBytes +
                                   static_cast<size_t>(kStagesR) * (kTileBytesB + kSfBytesStage) +
-                                  kGemmBarrierBytes + kHBytes + kSchedBytes + kP2Bytes;
+                                  kBarBytes + kHBytes + kSchedBytes + kP2Bytes;
   // Requested (not used) by launches that want one CTA per SM: two of these do not fit.
   static constexpr size_t kSmemSolo = (kQuantA && !kTok1) ? kSmem : 2 * kSmem;
   static_assert(!kQuantA || kSmallA, "the resident A holds one 32-row box per K stage");
   static_assert(kAccColsR + kStagesR * kTmemSfCols <= kTmemColsR, "TMEM budget");
-  static_assert((3 * kStagesR + 7) * 8 + 8 + 24 <= kGemmBarrierBytes, "barrier region and scratch");
+  static_assert((3 * kStagesR + 7) * 8 + 8 + 24 <= kBarBytes, "barrier region and scratch");
   static_assert(kSmemSolo <= 232448, "per-block shared memory limit");
   static_assert((kQuantA && !kTok1) || 2 * (kSmem + 1024) <= 233472, "two CTAs per SM");
   static_assert(kABytes % 1024 == 0, "128-byte swizzle atoms stay 1024-byte aligned");
