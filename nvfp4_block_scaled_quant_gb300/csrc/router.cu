@@ -275,7 +275,7 @@ __global__ void __launch_bounds__(kRtThreads, 1)
 // memory; warp 0 then takes the softmax over E (<= 1024) logits and the top-k by repeated warp
 // arg-max (larger probability first, lower expert id on ties), weights renormalised over the
 // k chosen.  logits (optional) receives the summed logits.
-constexpr int kTopkThreads = 256;
+constexpr int kTopkThreads = 512;
 template <int kPer>  // experts per lane: E <= 32 * kPer
 __global__ void __launch_bounds__(kTopkThreads) router_topk_kernel(const float *__restrict__ partial, int splits,
                                                                    int64_t T, int64_t E, int topk,
@@ -288,15 +288,15 @@ __global__ void __launch_bounds__(kTopkThreads) router_topk_kernel(const float *
   const int64_t t = blockIdx.x;
   const int64_t sstride = T * E;
   for (int64_t e = threadIdx.x; e < E; e += blockDim.x) {
+    // every split's partial in flight at once (one round trip), then summed in split order
     const float *p = partial + t * E + e;
+    float part[kRouterMaxSplits];
+#pragma unroll
+    for (int sp = 0; sp < kRouterMaxSplits; ++sp) part[sp] = sp < splits ? __ldg(p + sp * sstride) : 0.f;
     float v = 0.f;
-    int sp = 0;
-    for (; sp + 4 <= splits; sp += 4) {  // four loads in flight, summed in split order
-      const float a = __ldg(p + sp * sstride), b = __ldg(p + (sp + 1) * sstride),
-                  c = __ldg(p + (sp + 2) * sstride), d = __ldg(p + (sp + 3) * sstride);
-      v = __fadd_rn(__fadd_rn(__fadd_rn(__fadd_rn(v, a), b), c), d);
-    }
-    for (; sp < splits; ++sp) v = __fadd_rn(v, __ldg(p + sp * sstride));
+#pragma unroll
+    for (int sp = 0; sp < kRouterMaxSplits; ++sp)
+      if (sp < splits) v = __fadd_rn(v, part[sp]);
     s_logit[e] = v;
     if (logits != nullptr) logits[t * E + e] = v;
   }
