@@ -34,6 +34,17 @@ def test_grouped_linear_ragged(M, G, K, N):
     _run(M, G, K, N, seed=M * 31 + G)
 
 
+@pytest.mark.parametrize("M,G,K,N,gs", [(7, 4, 768, 256, None), (32, 2, 512, 128, None), (3, 2, 320, 384, None),
+                                        (1, 8, 4096, 1024, 0.0021), (16, 3, 1024, 640, None)])
+def test_grouped_linear_fused_shapes(M, G, K, N, gs):
+    """At most 32 tokens: the one-launch path (the GEMM CTAs quantise x themselves, one tile per
+    CTA, the K stages round-robin over four MMA issuers).  K = 768 and 320 leave issuers without a
+    stage (K = 320 ends in a one-step stage), M = 32 and 16 fill the token columns, N = 640 five
+    tiles per group.  Every output against the oracle, dynamic and static gs."""
+    _run(M, G, K, N, seed=M * 17 + G * 5 + K, gs=gs)
+    assert ops.device_error() == (0, 0)
+
+
 @pytest.mark.parametrize("M", sorted(workloads.GROUPED_LINEAR))
 def test_grouped_linear_oproj_workload(M):
     """8 groups x 4096 inputs -> 1024 outputs each, every output checked."""
