@@ -15,7 +15,7 @@
 //   warp 1       owns the pair's tensor memory; in the even CTA, one lane issues the MMAs
 //                of every other stage for both CTAs and commits them to the barriers of
 //                both; warp 14's first lane issues the stages in between (into the same
-//                accumulator, handing the turn back and forth through the turn barriers);
+//                accumulator, handing the turn on through the turn barriers);
 //   warps 2..5   scale staging: each stage's A scales (this CTA's 128 rows) and the B scales
 //                of all 256 B rows of the tile (the pair MMA reads B's scales for every N
 //                row from each CTA's own tensor memory: 8 columns per K step, column c
@@ -40,9 +40,9 @@ constexpr int kPHalf = 128;
 constexpr int kPStages = 5;
 constexpr int kPScaleWarps = 4;
 constexpr int kPEpiWarps = 8;
-// MMA issuers of the even CTA: warp 1 and warp kPIssuer2 take the launch's stages in turn
+// MMA issuers of the even CTA: warp 1 and warps kPIssuerWarp0.. take the launch's stages in turn
 constexpr int kPIssuers = 2;
-constexpr int kPIssuer2 = 2 + kPScaleWarps + kPEpiWarps;
+constexpr int kPIssuerWarp0 = 2 + kPScaleWarps + kPEpiWarps;
 constexpr int kPThreads = (2 + kPScaleWarps + kPEpiWarps + kPIssuers - 1) * 32;
 constexpr int kPTileA = kPHalf * kStageK / 2;    // 16 KiB: 128 rows x 128 bytes
 constexpr int kPTileB = kPHalf * kStageK / 2;    // 16 KiB
@@ -54,7 +54,7 @@ constexpr uint32_t kPTmemCols = 512;
 constexpr uint32_t kPAccCols = kPN;              // fp32 accumulator: 128 lanes x 256 columns
 static_assert(kPAccCols + kPStages * kPSfCols <= kPTmemCols, "TMEM budget");
 static_assert(kPSmem <= 232448, "per-block shared memory limit");
-static_assert((4 * kPStages + 5) * 8 + 16 <= kGemmBarrierBytes, "barrier region");
+static_assert((4 * kPStages + 3 + kPIssuers) * 8 + 16 <= kGemmBarrierBytes, "barrier region");
 
 // E2M1 x E2M1, UE4M3 scales, K-major A and B, M = 256 (the pair), N = 256.
 constexpr uint32_t kPIdesc = (1u << 7) | (1u << 10) | ((uint32_t(kPN) >> 3) << 17) | ((uint32_t(kPM) >> 4) << 24);
@@ -76,7 +76,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
   uint64_t *tempty = tfull + 1;           // used in the even CTA
   uint64_t *drain = tempty + 1;
   uint64_t *turn = drain + 1;             // turn[i]: issuer i may issue its next stage (even CTA)
-  uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(turn + 2);
+  uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(turn + kPIssuers);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_holder + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -92,7 +92,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
     mbar_init(tfull, kPIssuers);
     mbar_init(tempty, 2 * kPEpiWarps);
     mbar_init(drain, kPIssuers);
-    for (int i = 0; i < 2; ++i) mbar_init(&turn[i], 1);
+    for (int i = 0; i < kPIssuers; ++i) mbar_init(&turn[i], 1);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -178,18 +178,19 @@ __global__ void __launch_bounds__(kPThreads, 1)
           if (issued & (1u << s)) mbar_wait_bounded(&full[s], (issued >> (s + 8)) & 1u, &never, nullptr, 100000000ull);
       }
     }
-  } else if (warp == 1 || warp == kPIssuer2) {
+  } else if (warp == 1 || warp >= kPIssuerWarp0) {
     if (leader && lane == 0) {
       // ------------------------------------------------------------ MMA issuers (even CTA)
-      // Stage g of the launch (counted over all tiles) is issued by issuer g % 2, into the one
+      // Stage g of the launch (counted over all tiles) is issued by issuer g % kPIssuers, into the one
       // accumulator.  One tcgen05.mma holds its issuing thread about its own execution time;
-      // with two issuers, one thread's waits for its next stage (scales staged, operands landed)
-      // and its commits overlap the other's MMAs.  The hand-off orders the accumulator's
+      // with several issuers, one thread's waits for its next stage (scales staged, operands
+      // landed) and its commits overlap the others' MMAs.  The hand-off orders the accumulator's
       // updates: after its stage, an issuer fences (tcgen05.fence::before_thread_sync) and
-      // arrives on the other's turn barrier; the other waits on it and fences
-      // (::after_thread_sync) before its MMAs.  The turns strictly alternate, so a turn
-      // barrier never runs a phase ahead of its waiter.
-      const int iss = warp == 1 ? 0 : 1;
+      // arrives on the next issuer's turn barrier; that one waits on it and fences
+      // (::after_thread_sync) before its MMAs.  The turns go round in order, so a turn barrier
+      // never runs a phase ahead of its waiter.
+      const int iss = warp == 1 ? 0 : warp - kPIssuerWarp0 + 1;
+      const int pred = (iss + kPIssuers - 1) % kPIssuers;  // the issuer of the stage before ours
       int stage = 0;
       uint32_t phase = 0;
       int it = 0;
@@ -199,7 +200,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
       for (int idx = first; ok && idx < total_tiles; idx += active, ++it) {
         for (int ks = 0; ks < k_stages; ++ks, ++g) {
           const int kv = min(4, k_steps - 4 * ks);
-          if ((g & 1) == iss) {
+          if (g % kPIssuers == iss) {
             // the tile's first stage waits for the epilogue to have read the previous tile
             if (ks == 0 && !mbar_wait_bounded_cluster(tempty, (it & 1) ^ 1, abort_flag, args.err, kPipelineTimeoutNs)) {
               ok = false;
@@ -207,7 +208,8 @@ __global__ void __launch_bounds__(kPThreads, 1)
             }
             // both CTAs' operands of the stage have landed and their scales are in tensor memory
             if (!mbar_wait_bounded_cluster(&sf_ready[stage], phase, abort_flag, args.err, kPipelineTimeoutNs) ||
-                (g > 0 && !mbar_wait_bounded(&turn[iss], ((g - 1) >> 1) & 1, abort_flag, args.err, kPipelineTimeoutNs))) {
+                (g > 0 &&
+                 !mbar_wait_bounded(&turn[iss], ((g - 1 - pred) / kPIssuers) & 1, abort_flag, args.err, kPipelineTimeoutNs))) {
               ok = false;
               break;
             }
@@ -219,7 +221,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
               tc_mma_nvf4_pair(tmem_base, adesc + 2 * j, bdesc + 2 * j, kPIdesc, sf_col + j * 4, sf_col + 16 + j * 8,
                                (ks | j) != 0);
             tc_fence_before();
-            mbar_arrive(&turn[iss ^ 1]);  // the other issuer takes stage g + 1
+            mbar_arrive(&turn[(iss + 1) % kPIssuers]);  // the next issuer takes stage g + 1
             tc_commit_pair(&empty[stage], 0x3);
           }
           if (++stage == kPStages) {
