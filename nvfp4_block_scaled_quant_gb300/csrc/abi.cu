@@ -595,6 +595,9 @@ static nvfp4_status gemm_dense(const char *fn, DeviceInfo *d, const uint8_t *xq,
 // Dense (G = 1) or fixed-group linear for 1 <= M <= 32 rows in one launch: the GEMM CTAs
 // quantise x themselves (same arithmetic as nvfp4_quantize_act) into resident A boxes.
 // Every CTA reduces the amax over all G*K columns and quantises its group's K of them.
+// Weight stages of a fused linear tile prefetched into L2 beyond the ring at kernel start.
+constexpr int kLinearEarlyL2 = 16;
+
 static nvfp4_status linear_fused(const char *fn, DeviceInfo *d, const void *x, int64_t M, int64_t G, int64_t K,
                                  int64_t N, const uint8_t *w, const uint8_t *w_sf, const float *ws2, bool dyn,
                                  float *gs, void *y, cudaStream_t s) {
@@ -615,6 +618,7 @@ static nvfp4_status linear_fused(const char *fn, DeviceInfo *d, const void *x, i
   a.out_group_cols = static_cast<int>(N);
   a.err = d->flags;
   a.early_b = 1;  // the weights are older than the previous launch (prepare_weights does not trigger early)
+  a.early_l2 = kLinearEarlyL2;  // the tile's stages beyond the ring: into L2 before the dependency wait
   a.qa_x = x;
   a.qa_ld = G * K;
   a.qa_gs_static = dyn ? nullptr : gs;
