@@ -551,6 +551,10 @@ size_t nvfp4_linear_workspace_bytes(int64_t M, int64_t K) {
 
 // Dense GEMM, or G uniform groups where group g multiplies columns [gK, (g+1)K) of the
 // quantised activations with its own weight (G, N, K/2) into output columns [gN, (g+1)N).
+// Weight stages of a linear's first tile prefetched into L2 beyond the ring at kernel start
+// (before the dependency wait: the weights are older than the previous launch).
+constexpr int kLinearEarlyL2 = 16;
+
 static nvfp4_status gemm_dense(const char *fn, DeviceInfo *d, const uint8_t *xq, const uint8_t *xsf, const float *gs,
                                int64_t M, int64_t K, int64_t N, const uint8_t *w, const uint8_t *w_sf,
                                const float *ws2, void *y, cudaStream_t s, int early_b = 0, int64_t G = 1) {
@@ -579,6 +583,7 @@ static nvfp4_status gemm_dense(const char *fn, DeviceInfo *d, const uint8_t *xq,
   a.out_group_cols = static_cast<int>(N);
   a.err = d->flags;
   a.early_b = early_b;
+  a.early_l2 = early_b ? kLinearEarlyL2 : 0;  // the first tile's stages beyond the ring, into L2
   if (pair_clusters > 0) {
     const int64_t pair_tiles = ((M + 255) / 256) * (N / 256);
     const int clusters = static_cast<int>(pair_tiles < pair_clusters ? pair_tiles : pair_clusters);
@@ -595,9 +600,6 @@ static nvfp4_status gemm_dense(const char *fn, DeviceInfo *d, const uint8_t *xq,
 // Dense (G = 1) or fixed-group linear for 1 <= M <= 32 rows in one launch: the GEMM CTAs
 // quantise x themselves (same arithmetic as nvfp4_quantize_act) into resident A boxes.
 // Every CTA reduces the amax over all G*K columns and quantises its group's K of them.
-// Weight stages of a fused linear tile prefetched into L2 beyond the ring at kernel start.
-constexpr int kLinearEarlyL2 = 16;
-
 static nvfp4_status linear_fused(const char *fn, DeviceInfo *d, const void *x, int64_t M, int64_t G, int64_t K,
                                  int64_t N, const uint8_t *w, const uint8_t *w_sf, const float *ws2, bool dyn,
                                  float *gs, void *y, cudaStream_t s) {
