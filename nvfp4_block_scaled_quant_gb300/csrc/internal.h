@@ -48,8 +48,8 @@ constexpr size_t kGemmBarrierBytes = 256;
 // calls, M <= 32), the A slot shrinks to one 32-row box and 4 stages fit in less
 // shared memory: a third more weight bytes in flight per CTA.
 // With kQuantA (dense linear, M <= 32, K <= kQuantMaxK) the CTA quantises the bf16
-// activations itself: every K stage's A box and scale block stay resident (written once
-// by the epilogue warps), and a ring of kQuantStages stages carries the weights only.
+// activations itself: every K stage's A box and its rows' scale words stay resident (written
+// once by the epilogue warps), and a ring of kQuantStages stages carries the weights only.
 // One CTA per SM, owning all 512 TMEM columns.
 constexpr int kQuantMaxK = 4096;
 // Every CTA quantises all of x: the fused path pays off while x is small.
