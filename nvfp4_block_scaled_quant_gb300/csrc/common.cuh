@@ -472,14 +472,16 @@ __device__ __forceinline__ uint32_t encode_block16_x4(float4 v, float gs, float 
 }
 
 // Row and column of a flat block index g = r * kb + c, advanced by a fixed step with no
-// division in the loop (the step's own quotient and remainder are computed once).
-struct RowCol {
-  int64_t r, c;
-  __device__ __forceinline__ void init(int64_t g, int64_t kb) {
+// division in the loop (the step's own quotient and remainder are computed once).  Idx is
+// int32_t where every index and offset of the launch fits, which halves the integer work.
+template <typename Idx>
+struct RowColT {
+  Idx r, c;
+  __device__ __forceinline__ void init(Idx g, Idx kb) {
     r = g / kb;
     c = g - r * kb;
   }
-  __device__ __forceinline__ void advance(int64_t step_r, int64_t step_c, int64_t kb) {
+  __device__ __forceinline__ void advance(Idx step_r, Idx step_c, Idx kb) {
     c += step_c;
     r += step_r;
     if (c >= kb) {
@@ -488,6 +490,7 @@ struct RowCol {
     }
   }
 };
+using RowCol = RowColT<int64_t>;
 
 // Byte offset of the 32-bit word holding scales (row r, columns 4c'..4c'+3) in
 // the swizzled layout, for a buffer whose rows carry K elements (kc4 = K / 64
@@ -495,6 +498,10 @@ struct RowCol {
 __device__ __forceinline__ size_t sf_word_offset(int64_t r, int64_t col4, int64_t kc4) {
   return (static_cast<size_t>(r >> 7) * kc4 + col4) * 512u + static_cast<size_t>(r & 31) * 16u +
          static_cast<size_t>((r & 127) >> 5) * 4u;
+}
+// The same in 32-bit arithmetic, for buffers below 2^31 bytes.
+__device__ __forceinline__ uint32_t sf_word_offset32(uint32_t r, uint32_t col4, uint32_t kc4) {
+  return ((r >> 7) * kc4 + col4) * 512u + (r & 31u) * 16u + ((r & 127u) >> 5) * 4u;
 }
 
 // Global scale from the block partials: gs = fl32(amax / 2688).

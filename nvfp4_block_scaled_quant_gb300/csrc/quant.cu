@@ -70,8 +70,9 @@ __device__ __forceinline__ uint32_t encode_and_store(uint4 a, uint4 b, float gs,
 // Store the scale byte of block (r, c): one byte (row-major layout) or, in the swizzled
 // layout, one 32-bit word per four consecutive blocks of a row, gathered from lanes 4i..4i+3
 // (all 32 lanes must call this together).
-__device__ __forceinline__ void store_scale(uint8_t *sf, int sf_layout, bool valid, bool live, int64_t r, int64_t c,
-                                            int64_t kb, uint32_t sfb) {
+template <typename Idx>
+__device__ __forceinline__ void store_scale(uint8_t *sf, int sf_layout, bool valid, bool live, Idx r, Idx c, Idx kb,
+                                            uint32_t sfb) {
   if (sf_layout == NVFP4_SF_LINEAR) {
     if (live) sf[r * kb + c] = static_cast<uint8_t>(sfb);
   } else {
@@ -79,7 +80,13 @@ __device__ __forceinline__ void store_scale(uint8_t *sf, int sf_layout, bool val
     uint32_t word = sfb << ((lane & 3) * 8);
     word |= __shfl_xor_sync(0xffffffffu, word, 1);
     word |= __shfl_xor_sync(0xffffffffu, word, 2);
-    if (valid && (lane & 3) == 0) *reinterpret_cast<uint32_t *>(sf + sf_word_offset(r, c >> 2, kb >> 2)) = word;
+    if (valid && (lane & 3) == 0) {
+      if constexpr (sizeof(Idx) == 4)
+        *reinterpret_cast<uint32_t *>(sf + sf_word_offset32(static_cast<uint32_t>(r), static_cast<uint32_t>(c >> 2),
+                                                            static_cast<uint32_t>(kb >> 2))) = word;
+      else
+        *reinterpret_cast<uint32_t *>(sf + sf_word_offset(r, c >> 2, kb >> 2)) = word;
+    }
   }
 }
 
@@ -88,31 +95,33 @@ __device__ __forceinline__ void store_scale(uint8_t *sf, int sf_layout, bool val
 // blocks with kQuantUnroll blocks' loads in flight per thread, and each CTA derives gs once.
 // The swizzled output also covers the padding rows up to a multiple of 128 (scale 0, no codes).
 constexpr int kQuantUnroll = 2;
+template <typename Idx>  // int32_t when every block index and byte offset of the launch fits
 __global__ void __launch_bounds__(kQuantThreads, kStreamCtasPerSm) quantize_kernel(
-    const uint16_t *__restrict__ x, int64_t M, int64_t K, int64_t ldx,
+    const uint16_t *__restrict__ x, int64_t M_, int64_t K_, int64_t ldx_,
     const uint32_t *__restrict__ partials, int nparts, const float *__restrict__ gs_static,
     float *__restrict__ gs_out, uint8_t *__restrict__ q, uint8_t *__restrict__ sf,
     int sf_layout, int64_t rows_total) {
   __shared__ uint32_t scratch[32];
   pdl_wait();
   pdl_trigger();
-  const int64_t kb = K / 16;
-  const int64_t total = rows_total * kb;
-  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  const Idx M = static_cast<Idx>(M_), K = static_cast<Idx>(K_), ldx = static_cast<Idx>(ldx_);
+  const Idx kb = K / 16;
+  const Idx total = static_cast<Idx>(rows_total) * kb;
+  const Idx stride = static_cast<Idx>(gridDim.x) * static_cast<Idx>(blockDim.x);
   const int lane = threadIdx.x & 31;
-  const int64_t wbase0 = static_cast<int64_t>(blockIdx.x) * blockDim.x + (threadIdx.x & ~31);
+  const Idx wbase0 = static_cast<Idx>(blockIdx.x) * static_cast<Idx>(blockDim.x) + static_cast<Idx>(threadIdx.x & ~31);
   // (row, block) of each of this thread's kQuantUnroll blocks, advanced without division
-  const int64_t step = kQuantUnroll * stride;
-  const int64_t step_r = step / kb, step_c = step - step_r * kb;
-  RowCol pos[kQuantUnroll];
+  const Idx step = kQuantUnroll * stride;
+  const Idx step_r = step / kb, step_c = step - step_r * kb;
+  RowColT<Idx> pos[kQuantUnroll];
 #pragma unroll
   for (int u = 0; u < kQuantUnroll; ++u) pos[u].init(wbase0 + u * stride + lane, kb);
   // the first blocks' loads are issued before the gs reduction, which their latency overlaps
   uint4 a[kQuantUnroll], b[kQuantUnroll];
-  auto load = [&](int64_t wb) {
+  auto load = [&](Idx wb) {
 #pragma unroll
     for (int u = 0; u < kQuantUnroll; ++u) {
-      const int64_t g = wb + u * stride + lane;
+      const Idx g = wb + u * stride + lane;
       a[u] = b[u] = make_uint4(0u, 0u, 0u, 0u);
       if (g < total && pos[u].r < M) {
         const uint4 *src = reinterpret_cast<const uint4 *>(x + pos[u].r * ldx + pos[u].c * 16);
@@ -127,11 +136,11 @@ __global__ void __launch_bounds__(kQuantThreads, kStreamCtasPerSm) quantize_kern
     // Small input (at most kInlineAmaxElems elements): every block reduces the whole of x
     // itself, one launch fewer.  Block 0 writes gs (0 when M == 0).
     uint32_t m = 0;
-    const int64_t chunks = K / 8;
-    RowCol ix;
-    ix.init(threadIdx.x, chunks);
-    const int64_t sr = blockDim.x / chunks, sc = blockDim.x - sr * chunks;
-    for (int64_t i = threadIdx.x; i < M * chunks; i += blockDim.x, ix.advance(sr, sc, chunks)) {
+    const Idx chunks = K / 8;
+    RowColT<Idx> ix;
+    ix.init(static_cast<Idx>(threadIdx.x), chunks);
+    const Idx sr = static_cast<Idx>(blockDim.x) / chunks, sc = static_cast<Idx>(blockDim.x) - sr * chunks;
+    for (Idx i = threadIdx.x; i < M * chunks; i += blockDim.x, ix.advance(sr, sc, chunks)) {
       const uint4 v = __ldg(reinterpret_cast<const uint4 *>(x + ix.r * ldx) + ix.c);
       m = max(m, max(max(max_abs_bf16x2(v.x), max_abs_bf16x2(v.y)), max(max_abs_bf16x2(v.z), max_abs_bf16x2(v.w))));
     }
@@ -145,13 +154,13 @@ __global__ void __launch_bounds__(kQuantThreads, kStreamCtasPerSm) quantize_kern
     gs = *gs_static;
   }
   const float six_gs = __fmul_rn(6.0f, gs);
-  for (int64_t wb = wbase0; wb < total; wb += step) {  // uniform over the warp
+  for (Idx wb = wbase0; wb < total; wb += step) {  // uniform over the warp
     if (wb != wbase0) load(wb);
 #pragma unroll
     for (int u = 0; u < kQuantUnroll; ++u) {
-      const int64_t g = wb + u * stride + lane;
+      const Idx g = wb + u * stride + lane;
       const bool valid = g < total;
-      const int64_t r = pos[u].r, c = pos[u].c;
+      const Idx r = pos[u].r, c = pos[u].c;
       const bool live = valid && r < M;
       uint32_t sfb = 0;
       if (live) sfb = encode_and_store(a[u], b[u], gs, six_gs, q + r * (K / 2) + c * 8);
@@ -245,9 +254,17 @@ cudaError_t launch_quantize(const void *x, int64_t M, int64_t K, int64_t ldx,
   const int64_t items = rows_total * (K / 16);
   int64_t blocks = items > 0 ? (items + kQuantThreads - 1) / kQuantThreads : 1;
   if (blocks > stream_grid_cap()) blocks = stream_grid_cap();
-  return launch_pdl(quantize_kernel, dim3(static_cast<unsigned>(blocks)), dim3(kQuantThreads), 0, s,
-                    static_cast<const uint16_t *>(x), M, K, ldx, partials, nparts, gs_static, gs_out, q, sf,
-                    sf_layout, rows_total);
+  // 32-bit indexing when every block index (plus a grid step) and every byte offset of x, the
+  // codes and the scales stays below 2^31
+  const int64_t lim = int64_t(1) << 31;
+  const bool small = rows_total * (K / 16) + 2 * kQuantUnroll * blocks * kQuantThreads < lim &&
+                     (M > 0 ? (M - 1) * ldx + K : 0) * 2 < lim && rows_total * K < lim;
+  return small ? launch_pdl(quantize_kernel<int32_t>, dim3(static_cast<unsigned>(blocks)), dim3(kQuantThreads), 0, s,
+                            static_cast<const uint16_t *>(x), M, K, ldx, partials, nparts, gs_static, gs_out, q, sf,
+                            sf_layout, rows_total)
+               : launch_pdl(quantize_kernel<int64_t>, dim3(static_cast<unsigned>(blocks)), dim3(kQuantThreads), 0, s,
+                            static_cast<const uint16_t *>(x), M, K, ldx, partials, nparts, gs_static, gs_out, q, sf,
+                            sf_layout, rows_total);
 }
 
 cudaError_t launch_act_quant(const void *x, int64_t M, int64_t K, int64_t ldx, bool dynamic, uint32_t *partials,
