@@ -126,31 +126,33 @@ __global__ void __launch_bounds__(kNormThreads) rmsnorm_stats_kernel(
 // 16-element blocks of the normalised rows, walked by a fixed grid as the plain quantiser
 // (kNormUnroll blocks' loads in flight per thread, gs derived once per CTA); same layouts.
 constexpr int kNormUnroll = 2;
+template <typename Idx>  // int32_t when every block index and byte offset of the launch fits
 __global__ void __launch_bounds__(kNormThreads, kStreamCtasPerSm) rmsnorm_quantize_kernel(
-    const uint16_t *__restrict__ x, int64_t M, int64_t K, int64_t ldx, const uint16_t *__restrict__ gamma,
+    const uint16_t *__restrict__ x, int64_t M_, int64_t K_, int64_t ldx_, const uint16_t *__restrict__ gamma,
     const float *__restrict__ inv_rms, const uint32_t *__restrict__ partials, int nparts,
     const float *__restrict__ gs_static, float *__restrict__ gs_out, uint8_t *__restrict__ q,
     uint8_t *__restrict__ sf, int sf_layout, int64_t rows_total) {
   __shared__ uint32_t scratch[32];
   pdl_wait();
   pdl_trigger();
-  const int64_t kb = K / 16;
-  const int64_t total = rows_total * kb;
-  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  const Idx M = static_cast<Idx>(M_), K = static_cast<Idx>(K_), ldx = static_cast<Idx>(ldx_);
+  const Idx kb = K / 16;
+  const Idx total = static_cast<Idx>(rows_total) * kb;
+  const Idx stride = static_cast<Idx>(gridDim.x) * static_cast<Idx>(blockDim.x);
   const int lane = threadIdx.x & 31;
-  const int64_t wbase0 = static_cast<int64_t>(blockIdx.x) * blockDim.x + (threadIdx.x & ~31);
+  const Idx wbase0 = static_cast<Idx>(blockIdx.x) * static_cast<Idx>(blockDim.x) + static_cast<Idx>(threadIdx.x & ~31);
   // (row, block) of each of this thread's kNormUnroll blocks, advanced without division
-  const int64_t step = kNormUnroll * stride;
-  const int64_t step_r = step / kb, step_c = step - step_r * kb;
-  RowCol pos[kNormUnroll];
+  const Idx step = kNormUnroll * stride;
+  const Idx step_r = step / kb, step_c = step - step_r * kb;
+  RowColT<Idx> pos[kNormUnroll];
 #pragma unroll
   for (int u = 0; u < kNormUnroll; ++u) pos[u].init(wbase0 + u * stride + lane, kb);
   uint4 a[kNormUnroll], b[kNormUnroll];
   float inv[kNormUnroll];
-  auto load = [&](int64_t wb) {
+  auto load = [&](Idx wb) {
 #pragma unroll
     for (int u = 0; u < kNormUnroll; ++u) {
-      const int64_t g = wb + u * stride + lane;
+      const Idx g = wb + u * stride + lane;
       a[u] = b[u] = make_uint4(0u, 0u, 0u, 0u);
       inv[u] = 0.f;
       if (g < total && pos[u].r < M) {
@@ -170,13 +172,13 @@ __global__ void __launch_bounds__(kNormThreads, kStreamCtasPerSm) rmsnorm_quanti
     gs = *gs_static;
   }
   const float six_gs = __fmul_rn(6.0f, gs);
-  for (int64_t wb = wbase0; wb < total; wb += step) {  // uniform over the warp
+  for (Idx wb = wbase0; wb < total; wb += step) {  // uniform over the warp
     if (wb != wbase0) load(wb);
 #pragma unroll
     for (int u = 0; u < kNormUnroll; ++u) {
-      const int64_t g = wb + u * stride + lane;
+      const Idx g = wb + u * stride + lane;
       const bool valid = g < total;
-      const int64_t r = pos[u].r, c = pos[u].c;
+      const Idx r = pos[u].r, c = pos[u].c;
       pos[u].advance(step_r, step_c, kb);
       const bool live = valid && r < M;
       uint32_t sfb = 0;
@@ -201,8 +203,13 @@ __global__ void __launch_bounds__(kNormThreads, kStreamCtasPerSm) rmsnorm_quanti
         uint32_t word = sfb << ((lane & 3) * 8);
         word |= __shfl_xor_sync(0xffffffffu, word, 1);
         word |= __shfl_xor_sync(0xffffffffu, word, 2);
-        if (valid && (lane & 3) == 0)
-          *reinterpret_cast<uint32_t *>(sf + sf_word_offset(r, c >> 2, kb >> 2)) = word;
+        if (valid && (lane & 3) == 0) {
+          if constexpr (sizeof(Idx) == 4)
+            *reinterpret_cast<uint32_t *>(sf + sf_word_offset32(static_cast<uint32_t>(r), static_cast<uint32_t>(c >> 2),
+                                                                static_cast<uint32_t>(kb >> 2))) = word;
+          else
+            *reinterpret_cast<uint32_t *>(sf + sf_word_offset(r, c >> 2, kb >> 2)) = word;
+        }
       }
     }
   }
@@ -225,7 +232,12 @@ cudaError_t launch_rmsnorm_quantize(const void *x, int64_t M, int64_t K, int64_t
   const int64_t items = rows_total * (K / 16);
   int64_t blocks = items > 0 ? (items + kNormThreads - 1) / kNormThreads : 1;
   if (blocks > stream_grid_cap()) blocks = stream_grid_cap();
-  return launch_pdl(rmsnorm_quantize_kernel, dim3(static_cast<unsigned>(blocks)), dim3(kNormThreads), 0, s,
+  // 32-bit indexing when every block index (plus a grid step) and every byte offset fits
+  const int64_t lim = int64_t(1) << 31;
+  const bool small = rows_total * (K / 16) + 2 * kNormUnroll * blocks * kNormThreads < lim &&
+                     (M > 0 ? (M - 1) * ldx + K : 0) * 2 < lim && rows_total * K < lim;
+  auto kernel = small ? rmsnorm_quantize_kernel<int32_t> : rmsnorm_quantize_kernel<int64_t>;
+  return launch_pdl(kernel, dim3(static_cast<unsigned>(blocks)), dim3(kNormThreads), 0, s,
                     static_cast<const uint16_t *>(x), M, K, ldx, static_cast<const uint16_t *>(gamma), inv_rms,
                     partials, nparts, gs_static, gs_out, q, sf, sf_layout, rows_total);
 }
