@@ -524,26 +524,31 @@ def run_secondary(state, args):
         y = torch.empty(M, N, dtype=torch.bfloat16, device=dev)
         gs = torch.empty(1, dtype=torch.float32, device=dev)
         it = [0]
+        # gs_mode 0: the activation global scale from x's amax on every call; 1: a static scale,
+        # read (the dynamic call's value, as a warm-up calibration leaves it)
+        for gs_mode in (0, 1):
 
-        def lin(st=stream, d=None):
-            if d is None:
-                d = dws[it[0] % 16]
-                it[0] += 1
-            ops.call("nvfp4_linear", x.data_ptr(), M, K, N, d.w.data_ptr(), d.sf.data_ptr(), d.ws2.data_ptr(), 0,
-                     gs.data_ptr(), y.data_ptr(), wsl.data_ptr(), wsl.numel(), st.cuda_stream)
+            def lin(st=stream, d=None, gs_mode=gs_mode):
+                if d is None:
+                    d = dws[it[0] % 16]
+                    it[0] += 1
+                ops.call("nvfp4_linear", x.data_ptr(), M, K, N, d.w.data_ptr(), d.sf.data_ptr(), d.ws2.data_ptr(),
+                         gs_mode, gs.data_ptr(), y.data_ptr(), wsl.data_ptr(), wsl.numel(), st.cuda_stream)
 
-        def lin16(st):
-            for d in dws:
-                lin(st, d)
+            def lin16(st, lin=lin):
+                for d in dws:
+                    lin(st, d)
 
-        eager_ms = time_fn(lin, 160)
-        ms = graph_time_fn(lin16, 16, 10)
-        b = N * K * (0.5 + 1 / 16) + M * K * 2 + M * N * 2
-        out.append({"workload": f"dense_linear_M{M}_K{K}_N{N}", "us_per_call": ms * 1e3,
-                    "hbm_gbs": b / (ms / 1e3) / 1e9, "hbm_frac": b / (ms / 1e3) / 1e9 / hbm,
-                    "tflops": 2 * M * N * K / (ms / 1e3) / 1e12, "eager_us_per_call": eager_ms * 1e3,
-                    "note": "quantise + GEMM; 16 weight copies rotated (230 MB > L2), replayed as one CUDA graph "
-                            "(eager_us_per_call: plain calls, bounded by the host)"})
+            eager_ms = time_fn(lin, 160)
+            ms = graph_time_fn(lin16, 16, 10)
+            b = N * K * (0.5 + 1 / 16) + M * K * 2 + M * N * 2
+            out.append({"workload": f"dense_linear_M{M}_K{K}_N{N}" + ("_static_gs" if gs_mode else ""),
+                        "us_per_call": ms * 1e3,
+                        "hbm_gbs": b / (ms / 1e3) / 1e9, "hbm_frac": b / (ms / 1e3) / 1e9 / hbm,
+                        "tflops": 2 * M * N * K / (ms / 1e3) / 1e12, "eager_us_per_call": eager_ms * 1e3,
+                        "note": ("quantise (static, calibrated gs) + GEMM" if gs_mode else "amax + quantise + GEMM")
+                                + "; 16 weight copies rotated (230 MB > L2), replayed as one CUDA graph "
+                                  "(eager_us_per_call: plain calls, bounded by the host)"})
     del dws
     # fixed-group linear (grouped o-projection): 8 x (4096 -> 1024); 16 weight copies rotated (> L2)
     for M in sorted(workloads.GROUPED_LINEAR):
@@ -554,26 +559,31 @@ def run_secondary(state, args):
         y = torch.empty(M, G * N, dtype=torch.bfloat16, device=dev)
         gs = torch.empty(1, dtype=torch.float32, device=dev)
         it = [0]
+        for gs_mode in (0, 1):  # dynamic, then the static (calibrated) scale as for the dense linear
 
-        def grp(st=stream, d=None):
-            if d is None:
-                d = gws[it[0] % 16]
-                it[0] += 1
-            ops.call("nvfp4_grouped_linear", x.data_ptr(), M, G, K, N, d.w.data_ptr(), d.sf.data_ptr(),
-                     d.ws2.data_ptr(), 0, gs.data_ptr(), y.data_ptr(), wsg.data_ptr(), wsg.numel(), st.cuda_stream)
+            def grp(st=stream, d=None, gs_mode=gs_mode):
+                if d is None:
+                    d = gws[it[0] % 16]
+                    it[0] += 1
+                ops.call("nvfp4_grouped_linear", x.data_ptr(), M, G, K, N, d.w.data_ptr(), d.sf.data_ptr(),
+                         d.ws2.data_ptr(), gs_mode, gs.data_ptr(), y.data_ptr(), wsg.data_ptr(), wsg.numel(),
+                         st.cuda_stream)
 
-        def grp16(st):
-            for d in gws:
-                grp(st, d)
+            def grp16(st, grp=grp):
+                for d in gws:
+                    grp(st, d)
 
-        eager_ms = time_fn(grp, 160)
-        ms = graph_time_fn(grp16, 16, 10)
-        b = G * N * K * (0.5 + 1 / 16) + M * G * K * 2 + M * G * N * 2
-        out.append({"workload": f"grouped_linear_M{M}_G{G}_K{K}_N{N}", "us_per_call": ms * 1e3,
-                    "hbm_gbs": b / (ms / 1e3) / 1e9, "hbm_frac": b / (ms / 1e3) / 1e9 / hbm,
-                    "tflops": 2 * M * G * N * K / (ms / 1e3) / 1e12, "eager_us_per_call": eager_ms * 1e3,
-                    "note": "quantise + grouped GEMM; 16 weight copies rotated (300 MB > L2), replayed as one CUDA "
-                            "graph (eager_us_per_call: plain calls, bounded by the host)"})
+            eager_ms = time_fn(grp, 160)
+            ms = graph_time_fn(grp16, 16, 10)
+            b = G * N * K * (0.5 + 1 / 16) + M * G * K * 2 + M * G * N * 2
+            out.append({"workload": f"grouped_linear_M{M}_G{G}_K{K}_N{N}" + ("_static_gs" if gs_mode else ""),
+                        "us_per_call": ms * 1e3,
+                        "hbm_gbs": b / (ms / 1e3) / 1e9, "hbm_frac": b / (ms / 1e3) / 1e9 / hbm,
+                        "tflops": 2 * M * G * N * K / (ms / 1e3) / 1e12, "eager_us_per_call": eager_ms * 1e3,
+                        "note": ("quantise (static, calibrated gs) + grouped GEMM" if gs_mode
+                                 else "amax + quantise + grouped GEMM")
+                                + "; 16 weight copies rotated (300 MB > L2), replayed as one CUDA graph "
+                                  "(eager_us_per_call: plain calls, bounded by the host)"})
         del gws
     # routing + dispatch (stages a and b): latency-bound at small T, reported in microseconds
     for T in (1, 8, 64, 128, 4096):
