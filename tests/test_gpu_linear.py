@@ -37,12 +37,14 @@ def test_linear_ragged_shapes(M, K, N):
 
 
 @pytest.mark.parametrize("M,K,N", [(512, 256, 256), (700, 320, 512), (640, 1536, 768), (1000, 64, 256),
-                                   (1300, 7168, 512), (2049, 512, 1024)])
+                                   (1300, 7168, 512), (2049, 512, 1024), (10240, 704, 512)])
 def test_linear_pair_tiles_ragged(M, K, N):
     """Shapes of the CTA-pair path (M >= 512, N % 256 == 0, 256 x 256 tiles): M not a multiple
     of 256 (a last tile whose second half starts past the padded scale rows at M = 640 and
     M = 2049), K with a short last stage (K = 320, 64), every output checked, through
-    nvfp4_linear and nvfp4_gemm."""
+    nvfp4_linear and nvfp4_gemm.  M = 10240, N = 512 is 80 tiles, so clusters take two tiles
+    in turn; K = 704 is three stages (the last of three K steps), so the two turn-taking MMA
+    issuers alternate in opening a tile."""
     x = workloads.activations(M, K, seed=M + 3 * K + N, device="cpu", outliers=True)
     wp, sfp, ws2, wq = _weights(N, K, seed=M + N)
     xd = x.to(DEV)
