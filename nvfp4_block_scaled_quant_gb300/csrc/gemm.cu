@@ -1033,8 +1033,10 @@ __global__ void __launch_bounds__(Ring<kSmallA, kQuantA, kQuantA && kEpi == stat
         const float six_gs2 = __fmul_rn(6.0f, gs2);
         const int64_t p = t.a_row0 + m;
         const int I = args.out_ld * 2;
-        // h of this thread's row; the accumulator is handed back once it has been read
-        float h[4][16];
+        // h of this thread's row, one 16-column block at a time (encoded at once, so that one
+        // block of h is live); the accumulator is handed back once it has been read
+        uint32_t codes[8];
+        uint32_t sfw = 0;
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
           uint32_t rg[16], ru[16];
@@ -1042,25 +1044,17 @@ __global__ void __launch_bounds__(Ring<kSmallA, kQuantA, kQuantA && kEpi == stat
           tmem_ld16(tbase + kBlockN / 2 + c * 16, ru);
           tmem_ld_wait();
           if (c == 3) release();
+          float h[16];
 #pragma unroll
           for (int i = 0; i < 16; ++i)
-            h[c][i] = silu_mul(__uint_as_float(rg[i]) * alpha, __uint_as_float(ru[i]) * alpha);
-        }
-        if (args.h_debug != nullptr && row_ok) {
-#pragma unroll
-          for (int c = 0; c < 4; ++c) {
+            h[i] = silu_mul(__uint_as_float(rg[i]) * alpha, __uint_as_float(ru[i]) * alpha);
+          if (args.h_debug != nullptr && row_ok) {
             float4 *hd = reinterpret_cast<float4 *>(args.h_debug + p * I + t.nt * 64 + c * 16);
 #pragma unroll
-            for (int i = 0; i < 4; ++i)
-              hd[i] = make_float4(h[c][4 * i], h[c][4 * i + 1], h[c][4 * i + 2], h[c][4 * i + 3]);
+            for (int i = 0; i < 4; ++i) hd[i] = make_float4(h[4 * i], h[4 * i + 1], h[4 * i + 2], h[4 * i + 3]);
           }
-        }
-        uint32_t codes[8];
-        uint32_t sfw = 0;
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
           uint32_t cw[2];
-          const uint32_t sfb = encode_block16(h[c], gs2, six_gs2, cw);
+          const uint32_t sfb = encode_block16(h, gs2, six_gs2, cw);
           codes[2 * c] = cw[0];
           codes[2 * c + 1] = cw[1];
           sfw |= sfb << (8 * c);

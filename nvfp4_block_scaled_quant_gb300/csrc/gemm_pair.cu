@@ -55,6 +55,11 @@ constexpr uint32_t kPAccCols = kPN;              // fp32 accumulator: 128 lanes 
 static_assert(kPAccCols + kPStages * kPSfCols <= kPTmemCols, "TMEM budget");
 static_assert(kPSmem <= 232448, "per-block shared memory limit");
 static_assert((4 * kPStages + 3 + kPIssuers) * 8 + 16 <= kGemmBarrierBytes, "barrier region");
+// An issuer's previous own stage is g - kPIssuers, issued (in turn order) after every
+// stage before it.  The slot of its next stage g has therefore landed stage g - kPStages,
+// i.e. its barriers are at most one phase behind, only if kPIssuers <= kPStages; with more
+// issuers a parity wait on that slot could match a phase two behind and pass too early.
+static_assert(kPIssuers <= kPStages, "turn-taking issuers: at most one per ring stage");
 
 // E2M1 x E2M1, UE4M3 scales, K-major A and B, M = 256 (the pair), N = 256.
 constexpr uint32_t kPIdesc = (1u << 7) | (1u << 10) | ((uint32_t(kPN) >> 3) << 17) | ((uint32_t(kPM) >> 4) << 24);

@@ -208,14 +208,10 @@ __global__ void __launch_bounds__(kRtThreads, 1)
   } else if (warp == 1) {
     if (lane == 0 && k1 > k0) {
       // ------------------------------------------------------------ MMA issuer
-      bool ok = true;
       const uint32_t sA0 = smem_u32(sA), sB0 = smem_u32(sB);
       for (int k = k0; k < k1; ++k) {
         const int i = k - k0, s = i % kRtStages;
-        if (!mbar_wait_bounded(&full[s], (i / kRtStages) & 1u, abort_flag, err, kPipelineTimeoutNs)) {
-          ok = false;
-          break;
-        }
+        if (!mbar_wait_bounded(&full[s], (i / kRtStages) & 1u, abort_flag, err, kPipelineTimeoutNs)) break;
         tc_fence_after();
         const uint64_t adesc = smem_desc(sA0 + s * kRtBox, 16, 1024, 2);
         const uint64_t bdesc = smem_desc(sB0 + s * kRtBox, 16, 1024, 2);
@@ -224,7 +220,6 @@ __global__ void __launch_bounds__(kRtThreads, 1)
           tc_mma_bf16(tmem_base, adesc + 2 * j, bdesc + 2 * j, kRtIdesc, (i | j) != 0);
         tc_commit(&empty[s]);
       }
-      (void)ok;
       tc_commit(done);  // fires once every MMA issued above has completed
     }
   } else {

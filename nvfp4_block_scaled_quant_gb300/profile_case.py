@@ -11,7 +11,8 @@
     python -m nvfp4_block_scaled_quant_gb300.profile_case quant --M 4096 --iters 3
 
 ``moe`` runs 128-token prefill chunks (hidden 7168, intermediate 2048, top-8
-Zipf(1.1) routing, shared expert) over ``--experts`` experts, so the weights
+Zipf(1.1) routing, shared expert; ``--T`` above 1 sets the batch instead, e.g.
+4096 for the whole prefill's 128-row tiles) over ``--experts`` experts, so the weights
 held on the device stay a few GB while the per-tile work of every kernel is
 the same as in the 384-expert layer.  The kernels launch in the same order and
 configuration as in the benchmark.  ``dispatch`` runs routing + amax + the
@@ -50,13 +51,14 @@ def main(argv=None):
     if a.case == "moe":
         cfg = workloads.PREFILL
         E = a.experts
+        T = a.T if a.T > 1 else cfg.T
         W = model.make_moe_weights(E, cfg.H, cfg.I, workloads.BENCH_WEIGHT_SEED, dev, shared=True)
-        sub = workloads.MoEConfig("profile", cfg.T, cfg.H, cfg.I, E, cfg.topk, True, "zipf", True)
+        sub = workloads.MoEConfig("profile", T, cfg.H, cfg.I, E, cfg.topk, True, "zipf", True)
         a2 = torch.full((E + 1,), 0.02, dtype=torch.float32, device=dev)
-        ws = ops.moe_workspace(cfg.T, cfg.H, cfg.I, E, cfg.topk, True, dev)
-        y = torch.empty(cfg.T, cfg.H, dtype=torch.bfloat16, device=dev)
+        ws = ops.moe_workspace(T, cfg.H, cfg.I, E, cfg.topk, True, dev)
+        y = torch.empty(T, cfg.H, dtype=torch.bfloat16, device=dev)
         for i in range(a.iters):
-            x = workloads.activations(cfg.T, cfg.H, seed=700_000 + i, device=dev, outliers=True)
+            x = workloads.activations(T, cfg.H, seed=700_000 + i, device=dev, outliers=True)
             ids, w = workloads.routing(sub, seed=800_000 + i, device=dev)
             ops.moe_forward(x, ids, w, W, a2, workspace=ws, out=y)
     elif a.case == "decode":

@@ -310,6 +310,32 @@ def test_moe_one_token_repeated_ids(ids_row, shared):
     run_moe_check(x, ids, w, W, oe, [0], shared)
 
 
+def test_moe_one_token_dirty_workspace():
+    """One token on a workspace full of stale bytes: the routing zeroes the fp32 accumulator
+    that the one-token launch adds into, so two calls in a row on the same workspace give the
+    zeroed workspace's y."""
+    H, I, E, k = 512, 128, 8, 4
+    W = model.make_moe_weights(E, H, I, 161, DEV, shared=True)
+    x = workloads.activations(1, H, seed=162, device=DEV)
+    ids = torch.tensor([[2, 7, 0, 5]], dtype=torch.int32, device=DEV)
+    w = torch.softmax(torch.randn(1, k, generator=torch.Generator().manual_seed(163)), -1).to(DEV)
+    a2 = torch.full((E + 1,), 0.01, device=DEV)
+    L = ops.moe_workspace_layout(1, H, I, E, k, True)
+    y0, _ = ops.moe_forward(x, ids, w, W, a2, workspace=torch.zeros(L.total, dtype=torch.uint8, device=DEV))
+    torch.cuda.synchronize()
+    assert ops.device_error() == (0, 0)
+    assert float(y0.float().abs().max()) > 0
+    ws = torch.full((L.total,), 0xFF, dtype=torch.uint8, device=DEV)
+    y = torch.empty(1, H, dtype=torch.bfloat16, device=DEV)
+    for _ in range(2):
+        y.fill_(float("nan"))
+        ops.moe_forward(x, ids, w, W, a2, workspace=ws, out=y)
+        torch.cuda.synchronize()
+        assert ops.device_error() == (0, 0)
+        assert bool(torch.isfinite(y.float()).all())
+        np.testing.assert_allclose(bf16_to_np(y), bf16_to_np(y0), rtol=1e-2, atol=1e-3 * float(y0.float().abs().max()))
+
+
 def test_moe_one_token_static_gs_and_bad_id():
     """One token: a static a1 scale equal to the dynamic one gives the same re-quantised rows; an
     out-of-range id is dropped (the routing flags it) and the w13 schedule drops it too."""
