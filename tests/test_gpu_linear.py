@@ -61,13 +61,14 @@ def test_linear_pair_tiles_ragged(M, K, N):
 
 
 @pytest.mark.parametrize("M,K,N", [(10, 1536, 256), (11, 1536, 256), (4, 4096, 384), (1, 4096, 128), (1, 4160, 128),
-                                   (2, 64, 1024), (2, 256, 20480), (3, 768, 512), (7, 320, 256), (32, 512, 384)])
+                                   (2, 64, 1024), (2, 256, 20480), (2, 1536, 19584), (3, 768, 512), (7, 320, 256),
+                                   (32, 512, 384)])
 def test_linear_fused_quantisation_edges(M, K, N):
     """Small M: the GEMM CTAs quantise x themselves (up to 16K elements, K <= 4096, every K stage
     resident); just beyond those limits the separate quantise launch runs.  Both give the same
-    result and the same dynamic gs.  N = 20480 has more tiles (160) than SMs, so CTAs reuse
-    their resident A for a second tile.  The K stages go round-robin to four MMA issuers, an
-    accumulator each: K = 64, 256, 320 and 768 leave some of them without a stage (K = 320 ends
+    result and the same dynamic gs.  N = 20480 and 19584 have more tiles (160, 153) than SMs, so
+    CTAs reuse their resident A for a second tile (one K stage, six K stages).  The K stages go
+    round-robin to four MMA issuers, an accumulator each: K = 64, 256, 320 and 768 leave some of them without a stage (K = 320 ends
     in a one-step stage); M = 32 fills every token column of the accumulators."""
     x = workloads.activations(M, K, seed=M * 31 + K, device="cpu", outliers=True)
     wp, sfp, ws2, wq = _weights(N, K, seed=M + N)
