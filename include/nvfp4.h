@@ -42,8 +42,9 @@
  *    nvfp4_last_error_string().  Faults detected on the device (an expert id
  *    out of range, a pipeline wait that timed out) set a per-device flag word
  *    that nvfp4_get_device_error reads.
- *  - Shape rules: K % 64 == 0, GEMM output widths N % 128 == 0; all pointers
- *    16-byte aligned; bf16 row strides a multiple of 8 elements.  Violations
+ *  - Shape rules: K % 64 == 0; GEMM output widths N % 16 == 0 for the dense
+ *    linear and GEMM, N % 128 == 0 for the grouped linear and the MoE; all
+ *    pointers 16-byte aligned; bf16 row strides a multiple of 8 elements.  Violations
  *    return NVFP4_ERR_UNSUPPORTED_SHAPE or NVFP4_ERR_MISALIGNED.
  */
 #ifndef NVFP4_GB300_H
@@ -68,7 +69,7 @@ extern "C" {
 typedef enum nvfp4_status {
   NVFP4_OK = 0,
   NVFP4_ERR_INVALID_ARG = 1,         /* null pointer, negative size, bad enum value     */
-  NVFP4_ERR_UNSUPPORTED_SHAPE = 2,   /* K % 64, N % 128, E or topk out of range         */
+  NVFP4_ERR_UNSUPPORTED_SHAPE = 2,   /* K % 64, N % 16 / 128, E or topk out of range    */
   NVFP4_ERR_MISALIGNED = 3,          /* a pointer not 16-byte aligned, bad row stride   */
   NVFP4_ERR_WORKSPACE = 4,           /* ws_bytes below the size the query returns       */
   NVFP4_ERR_CUDA = 5,                /* a CUDA runtime call or launch failed            */
@@ -155,7 +156,10 @@ NVFP4_API nvfp4_status nvfp4_rmsnorm_quantize(const void *x, int64_t M, int64_t 
  * 128 r of the 16 KiB block); slab bytes past K/2 are zero codes.  A GEMM stage reads one
  * such block.  NVFP4_PREP_W13_INTERLEAVE reorders the rows of a fused gate/up projection so
  * that every 128-row tile holds 64 gate rows followed by the 64 matching up rows.
- * K % 64 == 0, N % 128 == 0.  Run once at load time; w and w_out must not overlap.
+ * K % 64 == 0, N % 128 == 0; with G == 1 and no interleave N % 16 == 0 suffices, the
+ * last tile's rows from N on then being zero codes and zero scales (sf_out holds
+ * nvfp4_sf_bytes(N, K) bytes, which covers them).  Run once at load time; w and w_out
+ * must not overlap.
  * Every w / w13 / w2 / sh_* weight argument below is such a prepared buffer. */
 NVFP4_API size_t nvfp4_prepared_weight_bytes(int64_t G, int64_t N, int64_t K);
 NVFP4_API nvfp4_status nvfp4_prepare_weights(const uint8_t *w, const uint8_t *sf, int64_t G, int64_t N,
@@ -167,7 +171,9 @@ NVFP4_API nvfp4_status nvfp4_prepare_weights(const uint8_t *w, const uint8_t *sf
  * x (M, K) bf16 quantised at run time (gs_mode as for nvfp4_quantize_act,
  * *gs written in dynamic mode) and W is a prepared (N, K/2) + swizzled sf
  * weight with device scalar ws2 (Nvfp4Linear, page 2: the ws2-folding fixes).
- * K % 64 == 0, N % 128 == 0.  Workspace: quantised x + scales + partials. */
+ * K % 64 == 0, N % 16 == 0 (an N that is not a multiple of 128 ends in a partial tile of
+ * the prepared weight; only the first N output columns are written).  Workspace:
+ * quantised x + scales + partials. */
 NVFP4_API size_t nvfp4_linear_workspace_bytes(int64_t M, int64_t K);
 NVFP4_API nvfp4_status nvfp4_linear(const void *x, int64_t M, int64_t K, int64_t N, const uint8_t *w,
                           const uint8_t *w_sf, const float *ws2, int gs_mode, float *gs, void *y,

@@ -519,9 +519,14 @@ nvfp4_status nvfp4_rmsnorm_quantize(const void *x, int64_t M, int64_t K, int64_t
   return NVFP4_OK;
 }
 
+// Output widths: a multiple of 128, or of 16 for one group (the dense linear), whose last
+// 128-row weight tile is then padded with zero rows.
+static bool weight_rows_ok(int64_t G, int64_t N) { return N % 128 == 0 || (G == 1 && N % 16 == 0); }
+
 size_t nvfp4_prepared_weight_bytes(int64_t G, int64_t N, int64_t K) {
-  if (G <= 0 || N <= 0 || K <= 0 || K % 64 || N % 128) return 0;
-  return static_cast<size_t>(G) * static_cast<size_t>(N) * static_cast<size_t>((K / 2 + 127) / 128) * 128u;
+  if (G <= 0 || N <= 0 || K <= 0 || K % 64 || !weight_rows_ok(G, N)) return 0;
+  return static_cast<size_t>(G) * static_cast<size_t>(round_up(N, 128)) * static_cast<size_t>((K / 2 + 127) / 128) *
+         128u;
 }
 
 nvfp4_status nvfp4_prepare_weights(const uint8_t *w, const uint8_t *sf, int64_t G, int64_t N, int64_t K, int flags,
@@ -531,8 +536,10 @@ nvfp4_status nvfp4_prepare_weights(const uint8_t *w, const uint8_t *sf, int64_t 
              (long long)K);
   NV_REQUIRE(flags == NVFP4_PREP_PLAIN || flags == NVFP4_PREP_W13_INTERLEAVE, NVFP4_ERR_INVALID_ARG, "flags %d",
              flags);
-  NV_REQUIRE(K % 64 == 0 && N % 128 == 0, NVFP4_ERR_UNSUPPORTED_SHAPE,
-             "K=%lld must be a multiple of 64 and N=%lld of 128", (long long)K, (long long)N);
+  NV_REQUIRE(K % 64 == 0 && weight_rows_ok(G, N) && (N % 128 == 0 || flags == NVFP4_PREP_PLAIN),
+             NVFP4_ERR_UNSUPPORTED_SHAPE,
+             "K=%lld must be a multiple of 64 and N=%lld of 128 (of 16 for one group without the w13 interleave)",
+             (long long)K, (long long)N);
   NV_REQUIRE(aligned(w, 16) && aligned(sf, 16) && aligned(w_out, 16) && aligned(sf_out, 16), NVFP4_ERR_MISALIGNED,
              "pointers must be 16-byte aligned");
   NV_REQUIRE(w != w_out && sf != sf_out, NVFP4_ERR_INVALID_ARG, "prepare cannot run in place");
@@ -564,7 +571,7 @@ static nvfp4_status gemm_dense(const char *fn, DeviceInfo *d, const uint8_t *xq,
   CUtensorMap ta, tb;
   nvfp4_status st = make_map(fn, &ta, xq, G * K / 2, M, G * K / 2, pair_clusters > 0 ? 128 : kABoxRows);
   if (st != NVFP4_OK) return st;
-  if ((st = make_weight_map(fn, &tb, w, G * N, K)) != NVFP4_OK) return st;
+  if ((st = make_weight_map(fn, &tb, w, G * round_up(N, kBlockN), K)) != NVFP4_OK) return st;
   GemmArgs a;
   std::memset(&a, 0, sizeof(a));
   a.G = static_cast<int>(G);
@@ -590,7 +597,7 @@ static nvfp4_status gemm_dense(const char *fn, DeviceInfo *d, const uint8_t *xq,
     NV_CUDA(launch_gemm_pair(ta, tb, a, clusters, s), "pair GEMM launch");
     return NVFP4_OK;
   }
-  const int64_t tiles = G * ((M + kBlockM - 1) / kBlockM) * (N / kBlockN);
+  const int64_t tiles = G * ((M + kBlockM - 1) / kBlockM) * ((N + kBlockN - 1) / kBlockN);
   const int grid = static_cast<int>(tiles < d->sms * kCtasPerSm ? tiles : d->sms * kCtasPerSm);
   // M <= 32: every tile has at most one 32-row A box, so the ring with 4 small stages applies
   NV_CUDA(launch_gemm(Epi::kLinear, ta, tb, tb, a, grid, grid <= d->sms, M <= kABoxRows, s), "GEMM launch");
@@ -604,7 +611,7 @@ static nvfp4_status linear_fused(const char *fn, DeviceInfo *d, const void *x, i
                                  int64_t N, const uint8_t *w, const uint8_t *w_sf, const float *ws2, bool dyn,
                                  float *gs, void *y, cudaStream_t s) {
   CUtensorMap tb;
-  nvfp4_status st = make_weight_map(fn, &tb, w, G * N, K);
+  nvfp4_status st = make_weight_map(fn, &tb, w, G * round_up(N, kBlockN), K);
   if (st != NVFP4_OK) return st;
   GemmArgs a;
   std::memset(&a, 0, sizeof(a));
@@ -625,7 +632,7 @@ static nvfp4_status linear_fused(const char *fn, DeviceInfo *d, const void *x, i
   a.qa_ld = G * K;
   a.qa_gs_static = dyn ? nullptr : gs;
   a.qa_gs_out = dyn ? gs : nullptr;
-  const int64_t tiles = G * (N / kBlockN);
+  const int64_t tiles = G * ((N + kBlockN - 1) / kBlockN);
   // a dense linear's CTAs may take several tiles (all of group 0); groups need one tile per CTA
   const int grid = static_cast<int>(tiles < d->sms ? tiles : d->sms);
   NV_CUDA(launch_gemm_quant_a(tb, a, grid, s), "fused linear launch");
@@ -634,14 +641,14 @@ static nvfp4_status linear_fused(const char *fn, DeviceInfo *d, const void *x, i
 
 static bool linear_fusable(const DeviceInfo *d, int64_t M, int64_t G, int64_t K, int64_t N) {
   return M >= 1 && M <= kABoxRows && K <= kQuantMaxK && M * K <= kQuantMaxElems &&
-         M * G * K <= 4 * kQuantMaxElems && (G == 1 || G * (N / kBlockN) <= d->sms);
+         M * G * K <= 4 * kQuantMaxElems && (G == 1 || G * ((N + kBlockN - 1) / kBlockN) <= d->sms);
 }
 
 #define NV_CHECK_GEMM_SHAPE(M, K, N)                                                                          \
   NV_REQUIRE((M) >= 0 && (K) > 0 && (N) > 0, NVFP4_ERR_INVALID_ARG, "M=%lld K=%lld N=%lld", (long long)(M),    \
              (long long)(K), (long long)(N));                                                                  \
-  NV_REQUIRE((K) % 64 == 0 && (N) % 128 == 0, NVFP4_ERR_UNSUPPORTED_SHAPE,                                    \
-             "K=%lld must be a multiple of 64 and N=%lld of 128", (long long)(K), (long long)(N));              \
+  NV_REQUIRE((K) % 64 == 0 && (N) % 16 == 0, NVFP4_ERR_UNSUPPORTED_SHAPE,                                     \
+             "K=%lld must be a multiple of 64 and N=%lld of 16", (long long)(K), (long long)(N));               \
   NV_REQUIRE((M) < (int64_t(1) << 30) && (N) < (int64_t(1) << 30) && (K) < (int64_t(1) << 24),              \
              NVFP4_ERR_UNSUPPORTED_SHAPE, "sizes too large")
 

@@ -346,7 +346,7 @@ __global__ void __launch_bounds__(Ring<kSmallA, kQuantA, kQuantA && kEpi == stat
   }
   auto entry = [&](int mtg) { return kTok1 ? sched[mtg] : tile_entry(args, mtg); };
 
-  const int n_tiles = args.N / kBlockN;
+  const int n_tiles = (args.N + kBlockN - 1) / kBlockN;  // (a dense linear's N may end mid-tile)
   const int k_steps = args.K / kUmmaK;
   const int k_stages = (k_steps + 3) / 4;
   const int total_mtiles = kTok1 ? sched[15].x
@@ -968,6 +968,8 @@ __global__ void __launch_bounds__(Ring<kSmallA, kQuantA, kQuantA && kEpi == stat
         const int64_t ld = args.out_ld;
         __nv_bfloat16 *y = static_cast<__nv_bfloat16 *>(args.out) + static_cast<int64_t>(t.a_row0) * ld +
                            static_cast<int64_t>(t.g) * args.out_group_cols + t.nt * kBlockN + m;
+        // features past N (a dense linear's last tile when N % 128 != 0) are padding
+        const bool col_ok = t.nt * kBlockN + m < args.out_group_cols;
         if (t.rows <= 0) release();
 #pragma unroll 1
         for (int c0 = 0; c0 < t.rows; c0 += 16) {
@@ -985,9 +987,10 @@ __global__ void __launch_bounds__(Ring<kSmallA, kQuantA, kQuantA && kEpi == stat
             if (i < nacc)
 #pragma unroll
               for (int q = 0; q < 16; ++q) v[q] += __uint_as_float(r[i][q]);
+          if (col_ok)
 #pragma unroll
-          for (int q = 0; q < 16; ++q)
-            if (c0 + q < t.rows) y[(c0 + q) * ld] = __float2bfloat16_rn(v[q] * alpha);
+            for (int q = 0; q < 16; ++q)
+              if (c0 + q < t.rows) y[(c0 + q) * ld] = __float2bfloat16_rn(v[q] * alpha);
         }
       } else if constexpr (kEpi == static_cast<int>(Epi::kLinear)) {
         const float alpha = gs_scalar * ws2;
@@ -996,6 +999,7 @@ __global__ void __launch_bounds__(Ring<kSmallA, kQuantA, kQuantA && kEpi == stat
         __nv_bfloat16 *y = static_cast<__nv_bfloat16 *>(args.out) +
                            row * static_cast<int64_t>(args.out_ld) +
                            static_cast<int64_t>(t.g) * args.out_group_cols + t.nt * kBlockN;
+        const int n_chunks = min(kBlockN, args.out_group_cols - t.nt * kBlockN) / 16;  // 16-column chunks left of N
         // four TMEM loads in flight per wait
 #pragma unroll 1
         for (int c0 = 0; c0 < kBlockN / 16; c0 += 4) {
@@ -1008,6 +1012,7 @@ __global__ void __launch_bounds__(Ring<kSmallA, kQuantA, kQuantA && kEpi == stat
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
               const int c = c0 + q;
+              if (c >= n_chunks) break;  // a dense linear's last tile may end at N % 128 != 0
               uint32_t packed[8];
 #pragma unroll
               for (int i = 0; i < 8; ++i) {
@@ -1016,7 +1021,7 @@ __global__ void __launch_bounds__(Ring<kSmallA, kQuantA, kQuantA && kEpi == stat
                 packed[i] = *reinterpret_cast<const uint32_t *>(&v);
               }
               // 32 bytes per row and chunk: one 256-bit store when the output is 32-byte
-              // aligned (row strides and column offsets are multiples of 256 bytes)
+              // aligned (row strides and column offsets are multiples of 32 bytes)
               if (out32) {
                 st_global_v8(y + c * 16, packed);
               } else {

@@ -190,9 +190,9 @@ __global__ void prepare_kernel(const uint8_t *__restrict__ w, const uint8_t *__r
   pdl_wait();
   const int64_t row_bytes = K / 2;                // a multiple of 32 (K % 64 == 0)
   const int64_t slabs = (row_bytes + 127) / 128;  // 128-byte column slabs per row
-  const int64_t tiles = N / 128;
+  const int64_t tiles = (N + 127) / 128;          // (one group with N % 128 != 0: rows from N on are zero)
   const int64_t code_items = G * tiles * slabs * 1024;  // 16-byte chunks of the tile-major blocks
-  const int64_t words_per_group = N * K / 64;     // 4 scales per word
+  const int64_t words_per_group = tiles * 128 * K / 64;  // 4 scales per word
   const int64_t total = code_items + G * words_per_group;
   const int64_t kb = K / 16, kc4 = K / 64;
   for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
@@ -202,10 +202,11 @@ __global__ void prepare_kernel(const uint8_t *__restrict__ w, const uint8_t *__r
       const int64_t r = within >> 3, c16 = within & 7;
       const int64_t tile = blk / slabs, s = blk - tile * slabs;
       const int64_t g = tile / tiles, nt = tile - g * tiles;
-      const int64_t src = g * N + interleave_src_row(nt * 128 + r, N, flags);
+      const int64_t n = nt * 128 + r;
+      const int64_t src = g * N + interleave_src_row(n, N, flags);
       const int64_t byte = s * 128 + c16 * 16;
-      const uint4 v = byte < row_bytes ? __ldg(reinterpret_cast<const uint4 *>(w + src * row_bytes + byte))
-                                       : make_uint4(0u, 0u, 0u, 0u);
+      const uint4 v = byte < row_bytes && n < N ? __ldg(reinterpret_cast<const uint4 *>(w + src * row_bytes + byte))
+                                                : make_uint4(0u, 0u, 0u, 0u);
       reinterpret_cast<uint4 *>(w_out)[i] = v;
     } else {
       const int64_t j = i - code_items;
@@ -214,8 +215,8 @@ __global__ void prepare_kernel(const uint8_t *__restrict__ w, const uint8_t *__r
       const int64_t rb = blk / kc4, cb = blk - rb * kc4;
       const int64_t r = rb * 128 + (within & 3) * 32 + (within >> 2);
       const int64_t src = g * N + interleave_src_row(r, N, flags);
-      const uint32_t word = __ldg(reinterpret_cast<const uint32_t *>(sf + src * kb + cb * 4));
-      reinterpret_cast<uint32_t *>(sf_out + g * (N * kb))[wi] = word;
+      const uint32_t word = r < N ? __ldg(reinterpret_cast<const uint32_t *>(sf + src * kb + cb * 4)) : 0u;
+      reinterpret_cast<uint32_t *>(sf_out + g * (tiles * 128 * kb))[wi] = word;
     }
   }
 }

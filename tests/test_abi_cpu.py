@@ -66,6 +66,8 @@ def test_linear_and_moe_reject_bad_shapes(L):
     assert L.nvfp4_linear(p, 4, 96, 128, p, p, p, 0, p, p, p, 1 << 20, None) == _lib.ERR_UNSUPPORTED_SHAPE
     assert L.nvfp4_linear(p, 4, 64, 128, p, p, p, 0, p, p, p, 16, None) == _lib.ERR_WORKSPACE
     assert L.nvfp4_gemm(p, p, p, 4, 64, 128, None, p, p, p, None) == _lib.ERR_INVALID_ARG
+    assert L.nvfp4_gemm(p, p, p, 4, 64, 136, p, p, p, p, None) == _lib.ERR_UNSUPPORTED_SHAPE   # N % 16
+    assert L.nvfp4_grouped_linear(p, 4, 2, 64, 144, p, p, p, 0, p, p, p, 1 << 20, None) == _lib.ERR_UNSUPPORTED_SHAPE
     assert L.nvfp4_moe_workspace_bytes(16, 250, 128, 8, 2, 0) == 0       # H % 128
     assert L.nvfp4_moe_workspace_bytes(16, 256, 100, 8, 2, 0) == 0       # I % 64
     assert L.nvfp4_moe_workspace_bytes(16, 256, 128, 2000, 2, 0) == 0    # E too large
@@ -78,6 +80,22 @@ def test_linear_and_moe_reject_bad_shapes(L):
     assert L.nvfp4_moe_forward(p, 16, 256, 128, 8, 2, p, p, p, p, p, p, p, p, None, None, p, None, None, 0, p, p,
                                p, p, n, None) == _lib.ERR_INVALID_ARG  # sh_w2 without sh_w13
     assert L.nvfp4_debug_wait_timeout(0, None) == _lib.ERR_INVALID_ARG
+
+
+def test_prepared_weight_sizes_and_partial_tiles(L):
+    """Prepared codes are whole 128-row tiles of 128-byte slabs: N % 16 is enough for one group
+    (the last tile padded), the grouped layouts and the w13 interleave keep N % 128."""
+    assert L.nvfp4_prepared_weight_bytes(1, 256, 256) == 256 * 128
+    assert L.nvfp4_prepared_weight_bytes(1, 144, 256) == 256 * 128      # 144 rows -> two tiles
+    assert L.nvfp4_prepared_weight_bytes(1, 16, 7168) == 128 * 28 * 128
+    assert L.nvfp4_prepared_weight_bytes(3, 128, 320) == 3 * 128 * 2 * 128  # K/2 = 160 bytes -> two slabs
+    assert L.nvfp4_prepared_weight_bytes(2, 144, 256) == 0
+    assert L.nvfp4_prepared_weight_bytes(1, 100, 256) == 0
+    p = 1 << 20
+    assert L.nvfp4_prepare_weights(p, p, 1, 144, 256, _lib.PREP_W13_INTERLEAVE, p + 4096, p + 8192,
+                                   None) == _lib.ERR_UNSUPPORTED_SHAPE
+    assert L.nvfp4_prepare_weights(p, p, 2, 144, 256, _lib.PREP_PLAIN, p + 4096, p + 8192,
+                                   None) == _lib.ERR_UNSUPPORTED_SHAPE
 
 
 def test_valid_call_without_a_gpu_fails_cleanly(L):

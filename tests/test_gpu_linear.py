@@ -36,6 +36,32 @@ def test_linear_ragged_shapes(M, K, N):
     assert_parity(bf16_to_np(y), O.linear(xq, wq.codes, wq.sf, wq.gs), what=f"linear {M}x{K}x{N}")
 
 
+@pytest.mark.parametrize("M,K,N", [(1, 256, 16), (5, 512, 144), (32, 128, 400), (3, 4160, 144), (48, 256, 1936),
+                                   (130, 1536, 272), (600, 320, 400)])
+def test_linear_output_width_multiple_of_16(M, K, N):
+    """N % 16 == 0 but not % 128: the prepared weight ends in a partial 128-row tile (zero codes
+    and scales from row N on) and only the first N output columns are written.  The fused path
+    (M <= 32, small K), the small-A ring (K > 4096), the 128-row tiles (M = 48, 130) and M >= 512,
+    where N % 256 != 0 keeps the one-SM tiles; through nvfp4_linear and nvfp4_gemm, every output
+    checked, and nothing written past the output."""
+    x = workloads.activations(M, K, seed=M + 5 * K + N, device="cpu", outliers=True)
+    wp, sfp, ws2, wq = _weights(N, K, seed=M + 3 * N)
+    assert wp.numel() == (N + 127) // 128 * 128 * ((K // 2 + 127) // 128) * 128
+    xd = x.to(DEV)
+    y, gs = ops.linear(xd, wp, sfp, ws2, N)
+    q, sf, gq = ops.quantize_act(xd)
+    sentinel = torch.full((M * N + 512,), -7.0, dtype=torch.bfloat16, device=DEV)
+    y2 = ops.gemm(q, sf, gq, K, wp, sfp, ws2, N, out=sentinel[:M * N].view(M, N))
+    torch.cuda.synchronize()
+    assert ops.device_error() == (0, 0)
+    assert bool((sentinel[M * N:] == -7.0).all())
+    xq = O.quantize(x.float().numpy())
+    assert gs.item() == float(xq.gs)
+    ref = O.linear(xq, wq.codes, wq.sf, wq.gs)
+    assert_parity(bf16_to_np(y), ref, what=f"linear {M}x{K}x{N}")
+    assert_parity(bf16_to_np(y2), ref, what=f"gemm {M}x{K}x{N}")
+
+
 @pytest.mark.parametrize("M,K,N", [(512, 256, 256), (700, 320, 512), (640, 1536, 768), (1000, 64, 256),
                                    (1300, 7168, 512), (2049, 512, 1024), (10240, 704, 512)])
 def test_linear_pair_tiles_ragged(M, K, N):
