@@ -117,7 +117,7 @@ enum class Epi : int { kLinear = 0, kW13 = 1, kW2 = 2 };
 struct GemmArgs {
   // problem
   int G;              // groups (1 for a dense GEMM)
-  int N;              // output width per group, multiple of 128
+  int N;              // output width per group: a multiple of 128 (of 16 for one group, last tile partial)
   int K;              // reduction length, multiple of 64
   int dense_M;        // rows of every group when counts == nullptr (dense / uniform groups)
   // grouped segments (device arrays written by the routing kernel)
